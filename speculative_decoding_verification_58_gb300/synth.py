@@ -1,0 +1,200 @@
+"""Seeded synthetic verification inputs, shared by the tests, the benchmark and the smoke check.
+
+This module only draws random numbers: it holds none of the verification
+arithmetic (no softmax, no ratio, no residual).  Draft tokens stand for the
+drafter's own samples and are drawn with the Gumbel-max trick,
+``argmax(z_d + T * G)`` with ``G`` standard Gumbel, which samples
+``softmax(z_d / T)`` without normalising anything; at ``T == 0`` the draft
+token is ``argmax(z_d)``.
+
+Workloads mimic the pages' serving setting: Qwen3-sized vocabularies
+(V = 151936), blocks of k = 16 draft tokens (AdaFlash Appendix B.1), batch
+concurrency 1-128 (AdaFlash Table 1), per-request verification lengths
+1 <= L_b <= k (AdaFlash Section 3.2) and acceptance that decays with the
+draft position (AdaFlash reading notes, Figure 2c discussion).  No dataset or
+trained weight is involved.
+
+Recipes (logits generated in fp32, rounded to nearest-even bf16 where the
+workload is bf16):
+
+``gauss``            target ~ N(0, 2^2) i.i.d.; draft = target + N(0, 0.5^2).
+``zipf``             target = N(0, 1) - 1.1 * log(rank + 1), rank from one seeded
+                     vocabulary permutation per request (shared by all of its
+                     target and draft rows); draft = target + N(0, 1).
+``zipf_adaptive``    ``zipf`` with L_b ~ U{1..k} and T_b ~ U[0.6, 1.0].
+``zipf_mixed_noise`` ``zipf`` target; a seeded half of the requests draws draft
+                     noise sigma_b = 0.3 and the other half 2.0, growing by 1.08x
+                     per position (sigma_b * 1.08^i); L_b ~ U{min(4,k)..k}; T = 1.
+``zipf_mixed_temp``  ``zipf_mixed_noise`` logits; a seeded quarter of the requests
+                     is greedy (T = 0), the rest T_b ~ U[0.5, 1.2]; L_b ~ U{1..k}.
+
+Uniforms are ``(uint32 >> 8) * 2^-24``, strictly inside [0, 1).
+
+Every request draws from its own child of ``numpy.random.SeedSequence(seed)``,
+so the result is the same for any thread count.
+"""
+
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass
+
+import numpy as np
+
+RECIPES = ("gauss", "zipf", "zipf_adaptive", "zipf_mixed_noise", "zipf_mixed_temp")
+
+# The five workloads the library is measured and checked on, named by what they are.
+WORKLOADS = {
+    "b1_k4_v1024_f32_gauss": dict(recipe="gauss", B=1, k=4, V=1024, dtype="f32", seed=20260001),
+    "b1_k16_v151936_bf16_zipf": dict(recipe="zipf", B=1, k=16, V=151936, dtype="bf16",
+                                     seed=20260002),
+    "b32_k16_v151936_bf16_zipf_adaptive": dict(recipe="zipf_adaptive", B=32, k=16, V=151936,
+                                               dtype="bf16", seed=20260003),
+    "b128_k16_v151936_bf16_zipf_mixed_noise": dict(recipe="zipf_mixed_noise", B=128, k=16,
+                                                   V=151936, dtype="bf16", seed=20260004),
+    "b256_k16_v151936_f32_zipf_mixed_temp": dict(recipe="zipf_mixed_temp", B=256, k=16,
+                                                 V=151936, dtype="f32", seed=20260005),
+}
+
+HEADLINE = "b128_k16_v151936_bf16_zipf_mixed_noise"
+
+
+@dataclass
+class SpecInputs:
+    """Host arrays laid out exactly like the C-ABI's buffers."""
+
+    target: np.ndarray       # [B, k+1, V] float32, or uint16 holding bf16 bits
+    draft: np.ndarray        # [B, k, V]   same dtype as target
+    tokens: np.ndarray       # [B, k]   int32
+    lengths: np.ndarray      # [B]      int32
+    uniforms: np.ndarray     # [B, k+1] float32 in [0, 1)
+    temperature: np.ndarray  # [B]      float32, 0 = greedy
+    dtype: str               # "f32" or "bf16"
+
+    @property
+    def B(self) -> int:
+        return self.target.shape[0]
+
+    @property
+    def k(self) -> int:
+        return self.draft.shape[1]
+
+    @property
+    def V(self) -> int:
+        return self.target.shape[2]
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round finite float32 values to the nearest bf16 (ties to even); return the raw bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounded = u + (np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))
+    return (rounded >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen raw bf16 bits to float32 (exact)."""
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def uniform_24bit(rng: np.random.Generator, shape) -> np.ndarray:
+    """Uniforms (uint32 >> 8) * 2^-24: 24-bit float32 values strictly inside [0, 1)."""
+    bits = rng.integers(0, 2**32, size=shape, dtype=np.uint64).astype(np.uint32)
+    return ((bits >> np.uint32(8)).astype(np.float32) * np.float32(2.0**-24)).astype(np.float32)
+
+
+def _zipf_table(V: int) -> np.ndarray:
+    return (-1.1 * np.log(np.arange(V, dtype=np.float64) + 1.0)).astype(np.float32)
+
+
+def make_inputs(recipe: str, B: int, k: int, V: int, dtype: str, seed: int,
+                threads: int | None = None) -> SpecInputs:
+    """Generate one batch of verification inputs for ``recipe`` (see module docstring)."""
+    if recipe not in RECIPES:
+        raise ValueError(f"unknown recipe {recipe!r}")
+    if dtype not in ("f32", "bf16"):
+        raise ValueError("dtype must be 'f32' or 'bf16'")
+    if B < 1 or k < 1 or V < 1:
+        raise ValueError("B, k and V must be positive")
+
+    ss = np.random.SeedSequence(seed)
+    batch_seq, *req_seqs = ss.spawn(B + 1)
+    brng = np.random.default_rng(batch_seq)
+
+    # Per-request scalars: verification length, temperature, draft noise scale.
+    if recipe in ("gauss", "zipf"):
+        lengths = np.full(B, k, np.int32)
+        temps = np.ones(B, np.float32)
+    elif recipe == "zipf_adaptive":
+        lengths = brng.integers(1, k + 1, size=B).astype(np.int32)
+        temps = brng.uniform(0.6, 1.0, size=B).astype(np.float32)
+    elif recipe == "zipf_mixed_noise":
+        lengths = brng.integers(min(4, k), k + 1, size=B).astype(np.int32)
+        temps = np.ones(B, np.float32)
+    else:  # zipf_mixed_temp
+        lengths = brng.integers(1, k + 1, size=B).astype(np.int32)
+        temps = brng.uniform(0.5, 1.2, size=B).astype(np.float32)
+        greedy = brng.permutation(B)[: B // 4]
+        temps[greedy] = 0.0
+
+    if recipe in ("zipf_mixed_noise", "zipf_mixed_temp"):
+        sigma = np.full(B, 2.0)
+        sigma[brng.permutation(B)[: B // 2]] = 0.3
+        sigma_pos = sigma[:, None] * (1.08 ** np.arange(k))[None, :]
+    elif recipe == "gauss":
+        sigma_pos = np.full((B, k), 0.5)
+    else:
+        sigma_pos = np.full((B, k), 1.0)
+
+    uniforms = uniform_24bit(brng, (B, k + 1))
+
+    store = np.uint16 if dtype == "bf16" else np.float32
+    target = np.empty((B, k + 1, V), store)
+    draft = np.empty((B, k, V), store)
+    tokens = np.empty((B, k), np.int32)
+    zipf = _zipf_table(V) if recipe != "gauss" else None
+
+    def one_request(b: int) -> None:
+        rng = np.random.default_rng(req_seqs[b])
+        if recipe == "gauss":
+            zt = rng.standard_normal((k + 1, V), dtype=np.float32) * np.float32(2.0)
+        else:
+            zt = rng.standard_normal((k + 1, V), dtype=np.float32)
+            zt += rng.permutation(zipf)[None, :]
+        zd = zt[:k] + rng.standard_normal((k, V), dtype=np.float32) * \
+            sigma_pos[b].astype(np.float32)[:, None]
+        if dtype == "bf16":
+            target[b] = bf16_bits(zt)
+            draft[b] = bf16_bits(zd)
+            zd_stored = bf16_to_f32(draft[b])
+        else:
+            target[b] = zt
+            draft[b] = zd
+            zd_stored = zd
+        T = float(temps[b])
+        if T == 0.0:
+            tokens[b] = np.argmax(zd_stored, axis=1)
+        else:
+            g = rng.gumbel(size=(k, V))
+            tokens[b] = np.argmax(zd_stored.astype(np.float64) + T * g, axis=1)
+
+    n_threads = threads or min(16, os.cpu_count() or 1, B)
+    if n_threads <= 1:
+        for b in range(B):
+            one_request(b)
+    else:
+        with ThreadPoolExecutor(n_threads) as pool:
+            list(pool.map(one_request, range(B)))
+
+    return SpecInputs(target, draft, tokens, lengths, uniforms, temps, dtype)
+
+
+def make_workload(name: str, seed: int | None = None, threads: int | None = None,
+                  **overrides) -> SpecInputs:
+    """Inputs of one named workload; ``overrides`` may shrink B, k or V for fast checks."""
+    cfg = dict(WORKLOADS[name])
+    cfg.update(overrides)
+    if seed is not None:
+        cfg["seed"] = seed
+    return make_inputs(cfg["recipe"], cfg["B"], cfg["k"], cfg["V"], cfg["dtype"], cfg["seed"],
+                       threads=threads)
