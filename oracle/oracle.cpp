@@ -6,6 +6,7 @@
 
 #include "oracle.h"
 
+#include <cfloat>
 #include <cmath>
 #include <cstring>
 #include <limits>
@@ -54,6 +55,7 @@ void row_argmax(const Row& r, double* max_out, int* arg_out) {
 struct Softmax {
   double M;
   double logS;
+  bool ok;  // the row has finite, positive mass (no NaN / +inf, not all -inf)
 };
 
 Softmax row_softmax(const Row& r, double T) {
@@ -62,7 +64,7 @@ Softmax row_softmax(const Row& r, double T) {
   row_argmax(r, &M, &arg);
   double S = 0.0;
   for (int v = 0; v < r.V; ++v) S += std::exp((r.z(v) - M) / T);
-  return Softmax{M, std::log(S)};
+  return Softmax{M, std::log(S), S > 0.0 && std::isfinite(S)};
 }
 
 double log_prob(const Row& r, const Softmax& sm, double T, int v) {
@@ -116,10 +118,13 @@ int verify_one(const void* tl, const void* dl, int dtype, const int32_t* tok, in
   *residual_zero = 0;
 
   // Input checks: the length head's clamp gives 1 <= L <= k; temperature is
-  // 0 (greedy) or finite and positive; tokens index the vocabulary; the
-  // uniforms a sampling request uses lie in [0, 1).
+  // 0 (greedy) or a finite normal float (>= 2^-126, so log2(e)/T stays finite
+  // in single precision); tokens index the vocabulary; the uniforms a
+  // sampling request uses lie in [0, 1).  Rows are checked as they are read:
+  // a row without finite mass makes the request invalid.
   if (L < 1 || L > k) return 1;
   if (!(T >= 0.0) || std::isinf(T)) return 1;
+  if (T > 0.0 && T < (double)FLT_MIN) return 1;
   for (int i = 0; i < L; ++i)
     if (tok[i] < 0 || tok[i] >= V) return 1;
   if (T > 0.0)
@@ -139,6 +144,7 @@ int verify_one(const void* tl, const void* dl, int dtype, const int32_t* tok, in
       double m;
       int g;
       row_argmax(target_row(i), &m, &g);
+      if (g < 0) return 1;
       if (tok[i] != g) {
         n = i;
         final_token = g;
@@ -148,6 +154,7 @@ int verify_one(const void* tl, const void* dl, int dtype, const int32_t* tok, in
     if (n == L) {
       double m;
       row_argmax(target_row(L), &m, &final_token);
+      if (final_token < 0) return 1;
     }
     for (int i = 0; i < n; ++i) out[i] = tok[i];
     out[n] = final_token;
@@ -162,7 +169,11 @@ int verify_one(const void* tl, const void* dl, int dtype, const int32_t* tok, in
   for (int i = 0; i < L; ++i) {
     Row tr = target_row(i), dr = draft_row(i);
     Softmax ps = row_softmax(tr, T), qs = row_softmax(dr, T);
-    double ratio = std::exp(log_prob(tr, ps, T, tok[i]) - log_prob(dr, qs, T, tok[i]));
+    if (!ps.ok || !qs.ok) return 1;
+    // A token the target gives probability zero is never accepted; one the
+    // drafter gives probability zero (and the target not) always is.
+    double lp = log_prob(tr, ps, T, tok[i]);
+    double ratio = lp == -kInf ? 0.0 : std::exp(lp - log_prob(dr, qs, T, tok[i]));
     double accept_prob = ratio < 1.0 ? ratio : 1.0;
     marg = std::fmin(marg, std::fabs(u[i] - accept_prob));
     if (!(u[i] < accept_prob)) {
@@ -197,6 +208,7 @@ int verify_one(const void* tl, const void* dl, int dtype, const int32_t* tok, in
   } else {
     Row tr = target_row(L);
     Softmax ps = row_softmax(tr, T);
+    if (!ps.ok) return 1;
     for (int v = 0; v < V; ++v) {
       mass[v] = prob(tr, ps, T, v);
       total += mass[v];

@@ -36,7 +36,11 @@
  *    cumulative mass exceeds u * total;
  *  - argmax ties go to the lowest index;
  *  - if the residual mass is exactly zero, the sample is drawn from p;
- *  - temperature == 0 exactly selects the greedy rule; any T > 0 samples.
+ *  - temperature == 0 exactly selects the greedy rule; any T > 0 samples;
+ *  - input domain (the pages state none): T is 0 or a finite normal float;
+ *    a token the target gives probability zero is never accepted; a logit row
+ *    the round reads that has no finite mass (NaN, +inf, or all -inf) makes
+ *    the request invalid.
  */
 #ifndef SPEC_VERIFY_ORACLE_H
 #define SPEC_VERIFY_ORACLE_H

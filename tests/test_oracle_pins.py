@@ -431,3 +431,36 @@ def test_first_rejection_ends_the_round():
                       np.ones(1, np.float32))
     assert r.num_accepted[0] == 0
     assert r.out_tokens[0, 0] != 0 and np.all(r.out_tokens[0, 1:] == -1)
+
+
+def test_token_impossible_under_both_is_rejected():
+    # p(x) = q(x) = 0: the target never emits x, so the draft cannot be kept.
+    V, k = 6, 1
+    tl = np.zeros((1, k + 1, V), np.float32)
+    dl = np.zeros((1, k, V), np.float32)
+    tl[0, 0, 2] = dl[0, 0, 2] = -np.inf
+    r = oracle.verify(tl, dl, np.array([[2]], np.int32), np.array([1], np.int32),
+                      np.zeros((1, k + 1), np.float32), np.ones(1, np.float32))
+    assert r.num_accepted[0] == 0 and r.out_tokens[0, 0] != 2
+
+
+def test_unreadable_rows_invalidate_only_when_reached():
+    V, k = 8, 3
+    rng = np.random.default_rng(6)
+    tl = rng.standard_normal((2, k + 1, V)).astype(np.float32)
+    dl = rng.standard_normal((2, k, V)).astype(np.float32)
+    tl[:, 0, 5] = -np.inf
+    tok = np.full((2, k), 5, np.int32)  # p(x_0) = 0: position 0 always rejects
+    tl[:, 2, 3] = np.nan                # row 2 is never reached
+    dl[1, 0, 1] = np.nan                # ... but request 1's row 0 is
+    r = oracle.verify(tl, dl, tok, np.full(2, k, np.int32), np.full((2, k + 1), 0.5, np.float32),
+                      np.ones(2, np.float32))
+    assert r.num_accepted.tolist() == [0, -1] and r.bad_requests == 1
+
+
+def test_subnormal_temperature_is_invalid():
+    V, k = 4, 1
+    r = oracle.verify(np.zeros((1, k + 1, V), np.float32), np.zeros((1, k, V), np.float32),
+                      np.zeros((1, k), np.int32), np.array([1], np.int32),
+                      np.zeros((1, k + 1), np.float32), np.array([1e-39], np.float32))
+    assert r.num_accepted[0] == -1
