@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Benchmark: batched speculative-decoding verification rounds/s and HBM GB/s on GB300.
+
+One step = one verification round = one ``spec_verify`` call over a whole
+batch (plan -> row sweep -> final pass).  Default workload: B=128 requests,
+k=16 draft positions, V=151936, bf16 logits, half the requests with low and
+half with high draft noise (see speculative_decoding_verification_58_gb300/synth.py).
+
+Prints one JSON line.  ``value`` is verification rounds per second over all
+ranks (each rank verifies its own batch: weak scaling, no collective on the
+data path), with inputs resident in HBM.  The logits (1.28 GB at the default
+workload) are far larger than L2, so no flush is needed between steps.
+
+``--impl reference`` times the plain CPU oracle (the reference this library
+is checked against) on the host cores on the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "verify rounds/s & achieved HBM GB/s at B=128,k=16,V=151936 bf16 (1 GB300)"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=None, help="a name from synth.WORKLOADS")
+    ap.add_argument("--seed", type=int, default=None)
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-full-sweep", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# Small helpers
+# ---------------------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def csrc_digest() -> str:
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "speculative_decoding_verification_58_gb300",
+                                          "csrc", "*")))
+    files.append(os.path.join(ROOT, "include", "spec_verify.h"))
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per sweep launch from the committed ncu summary, if it matches the sources."""
+    path = os.path.join(ROOT, "profiles", f"sweep_kernel_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("- traffic_bytes_per_launch", "- csrc_digest")):
+            key, val = line.strip()[2:].split(":", 1)
+            vals[key.strip()] = val.strip().strip("`")
+    if vals.get("csrc_digest") != csrc_digest():
+        return None
+    try:
+        return int(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the GPU is busy."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        for p in self.samples:
+            try:
+                sm.append(float(p[0]))
+                smax.append(float(p[1]))
+            except ValueError:
+                continue
+            for name, v in zip(self.NAMES, p[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def model_bytes(inp, o, esize):
+    """M1: rows i < L_b (2 per sampling position) + the final row(s); M2: only up to n_b."""
+    V = inp.V
+    m1 = m2 = 0
+    for b in range(inp.B):
+        n = int(o.num_accepted[b])
+        L = int(inp.lengths[b])
+        greedy = inp.temperature[b] == 0
+        per = 1 if greedy else 2
+        final = 0 if (greedy and n < L) else (2 if n < L else 1)
+        m1 += (per * L + final) * V * esize
+        m2 += (per * (min(n + 1, L)) + final) * V * esize
+    return m1, m2
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the CPU oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    from speculative_decoding_verification_58_gb300 import synth
+
+    name = args.workload or synth.HEADLINE
+    cfg = synth.WORKLOADS[name]
+    inp = synth.make_workload(name, seed=args.seed)
+    oracle.build()
+    sample_b = max(1, inp.B // 16)
+
+    def step(j):
+        lo = (j * sample_b) % inp.B
+        sl = slice(lo, lo + sample_b)
+        oracle.verify(inp.target[sl], inp.draft[sl], inp.tokens[sl], inp.lengths[sl],
+                      inp.uniforms[sl], inp.temperature[sl])
+
+    for j in range(args.warmup):
+        step(j)
+    t0 = time.perf_counter()
+    for j in range(args.steps):
+        step(args.warmup + j)
+    dt = time.perf_counter() - t0
+    sec_per_round = dt / args.steps * (inp.B / sample_b)
+    value = 1.0 / sec_per_round
+    sample = (f"{sample_b} of the {inp.B} requests per step (rotating), scaled to a full "
+              f"{inp.B}-request round; single-threaded fp64 C++ oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rounds/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec_per_round * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "B": cfg["B"], "k": cfg["k"], "V": cfg["V"],
+                   "logits": cfg["dtype"]},
+        "cpu_baseline": {"value": value, "unit": "rounds/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "rounds/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import speculative_decoding_verification_58_gb300 as sv
+    from speculative_decoding_verification_58_gb300 import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    sv.lib()
+
+    name = args.workload or synth.HEADLINE
+    cfg = synth.WORKLOADS[name]
+    seed = (args.seed if args.seed is not None else cfg["seed"]) + 1000 * rank
+    inp = synth.make_workload(name, seed=seed)
+    esize = 2 if inp.dtype == "bf16" else 4
+    d = sv.to_device(inp, dev)
+    ws = sv.alloc_workspace(inp.B, inp.k, inp.V, dev)
+    out = torch.empty((inp.B, inp.k + 1), dtype=torch.int32, device=dev)
+    nacc = torch.empty(inp.B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(full_sweep=False, events=None):
+        sv.spec_verify(**d, workspace=ws, out_tokens=out, num_accepted=nacc, stream=stream,
+                       full_sweep=full_sweep, events=events)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    props = torch.cuda.get_device_properties(dev)
+    sampler = ClockSampler(f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local))
+
+    # Warm-up, then the timed region: K rounds, device-timed with events on the launch stream.
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    rep = sv.spec_verify_report(ws, stream)
+    gpu_out, gpu_n = out.cpu().numpy(), nacc.cpu().numpy()
+
+    # Per-kernel durations: the same rounds with events between the kernels.
+    kreps = max(10, min(args.steps, 200))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(kreps)]
+    for row in evs:
+        for e in row:
+            e.record(stream)  # creates the handles
+    torch.cuda.synchronize(dev)
+    for row in evs:
+        step(events=row)
+    torch.cuda.synchronize(dev)
+    k_plan = statistics.mean(r[0].elapsed_time(r[1]) for r in evs)
+    k_sweep = statistics.mean(r[1].elapsed_time(r[2]) for r in evs)
+    k_final = statistics.mean(r[2].elapsed_time(r[3]) for r in evs)
+
+    # Same workload with early exit switched off (every row i < L_b is swept).
+    full = None
+    if not args.no_full_sweep:
+        for _ in range(3):
+            step(full_sweep=True)
+        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(kreps)]
+        for row in fev:
+            for e in row:
+                e.record(stream)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(kreps):
+            step(full_sweep=True)
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        frep = sv.spec_verify_report(ws, stream)
+        for row in fev:
+            step(full_sweep=True, events=row)
+        torch.cuda.synchronize(dev)
+        fsweep = statistics.mean(r[1].elapsed_time(r[2]) for r in fev)
+        full = {"ms_per_step": f0.elapsed_time(f1) / kreps, "sweep_ms": fsweep,
+                "sweep_bytes": frep.sweep_bytes,
+                "sweep_gbs": frep.sweep_bytes / (fsweep * 1e-3) / 1e9}
+
+    # End to end through the public API: pinned host inputs in, results out, every step.
+    import numpy as _np
+    host = {}
+    for key, t in d.items():
+        host[key] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        host[key].copy_(t.cpu())
+    h_out = torch.empty(out.shape, dtype=torch.int32, pin_memory=True)
+    h_n = torch.empty(nacc.shape, dtype=torch.int32, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = h_out.numel() * 4 + h_n.numel() * 4
+    e2e_steps = args.e2e_steps or max(5, min(50, args.steps))
+
+    def e2e_step():
+        for key, t in host.items():
+            d[key].copy_(t, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_n.copy_(nacc, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps)
+    clocks = sampler.stop()
+    barrier()
+
+    if rank != 0:
+        return
+
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    sweep_gbs = rep.sweep_bytes / (k_sweep * 1e-3) / 1e9
+    round_bytes = rep.sweep_bytes + rep.final_bytes
+    value = world * 1000.0 / ms
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": inp.dtype if inp.dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": name, "B": inp.B, "k": inp.k, "V": inp.V, "logits": inp.dtype,
+                   "seed": seed, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {(inp.target.nbytes + inp.draft.nbytes) / 1e9:.2f} "
+                         "GB of logits resident, no flush between steps",
+                   "early_exit": True},
+        "hbm_gbs": round_bytes / (ms * 1e-3) / 1e9,
+        "hbm_gbs_frac": round_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
+        "roofline": {"bound": "hbm", "kernel": "sweep_kernel", "achieved": sweep_gbs,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": sweep_gbs / hbm_peak,
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind ==
+                     "measured" else "fallback 6.8 TB/s",
+                     "traffic": ncu_traffic(name),
+                     "bytes_per_launch": rep.sweep_bytes},
+        "kernels_ms": {"plan": k_plan, "sweep": k_sweep, "final": k_final},
+        "round_bytes": {"sweep": rep.sweep_bytes, "final": rep.final_bytes},
+        "e2e": {"value": world / e2e_s, "unit": "rounds/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if full is not None:
+        full["sweep_frac"] = full["sweep_gbs"] / hbm_peak
+        result["full_sweep"] = full
+
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        reps, spent = 0, 0.0
+        t0 = time.perf_counter()
+        o = None
+        while reps < 1 or (spent < 10.0 and reps < 3):
+            o = oracle.verify(inp.target, inp.draft, inp.tokens, inp.lengths, inp.uniforms,
+                              inp.temperature)
+            reps += 1
+            spent = time.perf_counter() - t0
+        result["cpu_baseline"] = {
+            "value": reps / spent, "unit": "rounds/s", "cores": 1, "kind": "oracle",
+            "sample": f"the full {inp.B}-request round, {reps} time(s), single-threaded fp64 oracle"}
+        same = (gpu_n == o.num_accepted) & _np.all(gpu_out == o.out_tokens, axis=1)
+        near = o.margin < 1e-6
+        m1, m2 = model_bytes(inp, o, esize)
+        result["parity"] = {"requests": int(inp.B), "mismatches": int((~same).sum()),
+                            "outside_near_tie_band": int((~same & ~near).sum()),
+                            "near_ties": int(near.sum())}
+        result["byte_models"] = {"M1_all_rows": m1, "M2_rows_to_first_reject": m2,
+                                 "moved": round_bytes,
+                                 "M1_gbs": m1 / (ms * 1e-3) / 1e9,
+                                 "mean_accepted": float(o.num_accepted.mean())}
+    print(json.dumps(result), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

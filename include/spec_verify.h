@@ -1,0 +1,207 @@
+/*
+ * spec_verify.h - C ABI of the GB300 (sm_103a) batched speculative-decoding
+ * verification library (libspecverify.so).
+ *
+ * The operation follows AdaFlash: Adaptive Speculative Decoding via
+ * On-Policy Distilled Diffusion Drafters (arXiv 2607.19223), Section 2.1
+ * "Speculative Decoding": for each request b and draft position i < L_b, the
+ * draft token x_i is accepted with probability min{1, p_i(x_i) / q_i(x_i)},
+ * where p_i = softmax(target_logits[b,i,:] / T_b) and
+ * q_i = softmax(draft_logits[b,i,:] / T_b); every token before the first
+ * rejected one is kept and a corrected token is drawn at the rejection point
+ * from normalize(max(0, p_i - q_i)) (the residual distribution; restated in
+ * the AdaFlash reading notes, "Speculative decoding: the basic idea", step 4,
+ * and in the DFlash notes, section 5.2).  When all L_b drafts are accepted,
+ * one more token is drawn from p_{L_b} (DFlash notes, section 3.1, steps 6-7:
+ * m accepted + 1 emitted).  At T_b == 0 the rule is greedy matching: accept
+ * while x_i equals the target argmax, emit the target argmax at the first
+ * mismatch (DFlash notes, section 5.2, worked example #4; AdaFlash Appendix
+ * B.1).  L_b is the per-request verification length chosen by an adaptive
+ * length head, 1 <= L_b <= k (AdaFlash Section 3.2, the clamp of k-hat).
+ *
+ * Readings where the pages are silent:
+ *   - the accept test for position i uses uniforms[b][i] and is the strict
+ *     comparison u < min(1, ratio);
+ *   - the final (residual or bonus) token uses uniforms[b][L_b];
+ *   - sampling is by inverse CDF in ascending vocabulary index: the first
+ *     index whose cumulative mass exceeds u * total mass, so a token of zero
+ *     probability is never emitted;
+ *   - argmax ties go to the lowest index;
+ *   - if the residual mass is zero, the token is drawn from p instead.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA device (or managed) memory owned by the caller;
+ *     the library allocates nothing, keeps no state between calls and never
+ *     synchronises the stream except where stated.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously on it.
+ *   - Host-detectable argument errors return immediately and launch nothing.
+ *   - Errors in values that live on the device (tokens, lengths, temperature,
+ *     uniforms, non-finite logits) cannot be seen by the host call: the
+ *     affected request gets num_accepted = -1 and out_tokens all -1, and the
+ *     workspace records SPEC_ERR_BAD_INPUT, readable with
+ *     spec_verify_device_status() or spec_verify_report().  No kernel traps.
+ *   - Every device-side wait is bounded; a wait that runs out records
+ *     SPEC_ERR_TIMEOUT in the workspace and the kernel returns.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPEC_VERIFY_ABI_VERSION 1
+
+/* Largest supported sizes. */
+#define SPEC_MAX_K 31          /* draft positions per request (decisions are 32-bit masks) */
+#define SPEC_MAX_V (1 << 21)   /* vocabulary size */
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1,  /* bad size, null pointer or misaligned pointer */
+  SPEC_ERR_UNSUPPORTED = 2,  /* valid request the library does not support (e.g. k > SPEC_MAX_K) */
+  SPEC_ERR_WORKSPACE = 3,    /* workspace too small or not 256-byte aligned */
+  SPEC_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  SPEC_ERR_BAD_INPUT = 5,    /* device-detected invalid value in some request */
+  SPEC_ERR_TIMEOUT = 6,      /* a bounded device-side wait ran out */
+  SPEC_ERR_INTERNAL = 7      /* internal consistency check failed */
+} spec_status_t;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
+
+/* Flags for spec_verify_ex. */
+#define SPEC_FLAG_FULL_SWEEP 1u  /* sweep every row i < L_b even past a known rejection */
+
+/*
+ * Bytes of device workspace spec_verify needs for a batch of B requests with
+ * k draft positions over a vocabulary of V.  Depends only on (B, k, V).
+ * Returns 0 for sizes outside the supported range.
+ */
+size_t spec_verify_workspace_bytes(int B, int k, int V);
+
+/*
+ * Batched verification (asynchronous on `stream`).
+ *
+ *   target_logits [B, k+1, V]  dtype, row-major contiguous; row i (i <= k) is
+ *                              the target's next-token logits after x_0..x_{i-1}
+ *   draft_logits  [B, k, V]    dtype, row-major contiguous; row i is the
+ *                              drafter's distribution for position i (it may be a
+ *                              marginal, as for one-pass diffusion drafters)
+ *   dtype                      SPEC_F32 (float) or SPEC_BF16 (bfloat16 bits)
+ *   draft_tokens  [B, k]       int32 in [0, V) for i < L_b
+ *   lengths       [B]          int32 in [1, k]
+ *   uniforms      [B, k+1]     float in [0, 1): u_i for the test at position i,
+ *                              u_{L_b} for the final sample (unused at T = 0)
+ *   temperature   [B]          float: 0 = greedy; otherwise a normal float
+ *                              (>= 2^-126) and finite
+ *   out_tokens    [B, k+1]     int32 out: x_0..x_{n-1}, the final token, then -1
+ *   num_accepted  [B]          int32 out: n in [0, L_b], or -1 for a request
+ *                              whose inputs were invalid
+ *   workspace                  device scratch of >= spec_verify_workspace_bytes
+ *                              bytes, 256-byte aligned; holds the status until the
+ *                              next call on it.  Concurrent calls need separate
+ *                              workspaces.
+ *
+ * Logit pointers must be aligned to their element size; 16-byte aligned rows
+ * (V * element size a multiple of 16 and 16-byte aligned bases) take the fast
+ * path.  Logits may contain -inf; every row that is read must have at least
+ * one finite entry, and NaN or +inf make the request invalid.
+ *
+ * Returns SPEC_OK once the work is enqueued, or an error code (nothing
+ * enqueued).
+ */
+spec_status_t spec_verify(const void* target_logits, const void* draft_logits,
+                          spec_dtype_t dtype, const int32_t* draft_tokens,
+                          const int32_t* lengths, const float* uniforms,
+                          const float* temperature, int B, int k, int V,
+                          int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* spec_verify with flags (SPEC_FLAG_*).  flags = 0 is spec_verify. */
+spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits,
+                             spec_dtype_t dtype, const int32_t* draft_tokens,
+                             const int32_t* lengths, const float* uniforms,
+                             const float* temperature, int B, int k, int V,
+                             int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                             size_t workspace_bytes, void* stream, unsigned flags);
+
+/*
+ * Measurement only: spec_verify_ex that also records up to four caller-owned
+ * CUDA events (cudaEvent_t as void*, any may be NULL) on `stream`: before the
+ * plan kernel, before the row sweep, before the final pass, and after it.
+ * Recording events between the kernels removes the launch overlap they
+ * otherwise get from programmatic dependent launch, so use this to time the
+ * kernels one by one and spec_verify for end-to-end numbers.
+ */
+spec_status_t spec_verify_timed(const void* target_logits, const void* draft_logits,
+                                spec_dtype_t dtype, const int32_t* draft_tokens,
+                                const int32_t* lengths, const float* uniforms,
+                                const float* temperature, int B, int k, int V,
+                                int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                                size_t workspace_bytes, void* stream, unsigned flags,
+                                void* ev_plan, void* ev_sweep, void* ev_final, void* ev_end);
+
+/* What the last call on a workspace recorded. */
+typedef struct {
+  int32_t status;             /* spec_status_t recorded on the device */
+  int32_t bad_requests;       /* requests with invalid inputs */
+  int32_t first_bad_request;  /* lowest such request index, or -1 */
+  int32_t rows_planned;       /* logit rows the plan admitted (sum over valid b of L_b or 2 L_b) */
+  int64_t chunks_swept;       /* row chunks the sweep actually read */
+  int32_t chunks_per_row;     /* vocabulary chunks per row used by the sweep */
+  int32_t chunk_elems;        /* elements per chunk (last chunk may be shorter) */
+  int64_t final_rows;         /* logit rows the final pass read (residual 2, bonus 1) */
+  int32_t residual_zero;      /* requests whose residual mass was zero (fell back to p) */
+  int32_t reserved;
+  int64_t sweep_bytes;        /* logit bytes the sweep streamed from memory */
+  int64_t final_bytes;        /* logit bytes the final pass streamed (first pass over its rows) */
+} spec_verify_report_t;
+
+/*
+ * Wait for `stream`, then copy the report of the last spec_verify call on
+ * `workspace` into *report (host memory).  Returns SPEC_OK or SPEC_ERR_CUDA.
+ */
+spec_status_t spec_verify_report(const void* workspace, void* stream,
+                                 spec_verify_report_t* report);
+
+/*
+ * Wait for `stream` and return the device-recorded status of the last
+ * spec_verify call on `workspace` (SPEC_OK, SPEC_ERR_BAD_INPUT,
+ * SPEC_ERR_TIMEOUT or SPEC_ERR_INTERNAL), or SPEC_ERR_CUDA if reading it failed.
+ */
+spec_status_t spec_verify_device_status(const void* workspace, void* stream);
+
+/*
+ * The row sweep on its own: per-row statistics of `rows` rows of V logits
+ * (step 1 of verification; AdaFlash Section 2.1 needs p and q normalised
+ * over the full vocabulary).
+ *   logits       [rows, V] dtype, row-major contiguous (device)
+ *   temperature  [rows] float (device): 0 = argmax only
+ *   row_max      [rows] float out: max_v z
+ *   row_lse      [rows] float out: log sum_v exp(z_v / T) (natural log; NaN when T = 0)
+ *   row_arg      [rows] int32 out: lowest index attaining the max for T = 0
+ *                rows; -1 for T > 0 rows (their sweep keeps no index)
+ * Uses the same kernels and arithmetic as spec_verify.  Temperatures are
+ * not validated here: pass 0 or a finite normal float.
+ */
+size_t spec_row_stats_workspace_bytes(int rows, int V);
+spec_status_t spec_row_stats(const void* logits, spec_dtype_t dtype, int rows, int V,
+                             const float* temperature, float* row_max, float* row_lse,
+                             int32_t* row_arg, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* Static description of a status code. */
+const char* spec_status_string(spec_status_t status);
+
+/* SPEC_VERIFY_ABI_VERSION of the loaded library. */
+int spec_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,1 +1,285 @@
-"""GB300-native batched speculative-decoding verification (placeholder; binding added with the C-ABI)."""
+"""GB300-native batched speculative-decoding verification.
+
+A thin Python binding over the C ABI of ``libspecverify.so`` (declared in
+``include/spec_verify.h``).  Every step of verification runs in the
+library's CUDA kernels; this module only checks tensor shapes, passes raw
+device pointers and the current CUDA stream, and turns status codes into
+exceptions.  There is no CPU fallback: if the library has not been built,
+every call raises.
+
+The functions keep the C names:
+
+``spec_verify(...)``                 batched verification (asynchronous)
+``spec_verify_workspace_bytes(...)`` workspace size for (B, k, V)
+``spec_verify_report(ws)``           what the device recorded for the last call
+``spec_verify_device_status(ws)``    just the recorded status
+``spec_row_stats(...)``              the row sweep alone: max, logsumexp, argmax
+``spec_status_string(code)``
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+
+SPEC_OK = 0
+SPEC_ERR_INVALID_ARG = 1
+SPEC_ERR_UNSUPPORTED = 2
+SPEC_ERR_WORKSPACE = 3
+SPEC_ERR_CUDA = 4
+SPEC_ERR_BAD_INPUT = 5
+SPEC_ERR_TIMEOUT = 6
+SPEC_ERR_INTERNAL = 7
+SPEC_F32 = 0
+SPEC_BF16 = 1
+SPEC_FLAG_FULL_SWEEP = 1
+
+# Every entry point include/spec_verify.h declares.
+EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_ex", "spec_verify_timed",
+           "spec_verify_report",
+           "spec_verify_device_status", "spec_row_stats_workspace_bytes", "spec_row_stats",
+           "spec_status_string", "spec_abi_version")
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+
+
+class _Report(ctypes.Structure):
+    _fields_ = [("status", ctypes.c_int32), ("bad_requests", ctypes.c_int32),
+                ("first_bad_request", ctypes.c_int32), ("rows_planned", ctypes.c_int32),
+                ("chunks_swept", ctypes.c_int64), ("chunks_per_row", ctypes.c_int32),
+                ("chunk_elems", ctypes.c_int32), ("final_rows", ctypes.c_int64),
+                ("residual_zero", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("sweep_bytes", ctypes.c_int64), ("final_bytes", ctypes.c_int64)]
+
+
+@dataclass
+class Report:
+    status: int
+    bad_requests: int
+    first_bad_request: int
+    rows_planned: int
+    chunks_swept: int
+    chunks_per_row: int
+    chunk_elems: int
+    final_rows: int
+    residual_zero: int
+    sweep_bytes: int
+    final_bytes: int
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded ``libspecverify.so``; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32p, f32p = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+    ci, csz = ctypes.c_int, ctypes.c_size_t
+    L.spec_verify_workspace_bytes.argtypes = [ci, ci, ci]
+    L.spec_verify_workspace_bytes.restype = csz
+    L.spec_verify.argtypes = [vp, vp, ci, i32p, i32p, f32p, f32p, ci, ci, ci, i32p, i32p, vp, csz, vp]
+    L.spec_verify.restype = ci
+    L.spec_verify_ex.argtypes = L.spec_verify.argtypes + [ctypes.c_uint]
+    L.spec_verify_ex.restype = ci
+    L.spec_verify_timed.argtypes = L.spec_verify_ex.argtypes + [vp, vp, vp, vp]
+    L.spec_verify_timed.restype = ci
+    L.spec_verify_report.argtypes = [vp, vp, ctypes.POINTER(_Report)]
+    L.spec_verify_report.restype = ci
+    L.spec_verify_device_status.argtypes = [vp, vp]
+    L.spec_verify_device_status.restype = ci
+    L.spec_row_stats_workspace_bytes.argtypes = [ci, ci]
+    L.spec_row_stats_workspace_bytes.restype = csz
+    L.spec_row_stats.argtypes = [vp, ci, ci, ci, f32p, f32p, f32p, i32p, vp, csz, vp]
+    L.spec_row_stats.restype = ci
+    L.spec_status_string.argtypes = [ci]
+    L.spec_status_string.restype = ctypes.c_char_p
+    L.spec_abi_version.argtypes = []
+    L.spec_abi_version.restype = ci
+    _lib = L
+    return L
+
+
+def build(force: bool = False) -> str:
+    """Compile the library in-tree with nvcc for sm_103a."""
+    global _lib
+    from . import make_lib
+    path = make_lib.build(force=force)
+    _lib = None
+    return path
+
+
+def status_string(code: int) -> str:
+    try:
+        return lib().spec_status_string(code).decode()
+    except RuntimeError:
+        return f"status {code}"
+
+
+spec_status_string = status_string
+
+
+def _check(code: int, where: str) -> None:
+    if code != SPEC_OK:
+        raise SpecVerifyError(code, where)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _need(t, name, dtype, shape, device):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def spec_verify_workspace_bytes(B: int, k: int, V: int) -> int:
+    return int(lib().spec_verify_workspace_bytes(B, k, V))
+
+
+def alloc_workspace(B: int, k: int, V: int, device=None):
+    """A device workspace (torch uint8 tensor, 256-byte aligned by the caching allocator)."""
+    torch = _torch()
+    n = spec_verify_workspace_bytes(B, k, V)
+    if n == 0:
+        raise SpecVerifyError(SPEC_ERR_UNSUPPORTED, "spec_verify_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def spec_verify(target_logits, draft_logits, draft_tokens, lengths, uniforms, temperature, *,
+                workspace=None, out_tokens=None, num_accepted=None, stream=None,
+                full_sweep: bool = False, events=None):
+    """Batched verification on the current (or given) CUDA stream.
+
+    Shapes: target [B, k+1, V], draft [B, k, V] (float32 or bfloat16, same),
+    draft_tokens int32 [B, k], lengths int32 [B], uniforms float32 [B, k+1],
+    temperature float32 [B].  Returns (out_tokens int32 [B, k+1],
+    num_accepted int32 [B]); results are ready when the stream reaches them.
+
+    ``events``: optional four recorded ``torch.cuda.Event`` objects (or None
+    entries) marking plan / sweep / final / end, for per-kernel timing
+    (measurement only: it disables the kernels' launch overlap).
+    """
+    torch = _torch()
+    B, k1, V = target_logits.shape
+    k = k1 - 1
+    dev = target_logits.device
+    dt = _dtype_code(target_logits)
+    _need(target_logits, "target_logits", target_logits.dtype, (B, k + 1, V), dev)
+    _need(draft_logits, "draft_logits", target_logits.dtype, (B, k, V), dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, k), dev)
+    _need(lengths, "lengths", torch.int32, (B,), dev)
+    _need(uniforms, "uniforms", torch.float32, (B, k + 1), dev)
+    _need(temperature, "temperature", torch.float32, (B,), dev)
+    if workspace is None:
+        workspace = alloc_workspace(B, k, V, dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    if num_accepted is None:
+        num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, k + 1), dev)
+    _need(num_accepted, "num_accepted", torch.int32, (B,), dev)
+    flags = SPEC_FLAG_FULL_SWEEP if full_sweep else 0
+    args = (target_logits.data_ptr(), draft_logits.data_ptr(), dt, draft_tokens.data_ptr(),
+            lengths.data_ptr(), uniforms.data_ptr(), temperature.data_ptr(), B, k, V,
+            out_tokens.data_ptr(), num_accepted.data_ptr(), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_ptr(stream), flags)
+    if events is None:
+        code = lib().spec_verify_ex(*args)
+    else:
+        handles = [None if e is None else (e.cuda_event or None) for e in events]
+        code = lib().spec_verify_timed(*args, *handles)
+    _check(code, "spec_verify")
+    return out_tokens, num_accepted
+
+
+def spec_verify_report(workspace, stream=None) -> Report:
+    """Synchronise the stream and read what the last call on ``workspace`` recorded."""
+    r = _Report()
+    _check(lib().spec_verify_report(workspace.data_ptr(), _stream_ptr(stream), ctypes.byref(r)),
+           "spec_verify_report")
+    return Report(r.status, r.bad_requests, r.first_bad_request, r.rows_planned, r.chunks_swept,
+                  r.chunks_per_row, r.chunk_elems, r.final_rows, r.residual_zero, r.sweep_bytes,
+                  r.final_bytes)
+
+
+def spec_verify_device_status(workspace, stream=None) -> int:
+    return int(lib().spec_verify_device_status(workspace.data_ptr(), _stream_ptr(stream)))
+
+
+def spec_row_stats(logits, temperature, *, stream=None):
+    """Row sweep alone over [rows, V] logits: (max, natural-log logsumexp of z/T, argmax).
+
+    ``lse`` is NaN for T == 0 rows; ``argmax`` is -1 for T > 0 rows.
+    """
+    torch = _torch()
+    rows, V = logits.shape
+    dev = logits.device
+    dt = _dtype_code(logits)
+    _need(logits, "logits", logits.dtype, (rows, V), dev)
+    _need(temperature, "temperature", torch.float32, (rows,), dev)
+    n = int(lib().spec_row_stats_workspace_bytes(rows, V))
+    if n == 0:
+        raise SpecVerifyError(SPEC_ERR_UNSUPPORTED, "spec_row_stats_workspace_bytes")
+    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+    mx = torch.empty(rows, dtype=torch.float32, device=dev)
+    lse = torch.empty(rows, dtype=torch.float32, device=dev)
+    arg = torch.empty(rows, dtype=torch.int32, device=dev)
+    _check(lib().spec_row_stats(logits.data_ptr(), dt, rows, V, temperature.data_ptr(),
+                                mx.data_ptr(), lse.data_ptr(), arg.data_ptr(), ws.data_ptr(), n,
+                                _stream_ptr(stream)), "spec_row_stats")
+    return mx, lse, arg
+
+
+def to_device(inputs, device="cuda"):
+    """Copy a ``synth.SpecInputs`` batch to the device as the C-ABI's buffers."""
+    torch = _torch()
+    import numpy as np
+    if inputs.dtype == "bf16":
+        t = torch.from_numpy(inputs.target.view(np.int16)).view(torch.bfloat16)
+        d = torch.from_numpy(inputs.draft.view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(inputs.target)
+        d = torch.from_numpy(inputs.draft)
+    return dict(
+        target_logits=t.to(device), draft_logits=d.to(device),
+        draft_tokens=torch.from_numpy(inputs.tokens).to(device),
+        lengths=torch.from_numpy(inputs.lengths).to(device),
+        uniforms=torch.from_numpy(inputs.uniforms).to(device),
+        temperature=torch.from_numpy(inputs.temperature).to(device))

@@ -1,0 +1,461 @@
+// C ABI of the verification library: argument checks, workspace sizing and
+// the launch sequence plan -> sweep -> final on the caller's stream.  The
+// sweep and final kernels use programmatic dependent launch so that their
+// prologues overlap the previous kernel's tail; each waits for its
+// predecessor's results with griddepcontrol.wait before reading them.
+
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "final.cuh"
+#include "plan.cuh"
+#include "sweep.cuh"
+
+namespace specv {
+
+// ---------------------------------------------------------------------------
+// Row-statistics kernels (spec_row_stats).
+// ---------------------------------------------------------------------------
+
+__global__ void stats_plan_kernel(unsigned char* ws, WsLayout lay, int rows, int nch,
+                                  int chunk_elems) {
+  pdl_launch_dependents();
+  WsHeader* h = reinterpret_cast<WsHeader*>(ws + lay.header);
+  h->status = SPEC_OK;
+  h->bad_requests = 0;
+  h->first_bad = INT32_MAX;
+  h->work_next = 0;
+  h->rows_planned = rows;
+  h->units_total = rows * nch;
+  h->chunks_per_row = nch;
+  h->chunk_elems = chunk_elems;
+  h->chunks_swept = 0;
+  h->final_rows = 0;
+  h->residual_zero = 0;
+  h->sweep_bytes = 0;
+  h->final_bytes = 0;
+}
+
+// One warp per row: combine the chunk partials into max, natural-log
+// logsumexp of z/T (sampling rows) and argmax (greedy rows).
+__global__ void stats_finalize_kernel(const unsigned char* ws, WsLayout lay, int rows, int nch,
+                                      const float* temperature, float* row_max, float* row_lse,
+                                      int32_t* row_arg) {
+  pdl_wait();
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const Partial* parts = reinterpret_cast<const Partial*>(ws + lay.partials) + (size_t)r * nch;
+  const float T = temperature[r];
+  if (T == 0.0f) {
+    float v;
+    int g;
+    row_argmax_from_parts(parts, nch, &v, &g);
+    if (lane == 0) {
+      row_max[r] = v;
+      row_lse[r] = __int_as_float(0x7fc00000);
+      row_arg[r] = (g == INT32_MAX) ? -1 : g;
+    }
+  } else {
+    const float sc = softmax_scale(T);
+    double c;
+    float m;
+    const bool ok = row_log2_normaliser(parts, nch, sc, &c, &m);
+    if (lane == 0) {
+      row_max[r] = m;
+      row_lse[r] = ok ? (float)(c * kLn2) : __int_as_float(0x7fc00000);
+      row_arg[r] = -1;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Per-device launch facts.
+// ---------------------------------------------------------------------------
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int sweep_blocks_per_sm[2][2] = {{0, 0}, {0, 0}};  // [dtype][verify]
+  size_t final_smem_optin = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+template <typename TIn, bool kVerify>
+cudaError_t sweep_blocks(int* out) {
+  cudaError_t e = cudaFuncSetAttribute(sweep_kernel<TIn, kVerify>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sizeof(SweepSmem));
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, sweep_kernel<TIn, kVerify>,
+                                                       kSweepThreads, sizeof(SweepSmem));
+}
+
+cudaError_t device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    int optin = 0;
+    if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+        cudaSuccess)
+      return e;
+    d.final_smem_optin = (size_t)optin;
+    if ((e = sweep_blocks<float, true>(&d.sweep_blocks_per_sm[0][1])) != cudaSuccess) return e;
+    if ((e = sweep_blocks<uint16_t, true>(&d.sweep_blocks_per_sm[1][1])) != cudaSuccess) return e;
+    if ((e = sweep_blocks<float, false>(&d.sweep_blocks_per_sm[0][0])) != cudaSuccess) return e;
+    if ((e = sweep_blocks<uint16_t, false>(&d.sweep_blocks_per_sm[1][0])) != cudaSuccess) return e;
+    const int fsm = (int)(kMaxSegs * (sizeof(double) + sizeof(float)));
+    if ((e = cudaFuncSetAttribute(final_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  fsm)) != cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(final_kernel<uint16_t>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, fsm)) != cudaSuccess)
+      return e;
+    d.ready = true;
+  }
+  *out = &d;
+  return cudaSuccess;
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                   cudaStream_t stream, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+cudaError_t record(void* const* ev, int j, cudaStream_t stream) {
+  if (ev == nullptr || ev[j] == nullptr) return cudaSuccess;
+  return cudaEventRecord(static_cast<cudaEvent_t>(ev[j]), stream);
+}
+
+bool sizes_ok(int B, int k, int V) {
+  if (B < 1 || k < 1 || V < 1) return false;
+  if (k > SPEC_MAX_K || V > SPEC_MAX_V) return false;
+  // Row slots (b*k + i) * 2 + tensor and work units must fit in int32.
+  const long long slots = 2LL * B * k;
+  if (slots * (long long)chunks_per_row(slots, V) >= (1LL << 31)) return false;
+  return true;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Make the device that owns `p` current for this library's runtime on this
+// thread (the caller's framework may keep its own notion of the current
+// device).  Host or unregistered pointers leave the current device alone.
+cudaError_t use_device_of(const void* p) {
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) return e;
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    int cur = -1;
+    if ((e = cudaGetDevice(&cur)) != cudaSuccess) return e;
+    if (cur != a.device && a.device >= 0) return cudaSetDevice(a.device);
+  }
+  return cudaSuccess;
+}
+
+template <typename TIn>
+spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
+                           const int32_t* draft_tokens, const int32_t* lengths,
+                           const float* uniforms, const float* temperature, int B, int k, int V,
+                           int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                           cudaStream_t stream, unsigned flags, int dtype_index,
+                           void* const* ev) {
+  DeviceInfo* d = nullptr;
+  if (device_info(&d) != cudaSuccess) return SPEC_ERR_CUDA;
+  const long long slots = 2LL * B * k;
+  const int C = chunks_per_row(slots, V);
+  const int ce = chunk_elems_for(V, C);
+  const int nch = (V + ce - 1) / ce;
+  const WsLayout lay = ws_layout(B, k, C);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+
+  PlanParams pp;
+  pp.tokens = draft_tokens;
+  pp.lengths = lengths;
+  pp.uniforms = uniforms;
+  pp.temperature = temperature;
+  pp.B = B;
+  pp.k = k;
+  pp.V = V;
+  pp.C = C;
+  pp.chunk_elems = ce;
+  pp.nch = nch;
+  pp.ws = ws;
+  pp.lay = lay;
+  // With timing events between the kernels there is nothing to overlap.
+  const bool pdl = (ev == nullptr);
+  if (record(ev, 0, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (launch(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, false, pp) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+
+  SweepParams sp;
+  sp.target = target_logits;
+  sp.draft = draft_logits;
+  sp.tokens = draft_tokens;
+  sp.uniforms = uniforms;
+  sp.temperature = temperature;
+  sp.B = B;
+  sp.k = k;
+  sp.V = V;
+  sp.nch = nch;
+  sp.chunk_elems = ce;
+  sp.early_exit = (flags & SPEC_FLAG_FULL_SWEEP) ? 0 : 1;
+  sp.ws = ws;
+  sp.lay = lay;
+  const long long max_units = slots * nch;
+  long long grid = (long long)d->sms * d->sweep_blocks_per_sm[dtype_index][1];
+  if (grid > max_units) grid = max_units;
+  if (grid < 1) grid = 1;
+  if (record(ev, 1, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (launch(sweep_kernel<TIn, true>, dim3((unsigned)grid), dim3(kSweepThreads),
+             sizeof(SweepSmem), stream, pdl, sp) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+
+  FinalParams fp;
+  fp.target = target_logits;
+  fp.draft = draft_logits;
+  fp.tokens = draft_tokens;
+  fp.lengths = lengths;
+  fp.uniforms = uniforms;
+  fp.temperature = temperature;
+  fp.B = B;
+  fp.k = k;
+  fp.V = V;
+  fp.out_tokens = out_tokens;
+  fp.num_accepted = num_accepted;
+  fp.ws = ws;
+  fp.lay = lay;
+  const int nseg = (V + kSegElems - 1) / kSegElems;
+  const size_t fsm = (size_t)nseg * (sizeof(double) + sizeof(float));
+  if (record(ev, 2, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (launch(final_kernel<TIn>, dim3(B), dim3(kFinalThreads), fsm, stream, pdl, fp) !=
+      cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (record(ev, 3, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+template <typename TIn>
+spec_status_t row_stats_typed(const void* logits, int rows, int V, const float* temperature,
+                              float* row_max, float* row_lse, int32_t* row_arg, void* workspace,
+                              cudaStream_t stream, int dtype_index) {
+  DeviceInfo* d = nullptr;
+  if (device_info(&d) != cudaSuccess) return SPEC_ERR_CUDA;
+  const int C = chunks_per_row(rows, V);
+  const int ce = chunk_elems_for(V, C);
+  const int nch = (V + ce - 1) / ce;
+  // Stats mode keeps partials at row * nch + chunk: the layout of a batch of
+  // `rows` slots.
+  WsLayout lay = ws_layout(1, 1, 1);
+  lay.partials = align256(sizeof(WsHeader));
+  lay.total = lay.partials + align256((size_t)rows * C * sizeof(Partial));
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  if (launch(stats_plan_kernel, dim3(1), dim3(1), 0, stream, false, ws, lay, rows, nch, ce) !=
+      cudaSuccess)
+    return SPEC_ERR_CUDA;
+  SweepParams sp = {};
+  sp.target = logits;
+  sp.temperature = temperature;
+  sp.B = rows;
+  sp.k = 1;
+  sp.V = V;
+  sp.nch = nch;
+  sp.chunk_elems = ce;
+  sp.early_exit = 0;
+  sp.ws = ws;
+  sp.lay = lay;
+  long long grid = (long long)d->sms * d->sweep_blocks_per_sm[dtype_index][0];
+  if (grid > (long long)rows * nch) grid = (long long)rows * nch;
+  if (launch(sweep_kernel<TIn, false>, dim3((unsigned)grid), dim3(kSweepThreads),
+             sizeof(SweepSmem), stream, true, sp) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  const int wpb = 8;
+  if (launch(stats_finalize_kernel, dim3((rows + wpb - 1) / wpb), dim3(wpb * 32), 0, stream, true,
+             (const unsigned char*)ws, lay, rows, nch, temperature, row_max, row_lse,
+             row_arg) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+size_t row_stats_ws_bytes(int rows, int V) {
+  const int C = chunks_per_row(rows, V);
+  return align256(sizeof(WsHeader)) + align256((size_t)rows * C * sizeof(Partial));
+}
+
+}  // namespace specv
+
+using namespace specv;
+
+extern "C" {
+
+int spec_abi_version(void) { return SPEC_VERIFY_ABI_VERSION; }
+
+const char* spec_status_string(spec_status_t s) {
+  switch (s) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument (size, null or misaligned pointer)";
+    case SPEC_ERR_UNSUPPORTED: return "unsupported size";
+    case SPEC_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+    case SPEC_ERR_CUDA: return "CUDA runtime error";
+    case SPEC_ERR_BAD_INPUT: return "invalid value in device inputs (see num_accepted == -1)";
+    case SPEC_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+    case SPEC_ERR_INTERNAL: return "internal consistency check failed";
+  }
+  return "unknown status";
+}
+
+size_t spec_verify_workspace_bytes(int B, int k, int V) {
+  if (!sizes_ok(B, k, V)) return 0;
+  const long long slots = 2LL * B * k;
+  return ws_layout(B, k, chunks_per_row(slots, V)).total;
+}
+
+static spec_status_t verify_entry(const void* target_logits, const void* draft_logits,
+                             spec_dtype_t dtype, const int32_t* draft_tokens,
+                             const int32_t* lengths, const float* uniforms,
+                             const float* temperature, int B, int k, int V, int32_t* out_tokens,
+                             int32_t* num_accepted, void* workspace, size_t workspace_bytes,
+                             void* stream, unsigned flags, void* const* ev) {
+  if (B < 1 || k < 1 || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (!sizes_ok(B, k, V)) return SPEC_ERR_UNSUPPORTED;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if ((flags & ~SPEC_FLAG_FULL_SWEEP) != 0) return SPEC_ERR_INVALID_ARG;
+  if (!target_logits || !draft_logits || !draft_tokens || !lengths || !uniforms || !temperature ||
+      !out_tokens || !num_accepted)
+    return SPEC_ERR_INVALID_ARG;
+  const size_t esize = dtype == SPEC_F32 ? 4 : 2;
+  if (!aligned(target_logits, esize) || !aligned(draft_logits, esize) || !aligned(draft_tokens, 4) ||
+      !aligned(lengths, 4) || !aligned(uniforms, 4) || !aligned(temperature, 4) ||
+      !aligned(out_tokens, 4) || !aligned(num_accepted, 4))
+    return SPEC_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) ||
+      workspace_bytes < spec_verify_workspace_bytes(B, k, V))
+    return SPEC_ERR_WORKSPACE;
+  if (use_device_of(target_logits) != cudaSuccess) return SPEC_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == SPEC_F32)
+    return verify_typed<float>(target_logits, draft_logits, draft_tokens, lengths, uniforms,
+                               temperature, B, k, V, out_tokens, num_accepted, workspace, s, flags, 0,
+                               ev);
+  return verify_typed<uint16_t>(target_logits, draft_logits, draft_tokens, lengths, uniforms,
+                                temperature, B, k, V, out_tokens, num_accepted, workspace, s, flags,
+                                1, ev);
+}
+
+spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits,
+                             spec_dtype_t dtype, const int32_t* draft_tokens,
+                             const int32_t* lengths, const float* uniforms,
+                             const float* temperature, int B, int k, int V, int32_t* out_tokens,
+                             int32_t* num_accepted, void* workspace, size_t workspace_bytes,
+                             void* stream, unsigned flags) {
+  return verify_entry(target_logits, draft_logits, dtype, draft_tokens, lengths, uniforms,
+                      temperature, B, k, V, out_tokens, num_accepted, workspace, workspace_bytes,
+                      stream, flags, nullptr);
+}
+
+spec_status_t spec_verify_timed(const void* target_logits, const void* draft_logits,
+                                spec_dtype_t dtype, const int32_t* draft_tokens,
+                                const int32_t* lengths, const float* uniforms,
+                                const float* temperature, int B, int k, int V,
+                                int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                                size_t workspace_bytes, void* stream, unsigned flags,
+                                void* ev_plan, void* ev_sweep, void* ev_final, void* ev_end) {
+  void* const ev[4] = {ev_plan, ev_sweep, ev_final, ev_end};
+  return verify_entry(target_logits, draft_logits, dtype, draft_tokens, lengths, uniforms,
+                      temperature, B, k, V, out_tokens, num_accepted, workspace, workspace_bytes,
+                      stream, flags, ev);
+}
+
+spec_status_t spec_verify(const void* target_logits, const void* draft_logits, spec_dtype_t dtype,
+                          const int32_t* draft_tokens, const int32_t* lengths,
+                          const float* uniforms, const float* temperature, int B, int k, int V,
+                          int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  return spec_verify_ex(target_logits, draft_logits, dtype, draft_tokens, lengths, uniforms,
+                        temperature, B, k, V, out_tokens, num_accepted, workspace, workspace_bytes,
+                        stream, 0u);
+}
+
+spec_status_t spec_verify_report(const void* workspace, void* stream, spec_verify_report_t* report) {
+  if (!workspace || !report) return SPEC_ERR_INVALID_ARG;
+  WsHeader h;
+  if (use_device_of(workspace) != cudaSuccess) return SPEC_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&h, workspace, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SPEC_ERR_CUDA;
+  report->status = h.status;
+  report->bad_requests = h.bad_requests;
+  report->first_bad_request = h.first_bad == INT32_MAX ? -1 : h.first_bad;
+  report->rows_planned = h.rows_planned;
+  report->chunks_swept = (int64_t)h.chunks_swept;
+  report->chunks_per_row = h.chunks_per_row;
+  report->chunk_elems = h.chunk_elems;
+  report->final_rows = (int64_t)h.final_rows;
+  report->residual_zero = h.residual_zero;
+  report->reserved = 0;
+  report->sweep_bytes = (int64_t)h.sweep_bytes;
+  report->final_bytes = (int64_t)h.final_bytes;
+  return SPEC_OK;
+}
+
+spec_status_t spec_verify_device_status(const void* workspace, void* stream) {
+  spec_verify_report_t r;
+  spec_status_t st = spec_verify_report(workspace, stream, &r);
+  if (st != SPEC_OK) return st;
+  return (spec_status_t)r.status;
+}
+
+size_t spec_row_stats_workspace_bytes(int rows, int V) {
+  if (rows < 1 || V < 1 || V > SPEC_MAX_V) return 0;
+  if ((long long)rows * chunks_per_row(rows, V) >= (1LL << 31)) return 0;
+  return row_stats_ws_bytes(rows, V);
+}
+
+spec_status_t spec_row_stats(const void* logits, spec_dtype_t dtype, int rows, int V,
+                             const float* temperature, float* row_max, float* row_lse,
+                             int32_t* row_arg, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  if (rows < 1 || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (V > SPEC_MAX_V || spec_row_stats_workspace_bytes(rows, V) == 0) return SPEC_ERR_UNSUPPORTED;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (!logits || !temperature || !row_max || !row_lse || !row_arg) return SPEC_ERR_INVALID_ARG;
+  const size_t esize = dtype == SPEC_F32 ? 4 : 2;
+  if (!aligned(logits, esize) || !aligned(temperature, 4) || !aligned(row_max, 4) ||
+      !aligned(row_lse, 4) || !aligned(row_arg, 4))
+    return SPEC_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) ||
+      workspace_bytes < spec_row_stats_workspace_bytes(rows, V))
+    return SPEC_ERR_WORKSPACE;
+  if (use_device_of(logits) != cudaSuccess) return SPEC_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == SPEC_F32)
+    return row_stats_typed<float>(logits, rows, V, temperature, row_max, row_lse, row_arg, workspace,
+                                  s, 0);
+  return row_stats_typed<uint16_t>(logits, rows, V, temperature, row_max, row_lse, row_arg,
+                                   workspace, s, 1);
+}
+
+}  // extern "C"

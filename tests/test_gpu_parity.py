@@ -1,0 +1,241 @@
+"""CUDA path vs the CPU oracle, through the C-ABI (needs a GB300).
+
+out_tokens and num_accepted must match bit for bit, except for requests
+whose outcome depends on a decision within 1e-6 of its threshold (counted,
+at most 1e-5 of the logit rows evaluated); greedy requests match with no
+exemption.  Per-row max and argmax are exact, log-sum-exp within 1e-5
+relative.
+"""
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+import speculative_decoding_verification_58_gb300 as sv
+from speculative_decoding_verification_58_gb300 import synth
+from parity import compare
+
+pytestmark = pytest.mark.gpu
+
+LSE_RTOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sv.lib()
+
+
+def run_gpu(inp, full_sweep=False, workspace=None):
+    d = sv.to_device(inp)
+    ws = workspace if workspace is not None else sv.alloc_workspace(inp.B, inp.k, inp.V)
+    out, n = sv.spec_verify(**d, workspace=ws, full_sweep=full_sweep)
+    rep = sv.spec_verify_report(ws)
+    return out.cpu().numpy(), n.cpu().numpy(), rep
+
+
+def check(inp, label, full_sweep=False):
+    out, n, rep = run_gpu(inp, full_sweep=full_sweep)
+    o = oracle.verify(inp.target, inp.draft, inp.tokens, inp.lengths, inp.uniforms, inp.temperature)
+    info = compare(out, n, o, inp.temperature, label)
+    assert rep.status == sv.SPEC_OK, rep
+    assert rep.bad_requests == 0
+    return info, rep, o
+
+
+# ---------------------------------------------------------------------------
+# Row statistics (the sweep alone)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [1, 7, 1000, 4097, 151936])
+def test_row_stats_match_oracle(dtype, V):
+    rng = np.random.default_rng(V)
+    rows = 24 if V > 100000 else 61
+    z = (rng.standard_normal((rows, V)) * 2.5).astype(np.float32)
+    if V > 3:
+        z[0, V // 3] = z[0, V // 2] = z[0].max() + 2  # argmax tie
+    buf = synth.bf16_bits(z) if dtype == "bf16" else z
+    temp = rng.uniform(0.5, 1.5, rows).astype(np.float32)
+    temp[::5] = 0.0
+    mx_o, lse_o, arg_o = oracle.row_stats(buf, temp)
+    t = torch.from_numpy(buf.view(np.int16)).view(torch.bfloat16) if dtype == "bf16" \
+        else torch.from_numpy(buf)
+    mx, lse, arg = sv.spec_row_stats(t.cuda(), torch.from_numpy(temp).cuda())
+    mx, lse, arg = mx.cpu().numpy(), lse.cpu().numpy(), arg.cpu().numpy()
+    np.testing.assert_array_equal(mx.astype(np.float64), mx_o)
+    greedy = temp == 0
+    np.testing.assert_array_equal(arg[greedy], arg_o[greedy])
+    np.testing.assert_allclose(lse[~greedy], lse_o[~greedy], rtol=LSE_RTOL, atol=1e-6)
+
+
+# ---------------------------------------------------------------------------
+# Verification on reduced and full workloads
+# ---------------------------------------------------------------------------
+
+SMALL = [
+    ("gauss", 1, 4, 1024, "f32"),
+    ("zipf", 3, 16, 4096, "bf16"),
+    ("zipf_adaptive", 32, 16, 8200, "bf16"),
+    ("zipf_mixed_noise", 64, 16, 5000, "bf16"),
+    ("zipf_mixed_temp", 64, 16, 6000, "f32"),
+    ("zipf_mixed_temp", 40, 7, 1001, "bf16"),   # rows not 16-byte aligned
+    ("zipf_mixed_noise", 17, 3, 333, "f32"),
+    ("zipf_adaptive", 5, 1, 9, "bf16"),
+]
+
+
+@pytest.mark.parametrize("recipe,B,k,V,dtype", SMALL)
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_verify_small_matches_oracle(recipe, B, k, V, dtype, seed):
+    inp = synth.make_inputs(recipe, B, k, V, dtype, seed=seed)
+    check(inp, f"{recipe} B={B} k={k} V={V} {dtype} seed={seed}")
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_verify_full_workloads_match_oracle(name):
+    inp = synth.make_workload(name)
+    info, rep, o = check(inp, name)
+    # Every row the oracle needed was swept, and no more than the plan.
+    assert rep.rows_planned == int(np.sum(np.where(inp.temperature == 0, 1, 2) * inp.lengths))
+    assert rep.chunks_swept <= rep.rows_planned * rep.chunks_per_row
+
+
+@pytest.mark.parametrize("name", ["b128_k16_v151936_bf16_zipf_mixed_noise"])
+def test_full_sweep_flag_gives_same_outputs(name):
+    inp = synth.make_workload(name, seed=777)
+    a_out, a_n, a_rep = run_gpu(inp)
+    b_out, b_n, b_rep = run_gpu(inp, full_sweep=True)
+    np.testing.assert_array_equal(a_out, b_out)
+    np.testing.assert_array_equal(a_n, b_n)
+    assert b_rep.chunks_swept == b_rep.rows_planned * b_rep.chunks_per_row
+    assert a_rep.chunks_swept <= b_rep.chunks_swept
+
+
+def test_repeated_calls_are_deterministic_and_reuse_workspace():
+    inp = synth.make_inputs("zipf_mixed_temp", 48, 16, 20000, "bf16", seed=5)
+    small = synth.make_inputs("gauss", 2, 4, 300, "bf16", seed=6)
+    ws = sv.alloc_workspace(48, 16, 20000)
+    a = run_gpu(inp, workspace=ws)
+    run_gpu(small, workspace=ws)  # a different, smaller call on the same workspace
+    b = run_gpu(inp, workspace=ws)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+# ---------------------------------------------------------------------------
+# Edge cases
+# ---------------------------------------------------------------------------
+
+def _inputs(B, k, V, dtype="f32", seed=0, T=1.0):
+    rng = np.random.default_rng(seed)
+    tl = rng.standard_normal((B, k + 1, V)).astype(np.float32)
+    dl = (tl[:, :k] + rng.standard_normal((B, k, V)) * 0.7).astype(np.float32)
+    inp = synth.SpecInputs(tl, dl, rng.integers(0, V, (B, k)).astype(np.int32),
+                           np.full(B, k, np.int32), synth.uniform_24bit(rng, (B, k + 1)),
+                           np.full(B, T, np.float32), "f32")
+    if dtype == "bf16":
+        inp.target, inp.draft, inp.dtype = synth.bf16_bits(tl), synth.bf16_bits(dl), "bf16"
+    return inp
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_p_equals_q_always_accepts(dtype):
+    inp = _inputs(64, 8, 3000, dtype, seed=1)
+    inp.draft = inp.target[:, :8].copy()
+    inp.uniforms[:, :8] = np.float32(1.0 - 2.0**-24)
+    inp.lengths = np.random.default_rng(2).integers(1, 9, 64).astype(np.int32)
+    out, n, _ = run_gpu(inp)
+    np.testing.assert_array_equal(n, inp.lengths)
+    check(inp, "p == q")
+
+
+def test_single_token_vocabulary():
+    inp = _inputs(4, 3, 1)
+    inp.tokens[:] = 0
+    out, n, _ = run_gpu(inp)
+    assert np.all(n == 3) and np.all(out == 0)
+
+
+def test_greedy_ties_and_worked_example_structure():
+    B, k, V = 3, 8, 64
+    tl = np.zeros((B, k + 1, V), np.float32)
+    tl[:, :, 10] = 1.0
+    tl[:, :, 40] = 1.0                   # tie: argmax is 10
+    tl[0, 4, 10] = 0.0                   # request 0: position 4 prefers 40
+    dl = np.zeros((B, k, V), np.float32)
+    tok = np.full((B, k), 10, np.int32)
+    inp = synth.SpecInputs(tl, dl, tok, np.array([8, 8, 3], np.int32),
+                           np.full((B, k + 1), np.nan, np.float32), np.zeros(B, np.float32), "f32")
+    out, n, rep = run_gpu(inp)
+    assert n.tolist() == [4, 8, 3]
+    assert out[0].tolist() == [10, 10, 10, 10, 40, -1, -1, -1, -1]
+    assert out[1].tolist() == [10] * 9
+    assert out[2].tolist() == [10, 10, 10, 10, -1, -1, -1, -1, -1]
+    assert rep.status == sv.SPEC_OK
+
+
+def test_disjoint_supports_and_masked_logits():
+    inp = _inputs(50, 4, 512, "f32", seed=3)
+    inp.target[:, :, 256:] = -np.inf
+    inp.draft[:, :, :256] = -np.inf
+    inp.tokens[:] = np.random.default_rng(4).integers(256, 512, inp.tokens.shape)
+    out, n, _ = run_gpu(inp)
+    assert np.all(n == 0)
+    check(inp, "disjoint supports")
+
+
+@pytest.mark.parametrize("field", ["length0", "length_big", "token", "uniform", "temp_neg",
+                                   "temp_nan", "temp_subnormal", "nan_logit_reached"])
+def test_invalid_inputs_flagged_on_device(field):
+    inp = _inputs(6, 4, 700, "bf16", seed=7)
+    if field == "length0":
+        inp.lengths[2] = 0
+    elif field == "length_big":
+        inp.lengths[2] = 5
+    elif field == "token":
+        inp.tokens[2, 1] = 700
+    elif field == "uniform":
+        inp.uniforms[2, 4] = 1.0
+    elif field == "temp_neg":
+        inp.temperature[2] = -0.5
+    elif field == "temp_nan":
+        inp.temperature[2] = np.nan
+    elif field == "temp_subnormal":
+        inp.temperature[2] = 1e-40
+    else:
+        inp.target[2, 0, 5] = 0x7FC0  # bf16 NaN in a row every round reads
+    out, n, rep = run_gpu(inp)
+    o = oracle.verify(inp.target, inp.draft, inp.tokens, inp.lengths, inp.uniforms, inp.temperature)
+    assert n[2] == -1 and np.all(out[2] == -1)
+    assert o.num_accepted[2] == -1
+    assert rep.status == sv.SPEC_ERR_BAD_INPUT and rep.bad_requests == 1
+    assert rep.first_bad_request == 2
+    keep = np.arange(6) != 2
+    np.testing.assert_array_equal(n[keep], o.num_accepted[keep])
+
+
+def test_host_argument_errors_launch_nothing():
+    inp = _inputs(2, 3, 64)
+    d = sv.to_device(inp)
+    ws = sv.alloc_workspace(2, 3, 64)
+    L = sv.lib()
+    args = [d["target_logits"].data_ptr(), d["draft_logits"].data_ptr(), sv.SPEC_F32,
+            d["draft_tokens"].data_ptr(), d["lengths"].data_ptr(), d["uniforms"].data_ptr(),
+            d["temperature"].data_ptr(), 2, 3, 64, 0, 0, ws.data_ptr(), ws.numel(), 0]
+    out = torch.empty((2, 4), dtype=torch.int32, device="cuda")
+    n = torch.empty(2, dtype=torch.int32, device="cuda")
+    args[10], args[11] = out.data_ptr(), n.data_ptr()
+    assert L.spec_verify(*args) == sv.SPEC_OK
+    bad = list(args); bad[13] = 16
+    assert L.spec_verify(*bad) == sv.SPEC_ERR_WORKSPACE
+    bad = list(args); bad[0] = 0
+    assert L.spec_verify(*bad) == sv.SPEC_ERR_INVALID_ARG
+    bad = list(args); bad[8] = 40
+    assert L.spec_verify(*bad) == sv.SPEC_ERR_UNSUPPORTED
+    bad = list(args); bad[0] += 1
+    assert L.spec_verify(*bad) == sv.SPEC_ERR_INVALID_ARG
+    torch.cuda.synchronize()
