@@ -57,6 +57,7 @@ extern "C" {
 #define SPEC_VERIFY_ABI_VERSION 1
 
 /* Largest supported sizes. */
+#define SPEC_MAX_B (1 << 18)   /* requests per call */
 #define SPEC_MAX_K 31          /* draft positions per request (decisions are 32-bit masks) */
 #define SPEC_MAX_V (1 << 21)   /* vocabulary size */
 

@@ -20,10 +20,13 @@ constexpr double kLn2 = 0.69314718055994530942;
 
 // Sweep kernel geometry.
 constexpr int kSweepConsumerWarps = 8;
-constexpr int kSweepThreads = (kSweepConsumerWarps + 1) * 32;  // + one producer warp
+// + one producer warp (lane 0 issues the bulk copies) + one bookkeeping warp
+// (unit partials, completion counters, accept decisions).
+constexpr int kSweepThreads = (kSweepConsumerWarps + 2) * 32;
 constexpr int kStageBytes = 16384;
-constexpr int kStages = 6;
-constexpr int kRedDepth = kStages + 2;  // unit-end reduction slots in flight
+constexpr int kStages = 4;
+constexpr int kSweepMinBlocks = 3;  // CTAs per SM the register budget is sized for
+constexpr int kRedDepth = 8;  // unit-end reduction slots in flight
 
 // Final-pass kernel geometry.
 constexpr int kFinalThreads = 1024;
@@ -58,15 +61,18 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte block");
 
 // Per-unit partial result of the sweep: softmax (m, s) or argmax (m, arg).
-struct __align__(16) Partial {
-  float m;    // largest logit of the chunk
-  float s;    // sum of 2^(z*sc - fl(m*sc)) over the chunk (sampling rows)
-  int arg;    // lowest index attaining m (greedy rows)
-  int pad;
+// One 8-byte word, written and read in a single access, so that a reader on
+// another SM sees either the whole partial or the empty marker.
+struct __align__(8) Partial {
+  float m;       // largest logit of the chunk
+  uint32_t aux;  // sampling rows: bits of s = sum 2^(z*sc - fl(m*sc)); greedy rows: lowest index of m
 };
+// What a partial slot holds from the plan kernel until its unit is stored: m
+// is a NaN, which no chunk max can be (max-reductions skip NaN logits).
+constexpr unsigned long long kPartialEmpty = 0x7FC0DEAD7FC0DEADull;
 
 struct WsLayout {
-  size_t header, rowlist, flags, first_reject, acc_bits, dec_bits, bad_bits, done, pos_c, pos_arg,
+  size_t header, rowdesc, flags, first_reject, acc_bits, dec_bits, bad_bits, done, pos_c, pos_arg,
       partials, total;
 };
 
@@ -75,7 +81,7 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 // Vocabulary chunks per row: enough units to keep every SM busy when all
 // rows are active, chunks of at least 2048 elements.
 __host__ __device__ inline int chunks_per_row(long long rows_max, int V) {
-  long long want = (16384 + rows_max - 1) / rows_max;
+  long long want = (8192 + rows_max - 1) / rows_max;
   long long maxc = (V + 2047) / 2048;
   if (maxc < 1) maxc = 1;
   if (want > maxc) want = maxc;
@@ -94,7 +100,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int k, int C) {
   size_t o = 0;
   size_t slots = (size_t)B * (size_t)k * 2;
   l.header = o;       o = align256(o + sizeof(WsHeader));
-  l.rowlist = o;      o = align256(o + slots * sizeof(int32_t));
+  l.rowdesc = o;      o = align256(o + slots * sizeof(int2));
   l.flags = o;        o = align256(o + (size_t)B * sizeof(int32_t));
   l.first_reject = o; o = align256(o + (size_t)B * sizeof(int32_t));
   l.acc_bits = o;     o = align256(o + (size_t)B * sizeof(uint32_t));
@@ -208,6 +214,83 @@ __device__ __forceinline__ void soft_add(SoftAcc& a, const float* x, float sc) {
 
 __device__ __forceinline__ void soft_add1(SoftAcc& a, float x, float sc) { soft_add<1>(a, &x, sc); }
 
+// Packed two-lane arithmetic (bf16x2 max; f32x2 FMA / add, sm_100 and later):
+// one instruction does the work of two.
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ float2 f32x2_fma(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 f32x2_add(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 ex2x2(float2 y) { return make_float2(ex2(y.x), ex2(y.y)); }
+
+// Fold one 16-byte vector of logits into a softmax accumulator: packed max
+// to find a new running max, packed FMA for z*sc - ms, one ex2 per element,
+// packed pairwise sums.
+template <typename TIn>
+__device__ __forceinline__ void soft_add_vec(SoftAcc& a, const uint4& v, float sc);
+
+template <>
+__device__ __forceinline__ void soft_add_vec<uint16_t>(SoftAcc& a, const uint4& v, float sc) {
+  const uint32_t mx = bf16x2_max(bf16x2_max(v.x, v.y), bf16x2_max(v.z, v.w));
+  const float gm = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xffff0000u));
+  if (gm > a.m) {
+    const float nms = __fmul_rn(gm, sc);
+    a.s = __fmul_rn(a.s, ex2(__fsub_rn(a.ms, nms)));
+    a.m = gm;
+    a.ms = nms;
+  }
+  const float2 s2 = make_float2(sc, sc), c2 = make_float2(-a.ms, -a.ms);
+  const float2 e0 = ex2x2(f32x2_fma(
+      make_float2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u)), s2, c2));
+  const float2 e1 = ex2x2(f32x2_fma(
+      make_float2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u)), s2, c2));
+  const float2 e2 = ex2x2(f32x2_fma(
+      make_float2(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u)), s2, c2));
+  const float2 e3 = ex2x2(f32x2_fma(
+      make_float2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u)), s2, c2));
+  const float2 t = f32x2_add(f32x2_add(e0, e1), f32x2_add(e2, e3));
+  a.s = __fadd_rn(a.s, __fadd_rn(t.x, t.y));
+}
+
+template <>
+__device__ __forceinline__ void soft_add_vec<float>(SoftAcc& a, const uint4& v, float sc) {
+  const float x0 = __uint_as_float(v.x), x1 = __uint_as_float(v.y);
+  const float x2 = __uint_as_float(v.z), x3 = __uint_as_float(v.w);
+  const float gm = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+  if (gm > a.m) {
+    const float nms = __fmul_rn(gm, sc);
+    a.s = __fmul_rn(a.s, ex2(__fsub_rn(a.ms, nms)));
+    a.m = gm;
+    a.ms = nms;
+  }
+  const float2 s2 = make_float2(sc, sc), c2 = make_float2(-a.ms, -a.ms);
+  const float2 e0 = ex2x2(f32x2_fma(make_float2(x0, x1), s2, c2));
+  const float2 e1 = ex2x2(f32x2_fma(make_float2(x2, x3), s2, c2));
+  const float2 t = f32x2_add(e0, e1);
+  a.s = __fadd_rn(a.s, __fadd_rn(t.x, t.y));
+}
+
 __device__ __forceinline__ void soft_merge(SoftAcc& a, const SoftAcc& b) {
   if (b.m > a.m) {
     a.s = __fadd_rn(__fmul_rn(a.s, ex2(__fsub_rn(a.ms, b.ms))), b.s);
@@ -282,51 +365,6 @@ __device__ __forceinline__ double warp_sum_f64(double x) {
 }
 
 // ---------------------------------------------------------------------------
-// Combine the chunk partials of one row into its base-2 log normaliser
-// c = fl(M*sc) + log2(S), where M is the row max and
-// S = sum_v 2^(z_v*sc - fl(M*sc)); log2 p(v) = z_v*sc - c.  Warp-cooperative:
-// every lane returns the same value.  Returns false if the row has no finite
-// mass (all -inf, or a NaN / +inf logit made S non-finite).
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ bool row_log2_normaliser(const Partial* parts, int nch, float sc,
-                                                    double* c_out, float* max_out) {
-  const int lane = threadIdx.x & 31;
-  float m = -FLT_MAX;
-  for (int c = lane; c < nch; c += 32) m = fmaxf(m, __ldcg(&parts[c].m));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  const float msM = __fmul_rn(m, sc);
-  double S = 0.0;
-  for (int c = lane; c < nch; c += 32) {
-    float mc = __ldcg(&parts[c].m);
-    float sc_c = __ldcg(&parts[c].s);
-    if (sc_c > 0.0f) S += (double)sc_c * exp2((double)__fmul_rn(mc, sc) - (double)msM);
-    else if (!(sc_c == 0.0f)) S = __longlong_as_double(0x7ff8000000000000ll);  // NaN
-  }
-  S = warp_sum_f64(S);
-  *c_out = (double)msM + log2(S);
-  *max_out = m;
-  return S > 0.0 && S <= 1.79e308;
-}
-
-__device__ __forceinline__ void row_argmax_from_parts(const Partial* parts, int nch, float* v_out,
-                                                      int* i_out) {
-  const int lane = threadIdx.x & 31;
-  ArgAcc a;
-  arg_init(a);
-  for (int c = lane; c < nch; c += 32) {
-    ArgAcc b;
-    b.v = __ldcg(&parts[c].m);
-    b.i = __ldcg(&parts[c].arg);
-    arg_merge(a, b);
-  }
-  arg_warp_reduce(a);
-  *v_out = a.v;
-  *i_out = a.i;
-}
-
-// ---------------------------------------------------------------------------
 // Inline PTX: mbarrier, bulk async copy, programmatic dependent launch.
 // ---------------------------------------------------------------------------
 
@@ -358,6 +396,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking probe: has the phase with this parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_addr(bar)), "r"(parity)
@@ -403,6 +454,189 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 
 __device__ __forceinline__ void record_status(WsHeader* h, int code) {
   atomicCAS(&h->status, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// Partials: single 8-byte relaxed stores and loads.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void store_partial(Partial* p, float m, uint32_t aux) {
+  const unsigned long long v = ((unsigned long long)aux << 32) | __float_as_uint(m);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long load_u64_relaxed(const void* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Read a partial, waiting (bounded) while its slot still holds the empty
+// marker: its unit has been counted, so its store is already on its way.
+// Returns false if the wait ran out.
+__device__ __forceinline__ bool load_partial(const Partial* p, float* m, uint32_t* aux) {
+  unsigned long long v = load_u64_relaxed(p);
+  if (v == kPartialEmpty) {
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+      __nanosleep(64);
+      v = load_u64_relaxed(p);
+      if (v != kPartialEmpty) break;
+      if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+  *m = __uint_as_float((uint32_t)v);
+  *aux = (uint32_t)(v >> 32);
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// Combine the chunk partials of one row into its base-2 log normaliser
+// c = fl(M*sc) + log2(S), where M is the row max and
+// S = sum_v 2^(z_v*sc - fl(M*sc)); log2 p(v) = z_v*sc - c.  Warp-cooperative:
+// every lane returns the same value.  Returns false if the row has no finite
+// mass (all -inf, or a NaN / +inf logit made S non-finite) or if a partial
+// never arrived (*timed_out).
+// ---------------------------------------------------------------------------
+
+// log2 of a positive double: exact exponent, single-precision log2 of the
+// mantissa in [0.5, 1) (absolute error below 1e-7).  Non-positive or
+// non-finite input gives a non-finite result.
+__device__ __forceinline__ double log2_pos(double S) {
+  if (!(S > 0.0) || !(S <= 1.79e308)) return log2f((float)S);
+  int e;
+  const double mant = frexp(S, &e);
+  return (double)e + (double)log2f((float)mant);
+}
+
+// One chunk's sum rescaled to the row reference ms_ref = fl(M*sc):
+// s_c * 2^(fl(m_c*sc) - ms_ref), the difference taken exactly in double and
+// the power in single precision (the dominant chunk gets exactly 1).
+__device__ __forceinline__ double chunk_term(float m_c, uint32_t s_bits, float sc, float ms_ref) {
+  const float s_c = __uint_as_float(s_bits);
+  if (s_c > 0.0f) {
+    const float d = (float)((double)__fmul_rn(m_c, sc) - (double)ms_ref);
+    return (double)s_c * (double)exp2f(d);
+  }
+  return s_c == 0.0f ? 0.0 : __longlong_as_double(0x7ff8000000000000ll);  // NaN stays NaN
+}
+
+__device__ __forceinline__ bool row_log2_normaliser(const Partial* parts, int nch, float sc,
+                                                    double* c_out, float* max_out,
+                                                    bool* timed_out) {
+  const int lane = threadIdx.x & 31;
+  bool late = false;
+  float m = -FLT_MAX;
+  for (int c = lane; c < nch; c += 32) {
+    float mc;
+    uint32_t aux;
+    if (load_partial(&parts[c], &mc, &aux)) m = fmaxf(m, mc);
+    else late = true;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  const float msM = __fmul_rn(m, sc);
+  double S = 0.0;
+  for (int c = lane; c < nch; c += 32) {
+    float mc;
+    uint32_t aux;
+    if (!load_partial(&parts[c], &mc, &aux)) {
+      late = true;
+      continue;
+    }
+    S += chunk_term(mc, aux, sc, msM);
+  }
+  S = warp_sum_f64(S);
+  late = __any_sync(0xffffffffu, late);
+  *timed_out = late;
+  *c_out = (double)msM + log2_pos(S);
+  *max_out = m;
+  return !late && S > 0.0 && S <= 1.79e308;
+}
+
+// Both rows of a sampling position at once: parts[0, nch) are the target
+// row's chunk partials and parts[nch, 2 nch) the draft row's (they are
+// adjacent in the workspace).  Every partial is loaded in one round and kept
+// in registers while 2 nch <= 32 * kMaxPartsPerLane.
+constexpr int kMaxPartsPerLane = 8;
+
+__device__ __forceinline__ void pair_log2_normalisers(const Partial* parts, int nch, float sc,
+                                                      double* ct, double* cd, bool* ok_t,
+                                                      bool* ok_d, bool* timed_out) {
+  const int lane = threadIdx.x & 31;
+  const int n2 = 2 * nch;
+  if (n2 > 32 * kMaxPartsPerLane) {
+    float mt, md;
+    bool lt, ld;
+    *ok_t = row_log2_normaliser(parts, nch, sc, ct, &mt, &lt);
+    *ok_d = row_log2_normaliser(parts + nch, nch, sc, cd, &md, &ld);
+    *timed_out = lt || ld;
+    return;
+  }
+  float m[kMaxPartsPerLane];
+  uint32_t a[kMaxPartsPerLane];
+  bool late = false;
+  float mt = -FLT_MAX, md = -FLT_MAX;
+#pragma unroll
+  for (int j = 0; j < kMaxPartsPerLane; ++j) {
+    const int e = lane + 32 * j;
+    m[j] = -FLT_MAX;
+    a[j] = 0u;
+    if (e < n2) {
+      if (!load_partial(&parts[e], &m[j], &a[j])) {
+        late = true;
+        m[j] = -FLT_MAX;
+        a[j] = 0u;
+      }
+      if (e < nch) mt = fmaxf(mt, m[j]);
+      else md = fmaxf(md, m[j]);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+    md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, off));
+  }
+  const float msT = __fmul_rn(mt, sc), msD = __fmul_rn(md, sc);
+  double St = 0.0, Sd = 0.0;
+#pragma unroll
+  for (int j = 0; j < kMaxPartsPerLane; ++j) {
+    const int e = lane + 32 * j;
+    if (e < nch) St += chunk_term(m[j], a[j], sc, msT);
+    else if (e < n2) Sd += chunk_term(m[j], a[j], sc, msD);
+  }
+  St = warp_sum_f64(St);
+  Sd = warp_sum_f64(Sd);
+  late = __any_sync(0xffffffffu, late);
+  *timed_out = late;
+  *ct = (double)msT + log2_pos(St);
+  *cd = (double)msD + log2_pos(Sd);
+  *ok_t = !late && St > 0.0 && St <= 1.79e308;
+  *ok_d = !late && Sd > 0.0 && Sd <= 1.79e308;
+}
+
+// Max and lowest index of a greedy row from its chunk partials.
+__device__ __forceinline__ void row_argmax_from_parts(const Partial* parts, int nch, float* v_out,
+                                                      int* i_out, bool* timed_out) {
+  const int lane = threadIdx.x & 31;
+  bool late = false;
+  ArgAcc a;
+  arg_init(a);
+  for (int c = lane; c < nch; c += 32) {
+    ArgAcc b;
+    uint32_t aux;
+    if (!load_partial(&parts[c], &b.v, &aux)) {
+      late = true;
+      continue;
+    }
+    b.i = (int)aux;
+    arg_merge(a, b);
+  }
+  arg_warp_reduce(a);
+  late = __any_sync(0xffffffffu, late);
+  *timed_out = late;
+  *v_out = a.v;
+  *i_out = late ? INT32_MAX : a.i;
 }
 
 }  // namespace specv

@@ -137,7 +137,7 @@ __device__ bool row_normaliser_cta(const TIn* row, int V, float sc, FinalShared&
     soft_warp_reduce(r);
     if (lane == 0) {
       const double S = (double)r.s;
-      sh.c = (double)r.ms + log2(S);
+      sh.c = (double)r.ms + log2_pos(S);
       sh.bad = !(S > 0.0 && S <= 3.4e38);
     }
   }

@@ -19,9 +19,25 @@ namespace specv {
 // Row-statistics kernels (spec_row_stats).
 // ---------------------------------------------------------------------------
 
+WsLayout stats_layout(int rows, int C) {
+  WsLayout l = {};
+  l.header = 0;
+  l.rowdesc = align256(sizeof(WsHeader));
+  l.partials = l.rowdesc + align256((size_t)rows * sizeof(int2));
+  l.total = l.partials + align256((size_t)rows * C * sizeof(Partial));
+  return l;
+}
+
+// Row descriptors {row, bits of log2(e)/T} for the sweep, and the header.
 __global__ void stats_plan_kernel(unsigned char* ws, WsLayout lay, int rows, int nch,
-                                  int chunk_elems) {
+                                  int chunk_elems, const float* temperature) {
   pdl_launch_dependents();
+  int2* rowdesc = reinterpret_cast<int2*>(ws + lay.rowdesc);
+  for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x) {
+    const float T = temperature[r];
+    rowdesc[r] = make_int2(r, __float_as_int(T == 0.0f ? 0.0f : softmax_scale(T)));
+  }
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
   WsHeader* h = reinterpret_cast<WsHeader*>(ws + lay.header);
   h->status = SPEC_OK;
   h->bad_requests = 0;
@@ -52,7 +68,8 @@ __global__ void stats_finalize_kernel(const unsigned char* ws, WsLayout lay, int
   if (T == 0.0f) {
     float v;
     int g;
-    row_argmax_from_parts(parts, nch, &v, &g);
+    bool late;
+    row_argmax_from_parts(parts, nch, &v, &g, &late);
     if (lane == 0) {
       row_max[r] = v;
       row_lse[r] = __int_as_float(0x7fc00000);
@@ -62,7 +79,8 @@ __global__ void stats_finalize_kernel(const unsigned char* ws, WsLayout lay, int
     const float sc = softmax_scale(T);
     double c;
     float m;
-    const bool ok = row_log2_normaliser(parts, nch, sc, &c, &m);
+    bool late;
+    const bool ok = row_log2_normaliser(parts, nch, sc, &c, &m, &late);
     if (lane == 0) {
       row_max[r] = m;
       row_lse[r] = ok ? (float)(c * kLn2) : __int_as_float(0x7fc00000);
@@ -151,7 +169,7 @@ cudaError_t record(void* const* ev, int j, cudaStream_t stream) {
 
 bool sizes_ok(int B, int k, int V) {
   if (B < 1 || k < 1 || V < 1) return false;
-  if (k > SPEC_MAX_K || V > SPEC_MAX_V) return false;
+  if (B > SPEC_MAX_B || k > SPEC_MAX_K || V > SPEC_MAX_V) return false;
   // Row slots (b*k + i) * 2 + tensor and work units must fit in int32.
   const long long slots = 2LL * B * k;
   if (slots * (long long)chunks_per_row(slots, V) >= (1LL << 31)) return false;
@@ -215,7 +233,6 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
   sp.draft = draft_logits;
   sp.tokens = draft_tokens;
   sp.uniforms = uniforms;
-  sp.temperature = temperature;
   sp.B = B;
   sp.k = k;
   sp.V = V;
@@ -266,18 +283,14 @@ spec_status_t row_stats_typed(const void* logits, int rows, int V, const float* 
   const int C = chunks_per_row(rows, V);
   const int ce = chunk_elems_for(V, C);
   const int nch = (V + ce - 1) / ce;
-  // Stats mode keeps partials at row * nch + chunk: the layout of a batch of
-  // `rows` slots.
-  WsLayout lay = ws_layout(1, 1, 1);
-  lay.partials = align256(sizeof(WsHeader));
-  lay.total = lay.partials + align256((size_t)rows * C * sizeof(Partial));
+  // Stats mode: header, one descriptor per row, partials at row * nch + chunk.
+  const WsLayout lay = stats_layout(rows, C);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  if (launch(stats_plan_kernel, dim3(1), dim3(1), 0, stream, false, ws, lay, rows, nch, ce) !=
-      cudaSuccess)
+  if (launch(stats_plan_kernel, dim3((rows + 255) / 256), dim3(256), 0, stream, false, ws, lay,
+             rows, nch, ce, temperature) != cudaSuccess)
     return SPEC_ERR_CUDA;
   SweepParams sp = {};
   sp.target = logits;
-  sp.temperature = temperature;
   sp.B = rows;
   sp.k = 1;
   sp.V = V;
@@ -299,10 +312,7 @@ spec_status_t row_stats_typed(const void* logits, int rows, int V, const float* 
   return SPEC_OK;
 }
 
-size_t row_stats_ws_bytes(int rows, int V) {
-  const int C = chunks_per_row(rows, V);
-  return align256(sizeof(WsHeader)) + align256((size_t)rows * C * sizeof(Partial));
-}
+size_t row_stats_ws_bytes(int rows, int V) { return stats_layout(rows, chunks_per_row(rows, V)).total; }
 
 }  // namespace specv
 

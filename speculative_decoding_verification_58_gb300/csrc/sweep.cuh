@@ -5,20 +5,25 @@
 // vocabulary: AdaFlash Section 2.1); for a greedy row (T == 0) the max and
 // its lowest index (DFlash notes, section 5.2, worked example #4).
 //
-// Persistent, warp-specialised CTAs.  Lane 0 of the producer warp claims
-// work units (one vocabulary chunk of one row) from a global counter and
-// streams each chunk into a ring of shared-memory stages with 1-D bulk async
-// copies (cp.async.bulk, completion on an mbarrier).  Eight consumer warps
-// read the stages with 16-byte shared loads, fold them into per-thread
-// accumulators, and at the end of a unit reduce them with warp shuffles and
-// one mbarrier-guarded exchange; warp 0 writes the unit's partial.
+// Persistent, warp-specialised CTAs:
+//   - lane 0 of the producer warp claims work units (one vocabulary chunk of
+//     one row) from a global counter and streams each chunk into a ring of
+//     shared-memory stages with 1-D bulk async copies (cp.async.bulk,
+//     completion counted on an mbarrier);
+//   - eight consumer warps copy their share of a stage into registers, free
+//     the stage, take one packed max over it, rescale at most once, and then
+//     do independent FMA / ex2 / adds (or an argmax) on it;
+//   - at the end of a unit the consumer warps leave their warp-reduced
+//     accumulators in shared memory for the bookkeeping warp, which merges
+//     them, stores the unit's partial and, in verification mode, does the
+//     global counting and the accept decision, off the consumers' path.
 //
-// Verification mode also decides: the CTA that completes the last chunk of
-// (request b, position i) combines the partials, gathers p(x_i) and q(x_i),
-// and applies the accept test u_i < min(1, p(x_i)/q(x_i)) (or argmax == x_i at
-// T == 0) in double precision.  A rejection is published in first_reject[b];
-// the producer skips chunks of positions behind a known rejection, since
-// only tokens before the first rejection are kept (AdaFlash Section 2.1).
+// Verification mode: the CTA that completes the last chunk of (request b,
+// position i) combines the partials, gathers p(x_i) and q(x_i), and applies
+// the accept test u_i < min(1, p(x_i)/q(x_i)) (or argmax == x_i at T == 0) in
+// double precision.  A rejection is published in first_reject[b]; the
+// producer skips chunks of positions behind a known rejection, since only
+// tokens before the first rejection are kept (AdaFlash Section 2.1).
 #pragma once
 
 #include "common.cuh"
@@ -30,7 +35,6 @@ struct SweepParams {
   const void* draft;         // verify: [B, k, V]
   const int32_t* tokens;     // [B, k]
   const float* uniforms;     // [B, k+1]
-  const float* temperature;  // verify: [B]; stats: [rows]
   int B, k, V, nch, chunk_elems;
   int early_exit;
   unsigned char* ws;
@@ -51,15 +55,32 @@ struct StageInfo {
   int slot;         // row slot ((b*k+i)<<1 | tensor) or row index
 };
 
+// What the bookkeeping warp needs to know about a finished unit.
+struct UnitMeta {
+  int part;
+  int slot;
+  int flags;
+  float sc;
+};
+
 constexpr int kNC = kSweepConsumerWarps;
 constexpr int kNCT = kNC * 32;
+constexpr int kProducerWarp = kNC;
+constexpr int kBookWarp = kNC + 1;
+constexpr int kVecPerThread = kStageBytes / 16 / kNCT;  // 16-byte vectors per consumer thread
+static_assert(kSweepThreads == (kNC + 2) * 32, "kNC consumer warps + producer + bookkeeping");
+static_assert(kStageBytes % (16 * kNCT) == 0, "a stage splits evenly over the consumer threads");
+static_assert((kVecPerThread & (kVecPerThread - 1)) == 0, "batch_max reduces a power-of-two batch");
+static_assert(kNC <= 32, "unit-end merge gives one lane of the bookkeeping warp per consumer warp");
 
 struct SweepSmem {
   alignas(128) unsigned char stage[kStages][kStageBytes];
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t red_bar[kRedDepth];
+  uint64_t full[kStages];        // 1 arrival + bulk bytes: stage loaded
+  uint64_t empty[kStages];       // kNC arrivals: stage copied into registers
+  uint64_t red_bar[kRedDepth];   // kNC arrivals: unit accumulators posted
+  uint64_t red_free[kRedDepth];  // 1 arrival: bookkeeping warp has read the slot
   StageInfo info[kStages];
+  UnitMeta meta[kRedDepth];
   float4 red[kRedDepth][kNC];
   int abort_flag;
 };
@@ -70,17 +91,26 @@ __device__ __forceinline__ void sweep_abort(WsHeader* h, SweepSmem& sm) {
 }
 
 // ---------------------------------------------------------------------------
-// Producer: one thread.
+// Producer: one warp.  The warp claims a few consecutive units per atomic,
+// resolves their descriptors and skip checks with one lane per unit, and
+// claims the next batch before lane 0 issues this batch's bulk copies, so the
+// claim's round trip overlaps the copy issue.  Near the end of the work list
+// it claims single units so that the CTAs finish together.
 // ---------------------------------------------------------------------------
+constexpr int kClaim = 4;
+
 template <typename TIn, bool kVerify>
 __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h) {
   using Tr = ElemTraits<TIn>;
-  const int32_t* rowlist = reinterpret_cast<const int32_t*>(p.ws + p.lay.rowlist);
+  const int lane = threadIdx.x & 31;
+  const int2* rowdesc = reinterpret_cast<const int2*>(p.ws + p.lay.rowdesc);
   const int32_t* first_reject = reinterpret_cast<const int32_t*>(p.ws + p.lay.first_reject);
   const int units_total = __ldcg(&h->units_total);
+  const int small_after = units_total - 4 * kClaim * (int)gridDim.x;
   volatile int* abort_flag = &sm.abort_flag;
-  int it = 0;
+  int it = 0;  // stages issued (lane 0)
   bool ok = true;
+  unsigned long long my_chunks = 0, my_bytes = 0;
 
   auto acquire = [&](int& s) -> bool {
     s = it % kStages;
@@ -92,75 +122,138 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
     return true;
   };
 
-  for (;;) {
-    const int u = atomicAdd(&h->work_next, 1);
-    if (u >= units_total) break;
-    const int row = u / p.nch;
-    const int chunk = u - row * p.nch;
-    const int slot = kVerify ? __ldcg(&rowlist[row]) : row;
-    const TIn* rowp;
-    float T;
-    if (kVerify) {
-      const int bi = slot >> 1;
-      const int b = bi / p.k;
-      const int i = bi - b * p.k;
-      if (p.early_exit && *(volatile const int32_t*)&first_reject[b] < i) continue;
-      T = __ldg(&p.temperature[b]);
-      rowp = (slot & 1)
-                 ? static_cast<const TIn*>(p.draft) + ((size_t)b * p.k + i) * (size_t)p.V
-                 : static_cast<const TIn*>(p.target) + ((size_t)b * (p.k + 1) + i) * (size_t)p.V;
-    } else {
-      T = __ldg(&p.temperature[slot]);
-      rowp = static_cast<const TIn*>(p.target) + (size_t)slot * (size_t)p.V;
+  // Batches move through a three-deep pipeline: claimed (atomic in flight),
+  // described (row descriptors loaded, one lane per unit), checked (skip
+  // flag loaded), then issued.  Each step consumes values loaded one loop
+  // iteration earlier, so no global round trip stands in front of a copy.
+  auto want_at = [&](int base) { return base < small_after ? kClaim : 1; };
+  auto claim = [&](int want) {
+    int v = 0;
+    if (lane == 0) v = atomicAdd(&h->work_next, want);
+    return v;  // lane 0 only; broadcast when needed
+  };
+  auto describe = [&](int base, int want) {
+    int2 rd = make_int2(-1, 0);
+    if (lane < want && base + lane < units_total) rd = __ldcg(&rowdesc[(base + lane) / p.nch]);
+    return rd;
+  };
+  auto check = [&](int2 rd) {  // first known rejection of the unit's request, or k
+    int fr = INT32_MAX;
+    if (kVerify && p.early_exit && rd.x >= 0) {
+      const int b = (rd.x >> 1) / p.k;
+      fr = *(volatile const int32_t*)&first_reject[b];
     }
-    const bool greedy = (T == 0.0f);
-    const float sc = greedy ? 0.0f : softmax_scale(T);
+    return fr;
+  };
 
-    // Element range of the chunk and its 16-byte aligned core.
-    const int e0 = chunk * p.chunk_elems;
-    const int e1 = min(p.V, e0 + p.chunk_elems);
-    const uintptr_t addr0 = reinterpret_cast<uintptr_t>(rowp + e0);
-    int a0 = e0 + (int)(((16u - (unsigned)(addr0 & 15u)) & 15u) / Tr::kSize);
-    if (a0 > e1) a0 = e1;
-    const int core_bytes = (((e1 - a0) * Tr::kSize) & ~15);
-    const int a1 = a0 + core_bytes / Tr::kSize;
-    const int nstage = core_bytes > 0 ? (core_bytes + kStageBytes - 1) / kStageBytes : 1;
-    const char* src0 = reinterpret_cast<const char*>(rowp + a0);
-    atomicAdd(&h->chunks_swept, 1ull);
-    atomicAdd(&h->sweep_bytes, (unsigned long long)(e1 - e0) * Tr::kSize);
+  int wantC = want_at(0);
+  int baseC = __shfl_sync(0xffffffffu, claim(wantC), 0);
+  int2 rdC = describe(baseC, wantC);
+  int frC = check(rdC);
+  int wantB = want_at(baseC + wantC);
+  int baseB = __shfl_sync(0xffffffffu, claim(wantB), 0);
+  int2 rdB = describe(baseB, wantB);
+  int wantA = want_at(baseB + wantB);
+  int atomA = claim(wantA);
 
-    for (int j = 0; j < nstage; ++j) {
-      int s;
-      if (!acquire(s)) {
-        ok = false;
-        break;
+  while (baseC < units_total) {
+    // Advance the look-ahead: skip flag for B, descriptors for A, a new claim.
+    const int frB = check(rdB);
+    const int baseA = __shfl_sync(0xffffffffu, atomA, 0);
+    const int2 rdA = describe(baseA, wantA);
+    const int wantN = want_at(baseA + wantA);
+    const int atomN = claim(wantN);
+
+    // Issue batch C: units not behind a known rejection of their request.
+    bool live = rdC.x >= 0;
+    if (kVerify && live && p.early_exit) {
+      const int bi = rdC.x >> 1;
+      if (frC < bi - (bi / p.k) * p.k) live = false;
+    }
+    unsigned mask = __ballot_sync(0xffffffffu, live);
+    while (mask) {
+      const int l = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const int uu = baseC + l;
+      const int slot = __shfl_sync(0xffffffffu, rdC.x, l);
+      const float sc = __int_as_float(__shfl_sync(0xffffffffu, rdC.y, l));
+      if (lane == 0) {
+        const int row = uu / p.nch;
+        const int chunk = uu - row * p.nch;
+        const TIn* rowp;
+        if (kVerify) {
+          const int bi = slot >> 1;
+          const int b = bi / p.k;
+          const int i = bi - b * p.k;
+          rowp = (slot & 1)
+                     ? static_cast<const TIn*>(p.draft) + ((size_t)b * p.k + i) * (size_t)p.V
+                     : static_cast<const TIn*>(p.target) + ((size_t)b * (p.k + 1) + i) * (size_t)p.V;
+        } else {
+          rowp = static_cast<const TIn*>(p.target) + (size_t)slot * (size_t)p.V;
+        }
+        const bool greedy = (sc == 0.0f);
+        // Element range of the chunk and its 16-byte aligned core.
+        const int e0 = chunk * p.chunk_elems;
+        const int e1 = min(p.V, e0 + p.chunk_elems);
+        const uintptr_t addr0 = reinterpret_cast<uintptr_t>(rowp + e0);
+        int a0 = e0 + (int)(((16u - (unsigned)(addr0 & 15u)) & 15u) / Tr::kSize);
+        if (a0 > e1) a0 = e1;
+        const int core_bytes = (((e1 - a0) * Tr::kSize) & ~15);
+        const int a1 = a0 + core_bytes / Tr::kSize;
+        const int nstage = core_bytes > 0 ? (core_bytes + kStageBytes - 1) / kStageBytes : 1;
+        const char* src0 = reinterpret_cast<const char*>(rowp + a0);
+        my_chunks += 1;
+        my_bytes += (unsigned long long)(e1 - e0) * Tr::kSize;
+        for (int j = 0; j < nstage; ++j) {
+          int s;
+          if (!acquire(s)) {
+            ok = false;
+            break;
+          }
+          const int off = j * kStageBytes;
+          const int nb = core_bytes > 0 ? min(kStageBytes, core_bytes - off) : 0;
+          StageInfo& I = sm.info[s];
+          I.row = rowp;
+          I.part = slot * p.nch + chunk;
+          I.flags = (j == 0 ? kFlagFirst : 0) | (j == nstage - 1 ? kFlagLast : 0) |
+                    (greedy ? kFlagGreedy : 0);
+          I.elem0 = a0 + off / Tr::kSize;
+          I.nbytes = nb;
+          I.head0 = e0;
+          I.headn = a0 - e0;
+          I.tail0 = a1;
+          I.tailn = e1 - a1;
+          I.sc = sc;
+          I.slot = slot;
+          if (nb > 0) {
+            mbar_arrive_expect_tx(&sm.full[s], (uint32_t)nb);
+            bulk_g2s(sm.stage[s], src0 + off, (uint32_t)nb, &sm.full[s]);
+          } else {
+            mbar_arrive(&sm.full[s]);
+          }
+          ++it;
+        }
       }
-      const int off = j * kStageBytes;
-      const int nb = core_bytes > 0 ? min(kStageBytes, core_bytes - off) : 0;
-      StageInfo& I = sm.info[s];
-      I.row = rowp;
-      I.part = slot * p.nch + chunk;
-      I.flags = (j == 0 ? kFlagFirst : 0) | (j == nstage - 1 ? kFlagLast : 0) |
-                (greedy ? kFlagGreedy : 0);
-      I.elem0 = a0 + off / Tr::kSize;
-      I.nbytes = nb;
-      I.head0 = e0;
-      I.headn = a0 - e0;
-      I.tail0 = a1;
-      I.tailn = e1 - a1;
-      I.sc = sc;
-      I.slot = slot;
-      if (nb > 0) {
-        mbar_arrive_expect_tx(&sm.full[s], (uint32_t)nb);
-        bulk_g2s(sm.stage[s], src0 + off, (uint32_t)nb, &sm.full[s]);
-      } else {
-        mbar_arrive(&sm.full[s]);
-      }
-      ++it;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
     }
     if (!ok) break;
+
+    // Rotate the pipeline.
+    baseC = baseB;
+    wantC = wantB;
+    rdC = rdB;
+    frC = frB;
+    baseB = baseA;
+    wantB = wantA;
+    rdB = rdA;
+    wantA = wantN;
+    atomA = atomN;
   }
 
+  if (lane != 0) return;
+  atomicAdd(&h->chunks_swept, my_chunks);
+  atomicAdd(&h->sweep_bytes, my_bytes);
   if (ok) {
     int s;
     if (acquire(s)) {
@@ -180,10 +273,118 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
 }
 
 // ---------------------------------------------------------------------------
+// One consumer thread's share of a stage: kVecPerThread 16-byte vectors held
+// in registers.  Vectors past the stage's end are -inf in every element, so
+// they change neither a max nor a sum of exponentials.
+// ---------------------------------------------------------------------------
+template <typename TIn>
+__device__ __forceinline__ uint4 neg_inf_vec();
+template <>
+__device__ __forceinline__ uint4 neg_inf_vec<uint16_t>() {
+  return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+}
+template <>
+__device__ __forceinline__ uint4 neg_inf_vec<float>() {
+  return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+}
+
+// Largest element of the batch.
+template <typename TIn>
+__device__ __forceinline__ float batch_max(const uint4 (&v)[kVecPerThread]);
+template <>
+__device__ __forceinline__ float batch_max<uint16_t>(const uint4 (&v)[kVecPerThread]) {
+  uint32_t m[kVecPerThread];
+#pragma unroll
+  for (int t = 0; t < kVecPerThread; ++t)
+    m[t] = bf16x2_max(bf16x2_max(v[t].x, v[t].y), bf16x2_max(v[t].z, v[t].w));
+#pragma unroll
+  for (int w = kVecPerThread / 2; w > 0; w >>= 1)
+#pragma unroll
+    for (int t = 0; t < w; ++t) m[t] = bf16x2_max(m[t], m[t + w]);
+  return fmaxf(__uint_as_float(m[0] << 16), __uint_as_float(m[0] & 0xffff0000u));
+}
+template <>
+__device__ __forceinline__ float batch_max<float>(const uint4 (&v)[kVecPerThread]) {
+  float m[kVecPerThread];
+#pragma unroll
+  for (int t = 0; t < kVecPerThread; ++t)
+    m[t] = fmaxf(fmaxf(__uint_as_float(v[t].x), __uint_as_float(v[t].y)),
+                 fmaxf(__uint_as_float(v[t].z), __uint_as_float(v[t].w)));
+#pragma unroll
+  for (int w = kVecPerThread / 2; w > 0; w >>= 1)
+#pragma unroll
+    for (int t = 0; t < w; ++t) m[t] = fmaxf(m[t], m[t + w]);
+  return m[0];
+}
+
+// Element e (in index order) of one vector.
+template <typename TIn>
+__device__ __forceinline__ float vec_elem(const uint4& v, int e) {
+  const uint32_t w = e < ElemTraits<TIn>::kPerVec / 2
+                         ? (e < ElemTraits<TIn>::kPerVec / 4 ? v.x : v.y)
+                         : (e < 3 * ElemTraits<TIn>::kPerVec / 4 ? v.z : v.w);
+  if (ElemTraits<TIn>::kPerVec == 4) return __uint_as_float(w);
+  return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+
+// Softmax accumulation of a batch: one max, at most one rescale, then
+// independent packed FMAs, one ex2 per element and four packed accumulators.
+template <typename TIn>
+__device__ __forceinline__ void soft_stage(SoftAcc& a, const uint4 (&v)[kVecPerThread], float sc) {
+  const float gm = batch_max<TIn>(v);
+  if (gm > a.m) {
+    const float nms = __fmul_rn(gm, sc);
+    a.s = __fmul_rn(a.s, ex2(__fsub_rn(a.ms, nms)));
+    a.m = gm;
+    a.ms = nms;
+  }
+  const float2 s2 = make_float2(sc, sc), c2 = make_float2(-a.ms, -a.ms);
+  float2 acc[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int t = 0; t < kVecPerThread; ++t) {
+    const uint32_t w[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
+    if (ElemTraits<TIn>::kPerVec == 8) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 z = make_float2(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u));
+        acc[q] = f32x2_add(acc[q], ex2x2(f32x2_fma(z, s2, c2)));
+      }
+    } else {
+      const int q0 = (t & 1) * 2;
+      acc[q0] = f32x2_add(acc[q0], ex2x2(f32x2_fma(make_float2(__uint_as_float(w[0]), __uint_as_float(w[1])), s2, c2)));
+      acc[q0 + 1] = f32x2_add(acc[q0 + 1], ex2x2(f32x2_fma(make_float2(__uint_as_float(w[2]), __uint_as_float(w[3])), s2, c2)));
+    }
+  }
+  const float2 t2 = f32x2_add(f32x2_add(acc[0], acc[1]), f32x2_add(acc[2], acc[3]));
+  a.s = __fadd_rn(a.s, __fadd_rn(t2.x, t2.y));
+}
+
+// Argmax of a batch: one max; only when it beats the running best, a scan in
+// index order for its first occurrence.  `first` is the element index of
+// vector 0, vectors are `stride` elements apart.
+template <typename TIn>
+__device__ __forceinline__ void arg_stage(ArgAcc& a, const uint4 (&v)[kVecPerThread], int first,
+                                          int stride) {
+  constexpr int EPV = ElemTraits<TIn>::kPerVec;
+  const float gm = batch_max<TIn>(v);
+  if (!(gm > a.v)) return;
+  int found = INT32_MAX;
+#pragma unroll
+  for (int t = kVecPerThread - 1; t >= 0; --t)
+#pragma unroll
+    for (int e = EPV - 1; e >= 0; --e)
+      if (vec_elem<TIn>(v[t], e) == gm) found = first + t * stride + e;
+  a.v = gm;
+  a.i = found;
+}
+
+// ---------------------------------------------------------------------------
 // Decision for (b, i) once all of its chunks are in (warp-cooperative).
 // ---------------------------------------------------------------------------
 template <typename TIn>
-__device__ void decide_position(const SweepParams& p, WsHeader* h, int bi, bool greedy, float sc) {
+__device__ void decide_position(const SweepParams& p, int bi, bool greedy, float sc) {
   const int lane = threadIdx.x & 31;
   const int b = bi / p.k;
   const int i = bi - b * p.k;
@@ -197,20 +398,19 @@ __device__ void decide_position(const SweepParams& p, WsHeader* h, int bi, bool 
   int32_t* first_reject = reinterpret_cast<int32_t*>(p.ws + p.lay.first_reject);
   const int x = __ldg(&p.tokens[(size_t)b * p.k + i]);
 
-  bool accept, row_ok;
+  bool accept, row_ok, late;
   if (greedy) {
     float v;
     int g;
-    row_argmax_from_parts(pt, p.nch, &v, &g);
+    row_argmax_from_parts(pt, p.nch, &v, &g, &late);
     row_ok = (g != INT32_MAX);
     accept = (g == x);
     if (lane == 0) __stcg(&pos_arg[bi], g);
   } else {
-    const Partial* pd = parts + (size_t)((bi << 1) | 1) * p.nch;
+    // Target chunks then draft chunks: the two slots are adjacent.
     double ct, cd;
-    float mt, md;
-    const bool okt = row_log2_normaliser(pt, p.nch, sc, &ct, &mt);
-    const bool okd = row_log2_normaliser(pd, p.nch, sc, &cd, &md);
+    bool okt, okd;
+    pair_log2_normalisers(pt, p.nch, sc, &ct, &cd, &okt, &okd, &late);
     row_ok = okt && okd;
     const float zt = ElemTraits<TIn>::load(
         static_cast<const TIn*>(p.target) + ((size_t)b * (p.k + 1) + i) * (size_t)p.V, x);
@@ -222,7 +422,10 @@ __device__ void decide_position(const SweepParams& p, WsHeader* h, int bi, bool 
     const double u = (double)__ldg(&p.uniforms[(size_t)b * (p.k + 1) + i]);
     // A token the target gives probability zero is never accepted; a token
     // the drafter gives probability zero (and the target not) always is.
-    const double ratio = (lp == -INFINITY) ? 0.0 : exp2(lp - lq);
+    // 2^d in single precision: near any threshold u the absolute error is
+    // below 1e-7.
+    const double d = lp - lq;
+    const double ratio = (lp == -INFINITY) ? 0.0 : (d >= 0.0 ? 1.0 : (double)exp2f((float)d));
     accept = u < fmin(1.0, ratio);
     if (lane == 0) {
       __stcg(&pos_c[(size_t)bi * 2], ct);
@@ -233,6 +436,7 @@ __device__ void decide_position(const SweepParams& p, WsHeader* h, int bi, bool 
   // it; it also ends the round there so no later row is read for nothing.
   if (!row_ok) accept = false;
   if (lane == 0) {
+    if (late) record_status(reinterpret_cast<WsHeader*>(p.ws + p.lay.header), SPEC_ERR_TIMEOUT);
     if (!row_ok) atomicOr(&bad_bits[b], 1u << i);
     if (accept) atomicOr(&acc_bits[b], 1u << i);
     atomicOr(&dec_bits[b], 1u << i);
@@ -243,16 +447,35 @@ __device__ void decide_position(const SweepParams& p, WsHeader* h, int bi, bool 
 // ---------------------------------------------------------------------------
 // Consumers: warps 0..kNC-1.
 // ---------------------------------------------------------------------------
-template <typename TIn, bool kVerify>
-__device__ void sweep_consumers(const SweepParams& p, SweepSmem& sm, WsHeader* h) {
+
+// Post this warp's accumulator for the unit (or the end marker) in reduction
+// slot `units % kRedDepth`, once the bookkeeping warp has released it.
+__device__ __forceinline__ bool post_unit(SweepSmem& sm, WsHeader* h, int units, const float4& acc,
+                                          const UnitMeta& meta) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rs = units % kRedDepth;
+  if (units >= kRedDepth &&
+      !mbar_wait_bounded(&sm.red_free[rs], ((units / kRedDepth) - 1) & 1, &sm.abort_flag)) {
+    sweep_abort(h, sm);
+    return false;
+  }
+  if (lane == 0) {
+    sm.red[rs][warp] = acc;
+    if (warp == 0) sm.meta[rs] = meta;
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&sm.red_bar[rs]);
+  return true;
+}
+
+template <typename TIn>
+__device__ void sweep_consumers(SweepSmem& sm, WsHeader* h) {
   using Tr = ElemTraits<TIn>;
   constexpr int EPV = Tr::kPerVec;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int ctid = threadIdx.x;
   volatile int* abort_flag = &sm.abort_flag;
-  Partial* parts = reinterpret_cast<Partial*>(p.ws + p.lay.partials);
-  int32_t* done = reinterpret_cast<int32_t*>(p.ws + p.lay.done);
 
   SoftAcc sa;
   ArgAcc aa;
@@ -266,7 +489,11 @@ __device__ void sweep_consumers(const SweepParams& p, SweepSmem& sm, WsHeader* h
       return;
     }
     const StageInfo I = sm.info[s];
-    if (I.flags & kFlagEnd) return;
+    if (I.flags & kFlagEnd) {
+      UnitMeta end = {0, 0, kFlagEnd, 0.0f};
+      post_unit(sm, h, units, make_float4(0.f, 0.f, 0.f, 0.f), end);
+      return;
+    }
     const bool greedy = (I.flags & kFlagGreedy) != 0;
     const TIn* row = static_cast<const TIn*>(I.row);
     if (I.flags & kFlagFirst) {
@@ -278,102 +505,130 @@ __device__ void sweep_consumers(const SweepParams& p, SweepSmem& sm, WsHeader* h
         else soft_add1(sa, x, I.sc);
       }
     }
+    // Copy this thread's vectors out of the stage, then hand the stage back.
     const uint4* buf = reinterpret_cast<const uint4*>(sm.stage[s]);
     const int nvec = I.nbytes >> 4;
-    if (greedy) {
-#pragma unroll 4
-      for (int j = ctid; j < nvec; j += kNCT) {
-        float x[EPV];
-        Tr::unpack(buf[j], x);
-        const int base = I.elem0 + j * EPV;
+    uint4 v[kVecPerThread];
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) arg_add(aa, x[e], base + e);
-      }
-    } else {
-#pragma unroll 4
-      for (int j = ctid; j < nvec; j += kNCT) {
-        float x[EPV];
-        Tr::unpack(buf[j], x);
-        soft_add<EPV>(sa, x, I.sc);
-      }
+    for (int t = 0; t < kVecPerThread; ++t) {
+      const int j = ctid + t * kNCT;
+      v[t] = j < nvec ? buf[j] : neg_inf_vec<TIn>();
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[s]);
+    ++it;
+
+    if (greedy) arg_stage<TIn>(aa, v, I.elem0 + ctid * EPV, kNCT * EPV);
+    else soft_stage<TIn>(sa, v, I.sc);
     if ((I.flags & kFlagLast) && warp == 0 && lane < I.tailn) {
       const float x = Tr::load(row, I.tail0 + lane);
       if (greedy) arg_add(aa, x, I.tail0 + lane);
       else soft_add1(sa, x, I.sc);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[s]);
-    ++it;
     if (!(I.flags & kFlagLast)) continue;
 
-    // ---- end of a unit: reduce the consumer warps' accumulators ----
-    const int rs = units % kRedDepth;
-    const uint32_t rpar = (uint32_t)(units / kRedDepth) & 1u;
-    ++units;
+    // ---- end of a unit: warp-reduce and post for the bookkeeping warp ----
+    float4 acc;
     if (greedy) {
       arg_warp_reduce(aa);
-      if (lane == 0) sm.red[rs][warp] = make_float4(aa.v, __int_as_float(aa.i), 0.f, 0.f);
+      acc = make_float4(aa.v, __int_as_float(aa.i), 0.f, 0.f);
     } else {
       soft_warp_reduce(sa);
-      if (lane == 0) sm.red[rs][warp] = make_float4(sa.m, sa.ms, sa.s, 0.f);
+      acc = make_float4(sa.m, sa.ms, sa.s, 0.f);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.red_bar[rs]);
-    if (warp != 0) continue;
-    if (!mbar_wait_bounded(&sm.red_bar[rs], rpar, abort_flag)) {
+    const UnitMeta meta = {I.part, I.slot, I.flags, I.sc};
+    if (!post_unit(sm, h, units, acc, meta)) return;
+    ++units;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Bookkeeping warp: merges the consumer warps' accumulators of each unit,
+// stores the unit's partial and, in verification mode, counts the chunks of
+// (b, i) and decides when the last one is in.
+// ---------------------------------------------------------------------------
+template <typename TIn, bool kVerify>
+__device__ void sweep_bookkeeper(const SweepParams& p, SweepSmem& sm, WsHeader* h) {
+  const int lane = threadIdx.x & 31;
+  Partial* parts = reinterpret_cast<Partial*>(p.ws + p.lay.partials);
+  int32_t* done = reinterpret_cast<int32_t*>(p.ws + p.lay.done);
+  // The chunk count of a unit is looked at one unit later, so that the
+  // atomic's round trip overlaps the next unit's merge and store.  No fence
+  // orders a partial before its count: the deciding CTA instead waits for
+  // each partial slot of (b, i) to leave the empty marker, which it does
+  // because every counted unit has already issued its store.
+  int pend_bi = -1, pend_old = 0, pend_need = 0;
+  bool pend_greedy = false;
+  float pend_sc = 0.0f;
+  auto resolve_pending = [&]() {
+    if (!kVerify || pend_bi < 0) return;
+    const int old = __shfl_sync(0xffffffffu, pend_old, 0);
+    if (old == pend_need - 1) decide_position<TIn>(p, pend_bi, pend_greedy, pend_sc);
+    pend_bi = -1;
+  };
+  for (int u = 0;; ++u) {
+    const int rs = u % kRedDepth;
+    const uint32_t par = (u / kRedDepth) & 1;
+    // Nothing to merge yet: settle the previous unit's count while waiting.
+    const bool ready = mbar_test_wait(&sm.red_bar[rs], par);
+    if (!__all_sync(0xffffffffu, ready)) resolve_pending();
+    if (!mbar_wait_bounded(&sm.red_bar[rs], par, &sm.abort_flag)) {
       sweep_abort(h, sm);
       return;
     }
-    Partial out;
+    const UnitMeta meta = sm.meta[rs];
+    const float4 r = lane < kNC ? sm.red[rs][lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.red_free[rs]);
+    if (meta.flags & kFlagEnd) {
+      resolve_pending();
+      return;
+    }
+
+    const bool greedy = (meta.flags & kFlagGreedy) != 0;
+    float out_m;
+    uint32_t out_aux;
     if (greedy) {
       ArgAcc a;
       arg_init(a);
       if (lane < kNC) {
-        const float4 r = sm.red[rs][lane];
         a.v = r.x;
         a.i = __float_as_int(r.y);
       }
       arg_warp_reduce(a);
-      out.m = a.v;
-      out.s = 0.0f;
-      out.arg = a.i;
+      out_m = a.v;
+      out_aux = (uint32_t)a.i;
     } else {
       SoftAcc a;
       soft_init(a);
       if (lane < kNC) {
-        const float4 r = sm.red[rs][lane];
         a.m = r.x;
         a.ms = r.y;
         a.s = r.z;
       }
       soft_warp_reduce(a);
-      out.m = a.m;
-      out.s = a.s;
-      out.arg = 0;
+      out_m = a.m;
+      out_aux = __float_as_uint(a.s);
     }
-    out.pad = 0;
-    if (lane == 0) __stcg(reinterpret_cast<int4*>(&parts[I.part]), *reinterpret_cast<int4*>(&out));
+    if (lane == 0) store_partial(&parts[meta.part], out_m, out_aux);
 
     if (kVerify) {
-      const int bi = I.slot >> 1;
-      const int need = greedy ? p.nch : 2 * p.nch;
+      // Count this chunk of (b, i); the CTA that brings the count to its
+      // total decides.
       int old = 0;
-      if (lane == 0) {
-        __threadfence();
-        old = atomicAdd(&done[bi], 1);
-      }
-      old = __shfl_sync(0xffffffffu, old, 0);
-      if (old == need - 1) {
-        __threadfence();
-        decide_position<TIn>(p, h, bi, greedy, I.sc);
-      }
+      if (lane == 0) old = atomicAdd(&done[meta.slot >> 1], 1);
+      resolve_pending();
+      pend_bi = meta.slot >> 1;
+      pend_old = old;
+      pend_need = greedy ? p.nch : 2 * p.nch;
+      pend_greedy = greedy;
+      pend_sc = meta.sc;
     }
   }
 }
 
 template <typename TIn, bool kVerify>
-__global__ void __launch_bounds__(kSweepThreads, 2) sweep_kernel(SweepParams p) {
+__global__ void __launch_bounds__(kSweepThreads, kSweepMinBlocks) sweep_kernel(SweepParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SweepSmem& sm = *reinterpret_cast<SweepSmem*>(smem_raw);
   if (threadIdx.x == 0) {
@@ -381,7 +636,10 @@ __global__ void __launch_bounds__(kSweepThreads, 2) sweep_kernel(SweepParams p) 
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kNC);
     }
-    for (int r = 0; r < kRedDepth; ++r) mbar_init(&sm.red_bar[r], kNC);
+    for (int r = 0; r < kRedDepth; ++r) {
+      mbar_init(&sm.red_bar[r], kNC);
+      mbar_init(&sm.red_free[r], 1);
+    }
     sm.abort_flag = 0;
     fence_mbar_init();
   }
@@ -389,11 +647,16 @@ __global__ void __launch_bounds__(kSweepThreads, 2) sweep_kernel(SweepParams p) 
   // Everything below reads what the plan kernel wrote.
   pdl_wait();
   WsHeader* h = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
-  if ((threadIdx.x >> 5) == kNC) {
-    if ((threadIdx.x & 31) == 0) sweep_producer<TIn, kVerify>(p, sm, h);
-    return;
+  // Warps 0..kNC-1 consume, warp kNC produces, warp kNC+1 keeps the books;
+  // the mbarrier counts and reduction slots are sized for exactly this split.
+  const int warp = threadIdx.x >> 5;
+  if (warp < kNC) {
+    sweep_consumers<TIn>(sm, h);
+  } else if (warp == kProducerWarp) {
+    sweep_producer<TIn, kVerify>(p, sm, h);
+  } else if (warp == kBookWarp) {
+    sweep_bookkeeper<TIn, kVerify>(p, sm, h);
   }
-  sweep_consumers<TIn, kVerify>(p, sm, h);
 }
 
 }  // namespace specv

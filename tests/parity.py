@@ -9,8 +9,11 @@ import oracle
 # A decision is a near-tie when its uniform lies within this distance of the
 # threshold it is compared with (accept test or an edge of the sampled CDF
 # cell): there the fp32 GPU path and the fp64 oracle may legitimately differ.
+# Near-ties are a property of the inputs (a long-tailed vocabulary has many
+# CDF cells narrower than the band) and are only counted.
 NEAR_TIE = 1e-6
-# Near-ties may be at most this fraction of the logit rows evaluated.
+# Mismatches excused by a near-tie may be at most this fraction of the logit
+# rows evaluated (at least one per comparison).
 NEAR_TIE_RATE = 1e-5
 
 
@@ -35,7 +38,8 @@ def compare(gpu_out: np.ndarray, gpu_n: np.ndarray, o: oracle.OracleResult,
     bad = ~same & ~near
     rows = evaluated_rows(o, temperature)
     info = dict(requests=len(gpu_n), mismatches=int((~same).sum()), near_ties=int(near.sum()),
-                mismatches_outside_band=int(bad.sum()), rows=rows)
+                excused=int((~same & near).sum()), mismatches_outside_band=int(bad.sum()),
+                rows=rows)
     if bad.any():
         b = int(np.nonzero(bad)[0][0])
         raise AssertionError(
@@ -43,5 +47,5 @@ def compare(gpu_out: np.ndarray, gpu_n: np.ndarray, o: oracle.OracleResult,
             f"(margin {o.margin[b]:.3g}, T {temperature[b]}): gpu n={gpu_n[b]} "
             f"out={gpu_out[b].tolist()} oracle n={o.num_accepted[b]} "
             f"out={o.out_tokens[b].tolist()}; {info}")
-    assert info["near_ties"] <= max(1, NEAR_TIE_RATE * rows), (label, info)
+    assert info["excused"] <= max(1, NEAR_TIE_RATE * rows), (label, info)
     return info
