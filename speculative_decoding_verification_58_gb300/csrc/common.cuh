@@ -29,9 +29,10 @@ constexpr int kSweepMinBlocks = 3;  // CTAs per SM the register budget is sized 
 constexpr int kRedDepth = 8;  // unit-end reduction slots in flight
 
 // Final-pass kernel geometry.
-constexpr int kFinalThreads = 1024;
+constexpr int kFinalThreads = 256;
 constexpr int kSegElems = 256;  // one warp x 8 elements
 constexpr int kMaxSegs = SPEC_MAX_V / kSegElems;
+constexpr int kMaxSlices = 16;  // CTAs that share one request's final row(s)
 
 // Bounded waits: give up after this many nanoseconds of spinning.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -73,7 +74,7 @@ constexpr unsigned long long kPartialEmpty = 0x7FC0DEAD7FC0DEADull;
 
 struct WsLayout {
   size_t header, rowdesc, flags, first_reject, acc_bits, dec_bits, bad_bits, done, pos_c, pos_arg,
-      partials, total;
+      partials, seg_mass, slice_ref, slice_arg, final_done, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -95,7 +96,9 @@ __host__ __device__ inline int chunk_elems_for(int V, int C) {
   return (e + 7) & ~7;
 }
 
-__host__ __device__ inline WsLayout ws_layout(int B, int k, int C) {
+__host__ __device__ inline int segments_of(int V) { return (V + kSegElems - 1) / kSegElems; }
+
+__host__ __device__ inline WsLayout ws_layout(int B, int k, int C, int V) {
   WsLayout l;
   size_t o = 0;
   size_t slots = (size_t)B * (size_t)k * 2;
@@ -110,6 +113,10 @@ __host__ __device__ inline WsLayout ws_layout(int B, int k, int C) {
   l.pos_c = o;        o = align256(o + slots * sizeof(double));
   l.pos_arg = o;      o = align256(o + (size_t)B * k * sizeof(int32_t));
   l.partials = o;     o = align256(o + slots * (size_t)C * sizeof(Partial));
+  l.seg_mass = o;     o = align256(o + (size_t)B * segments_of(V) * sizeof(float));
+  l.slice_ref = o;    o = align256(o + (size_t)B * kMaxSlices * sizeof(float));
+  l.slice_arg = o;    o = align256(o + (size_t)B * kMaxSlices * sizeof(int32_t));
+  l.final_done = o;   o = align256(o + (size_t)B * sizeof(int32_t));
   l.total = o;
   return l;
 }

@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   uint32_t* bad_bits = reinterpret_cast<uint32_t*>(p.ws + p.lay.bad_bits);
   int32_t* done = reinterpret_cast<int32_t*>(p.ws + p.lay.done);
   Partial* parts = reinterpret_cast<Partial*>(p.ws + p.lay.partials);
+  int32_t* final_done = reinterpret_cast<int32_t*>(p.ws + p.lay.final_done);
 
   if (tid == 0) {
     h->status = SPEC_OK;
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
       acc_bits[b] = 0u;
       dec_bits[b] = 0u;
       bad_bits[b] = 0u;
+      final_done[b] = 0;
       if (!ok) {
         atomicAdd(&h->bad_requests, 1);
         atomicMin(&h->first_bad, b);

@@ -206,7 +206,7 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
   const int C = chunks_per_row(slots, V);
   const int ce = chunk_elems_for(V, C);
   const int nch = (V + ce - 1) / ce;
-  const WsLayout lay = ws_layout(B, k, C);
+  const WsLayout lay = ws_layout(B, k, C, V);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
 
   PlanParams pp;
@@ -264,10 +264,17 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
   fp.num_accepted = num_accepted;
   fp.ws = ws;
   fp.lay = lay;
-  const int nseg = (V + kSegElems - 1) / kSegElems;
+  const int nseg = segments_of(V);
+  // Slices per request: one wave of four CTAs per SM over the batch, each
+  // slice at least one segment.
+  int P = (4 * d->sms) / B;
+  if (P > kMaxSlices) P = kMaxSlices;
+  if (P > nseg) P = nseg;
+  if (P < 1) P = 1;
+  fp.P = P;
   const size_t fsm = (size_t)nseg * (sizeof(double) + sizeof(float));
   if (record(ev, 2, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (launch(final_kernel<TIn>, dim3(B), dim3(kFinalThreads), fsm, stream, pdl, fp) !=
+  if (launch(final_kernel<TIn>, dim3(P, B), dim3(kFinalThreads), fsm, stream, pdl, fp) !=
       cudaSuccess)
     return SPEC_ERR_CUDA;
   if (record(ev, 3, stream) != cudaSuccess) return SPEC_ERR_CUDA;
@@ -339,7 +346,7 @@ const char* spec_status_string(spec_status_t s) {
 size_t spec_verify_workspace_bytes(int B, int k, int V) {
   if (!sizes_ok(B, k, V)) return 0;
   const long long slots = 2LL * B * k;
-  return ws_layout(B, k, chunks_per_row(slots, V)).total;
+  return ws_layout(B, k, chunks_per_row(slots, V), V).total;
 }
 
 static spec_status_t verify_entry(const void* target_logits, const void* draft_logits,
