@@ -146,6 +146,39 @@ spec_status_t spec_verify_timed(const void* target_logits, const void* draft_log
                                 size_t workspace_bytes, void* stream, unsigned flags,
                                 void* ev_plan, void* ev_sweep, void* ev_final, void* ev_end);
 
+/*
+ * spec_verify for callers that cannot allocate device memory.  (The paper
+ * has no counterpart: this is a deployment convenience.)  Some callers are
+ * handed only their input and output buffers -- for example an operator
+ * plugged into a runtime that owns all device memory and offers no scratch,
+ * or code on a serving hot path where an allocation would stall or is
+ * forbidden -- so they cannot supply spec_verify's workspace.
+ *
+ * Instead of a workspace, this entry uses a fixed scratch array of
+ * SPEC_STATIC_SCRATCH_BYTES that lives inside the library: every GPU that
+ * loads the library holds that memory until the process exits.  The call
+ * itself allocates nothing (no cudaMalloc, no allocating library routine).
+ *   - Batches whose spec_verify_workspace_bytes(B, k, V) exceeds
+ *     SPEC_STATIC_SCRATCH_BYTES are rejected with SPEC_ERR_UNSUPPORTED and
+ *     nothing is launched.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls on a GPU share the one array, which keeps the last call's
+ *     contents; each call resets what it needs.  Calls that overlap on the
+ *     GPU (other streams, other host threads) race and must be serialised
+ *     by the caller.
+ *   - Invalid device-side inputs show as num_accepted[b] == -1; the status
+ *     word stays in the library's scratch and is not reported separately.
+ * Arguments are those of spec_verify without the workspace.
+ */
+#define SPEC_STATIC_SCRATCH_BYTES (8u << 20)
+spec_status_t spec_verify_static(const void* target_logits, const void* draft_logits,
+                                 spec_dtype_t dtype, const int32_t* draft_tokens,
+                                 const int32_t* lengths, const float* uniforms,
+                                 const float* temperature, int B, int k, int V,
+                                 int32_t* out_tokens, int32_t* num_accepted, void* stream);
+
 /* What the last call on a workspace recorded. */
 typedef struct {
   int32_t status;             /* spec_status_t recorded on the device */

@@ -42,7 +42,8 @@ SPEC_FLAG_FULL_SWEEP = 1
 EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_ex", "spec_verify_timed",
            "spec_verify_report",
            "spec_verify_device_status", "spec_row_stats_workspace_bytes", "spec_row_stats",
-           "spec_status_string", "spec_abi_version")
+           "spec_status_string", "spec_abi_version", "spec_verify_static")
+SPEC_STATIC_SCRATCH_BYTES = 8 << 20
 
 
 class SpecVerifyError(RuntimeError):
@@ -97,6 +98,8 @@ def lib() -> ctypes.CDLL:
     L.spec_verify_ex.restype = ci
     L.spec_verify_timed.argtypes = L.spec_verify_ex.argtypes + [vp, vp, vp, vp]
     L.spec_verify_timed.restype = ci
+    L.spec_verify_static.argtypes = [vp, vp, ci, i32p, i32p, f32p, f32p, ci, ci, ci, i32p, i32p, vp]
+    L.spec_verify_static.restype = ci
     L.spec_verify_report.argtypes = [vp, vp, ctypes.POINTER(_Report)]
     L.spec_verify_report.restype = ci
     L.spec_verify_device_status.argtypes = [vp, vp]
@@ -226,6 +229,40 @@ def spec_verify(target_logits, draft_logits, draft_tokens, lengths, uniforms, te
         handles = [None if e is None else (e.cuda_event or None) for e in events]
         code = lib().spec_verify_timed(*args, *handles)
     _check(code, "spec_verify")
+    return out_tokens, num_accepted
+
+
+def spec_verify_static(target_logits, draft_logits, draft_tokens, lengths, uniforms, temperature,
+                       *, out_tokens=None, num_accepted=None, stream=None):
+    """spec_verify for callers that cannot allocate: no workspace argument.
+
+    The library uses its own fixed scratch array (SPEC_STATIC_SCRATCH_BYTES
+    per GPU, held until exit) instead.  Calls that overlap on the GPU share it
+    and race.  If ``out_tokens`` / ``num_accepted`` are given, this wrapper
+    allocates nothing either.
+    """
+    torch = _torch()
+    B, k1, V = target_logits.shape
+    k = k1 - 1
+    dev = target_logits.device
+    dt = _dtype_code(target_logits)
+    _need(target_logits, "target_logits", target_logits.dtype, (B, k + 1, V), dev)
+    _need(draft_logits, "draft_logits", target_logits.dtype, (B, k, V), dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, k), dev)
+    _need(lengths, "lengths", torch.int32, (B,), dev)
+    _need(uniforms, "uniforms", torch.float32, (B, k + 1), dev)
+    _need(temperature, "temperature", torch.float32, (B,), dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    if num_accepted is None:
+        num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, k + 1), dev)
+    _need(num_accepted, "num_accepted", torch.int32, (B,), dev)
+    code = lib().spec_verify_static(
+        target_logits.data_ptr(), draft_logits.data_ptr(), dt, draft_tokens.data_ptr(),
+        lengths.data_ptr(), uniforms.data_ptr(), temperature.data_ptr(), B, k, V,
+        out_tokens.data_ptr(), num_accepted.data_ptr(), _stream_ptr(stream))
+    _check(code, "spec_verify_static")
     return out_tokens, num_accepted
 
 

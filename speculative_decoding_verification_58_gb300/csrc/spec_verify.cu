@@ -476,3 +476,75 @@ spec_status_t spec_row_stats(const void* logits, spec_dtype_t dtype, int rows, i
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// spec_verify_static: verification that uses the library's own fixed scratch
+// instead of a caller-provided workspace, for callers that cannot allocate
+// device memory.  Nothing here allocates.
+// ---------------------------------------------------------------------------
+
+namespace specv {
+namespace {
+
+// The scratch: one fixed array on every GPU that loads this library, held
+// until the process exits.  All spec_verify_static calls on a GPU share it.
+static __device__ __align__(256) unsigned char g_static_scratch[SPEC_STATIC_SCRATCH_BYTES];
+
+void* g_static_ptr[kMaxDevices];
+std::mutex g_static_mu;
+
+// Device address of the current GPU's scratch array.  The array's name is
+// only a host-side stand-in in host code, so the address is looked up once
+// per device, with that device current, and cached.
+cudaError_t static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace specv
+
+extern "C" spec_status_t spec_verify_static(const void* target_logits, const void* draft_logits,
+                                            spec_dtype_t dtype, const int32_t* draft_tokens,
+                                            const int32_t* lengths, const float* uniforms,
+                                            const float* temperature, int B, int k, int V,
+                                            int32_t* out_tokens, int32_t* num_accepted,
+                                            void* stream) {
+  using namespace specv;
+  if (B < 1 || k < 1 || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (!sizes_ok(B, k, V)) return SPEC_ERR_UNSUPPORTED;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (!target_logits || !draft_logits || !draft_tokens || !lengths || !uniforms || !temperature ||
+      !out_tokens || !num_accepted)
+    return SPEC_ERR_INVALID_ARG;
+  const size_t esize = dtype == SPEC_F32 ? 4 : 2;
+  if (!aligned(target_logits, esize) || !aligned(draft_logits, esize) || !aligned(draft_tokens, 4) ||
+      !aligned(lengths, 4) || !aligned(uniforms, 4) || !aligned(temperature, 4) ||
+      !aligned(out_tokens, 4) || !aligned(num_accepted, 4))
+    return SPEC_ERR_INVALID_ARG;
+  // The batch must fit the fixed scratch.
+  const size_t need = spec_verify_workspace_bytes(B, k, V);
+  if (need == 0 || need > SPEC_STATIC_SCRATCH_BYTES) return SPEC_ERR_UNSUPPORTED;
+  if (use_device_of(target_logits) != cudaSuccess) return SPEC_ERR_CUDA;
+  void* scratch = nullptr;
+  if (static_scratch(&scratch) != cudaSuccess) return SPEC_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == SPEC_F32)
+    return verify_typed<float>(target_logits, draft_logits, draft_tokens, lengths, uniforms,
+                               temperature, B, k, V, out_tokens, num_accepted, scratch, s, 0u, 0,
+                               nullptr);
+  return verify_typed<uint16_t>(target_logits, draft_logits, draft_tokens, lengths, uniforms,
+                                temperature, B, k, V, out_tokens, num_accepted, scratch, s, 0u, 1,
+                                nullptr);
+}
