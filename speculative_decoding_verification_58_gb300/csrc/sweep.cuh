@@ -41,7 +41,9 @@ struct SweepParams {
   WsLayout lay;
 };
 
-constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagGreedy = 4, kFlagEnd = 8;
+// kFlagDiscard closes a unit whose request was rejected at an earlier
+// position while it streamed: its partial is neither stored nor counted.
+constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagGreedy = 4, kFlagEnd = 8, kFlagDiscard = 16;
 
 struct StageInfo {
   const void* row;  // row base (element 0)
@@ -202,27 +204,35 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
         const int a1 = a0 + core_bytes / Tr::kSize;
         const int nstage = core_bytes > 0 ? (core_bytes + kStageBytes - 1) / kStageBytes : 1;
         const char* src0 = reinterpret_cast<const char*>(rowp + a0);
-        my_chunks += 1;
-        my_bytes += (unsigned long long)(e1 - e0) * Tr::kSize;
+        // Position and request of the unit, for the per-stage skip check.
+        const int ub = kVerify ? (slot >> 1) / p.k : 0;
+        const int ui = kVerify ? (slot >> 1) - ub * p.k : 0;
+        const bool recheck = kVerify && p.early_exit;
         for (int j = 0; j < nstage; ++j) {
+          // Look again for a rejection at an earlier position of the request
+          // before each stage; the load is issued before the ring wait, which
+          // hides its latency.
+          const int frj = recheck ? *(volatile const int32_t*)&first_reject[ub] : INT32_MAX;
           int s;
           if (!acquire(s)) {
             ok = false;
             break;
           }
+          const bool drop = frj < ui;
+          if (drop && j == 0) break;  // nothing issued yet: skip the unit
           const int off = j * kStageBytes;
-          const int nb = core_bytes > 0 ? min(kStageBytes, core_bytes - off) : 0;
+          const int nb = (core_bytes > 0 && !drop) ? min(kStageBytes, core_bytes - off) : 0;
           StageInfo& I = sm.info[s];
           I.row = rowp;
           I.part = slot * p.nch + chunk;
-          I.flags = (j == 0 ? kFlagFirst : 0) | (j == nstage - 1 ? kFlagLast : 0) |
-                    (greedy ? kFlagGreedy : 0);
+          I.flags = (j == 0 ? kFlagFirst : 0) | (j == nstage - 1 || drop ? kFlagLast : 0) |
+                    (drop ? kFlagDiscard : 0) | (greedy ? kFlagGreedy : 0);
           I.elem0 = a0 + off / Tr::kSize;
           I.nbytes = nb;
           I.head0 = e0;
           I.headn = a0 - e0;
           I.tail0 = a1;
-          I.tailn = e1 - a1;
+          I.tailn = drop ? 0 : e1 - a1;
           I.sc = sc;
           I.slot = slot;
           if (nb > 0) {
@@ -232,6 +242,13 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
             mbar_arrive(&sm.full[s]);
           }
           ++it;
+          if (j == 0) {
+            my_chunks += 1;
+            my_bytes += (unsigned long long)(a0 - e0) * Tr::kSize;
+          }
+          my_bytes += (unsigned long long)nb;
+          if (j == nstage - 1) my_bytes += (unsigned long long)(e1 - a1) * Tr::kSize;
+          if (drop) break;
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -584,6 +601,7 @@ __device__ void sweep_bookkeeper(const SweepParams& p, SweepSmem& sm, WsHeader* 
       resolve_pending();
       return;
     }
+    if (meta.flags & kFlagDiscard) continue;
 
     const bool greedy = (meta.flags & kFlagGreedy) != 0;
     float out_m;
