@@ -113,7 +113,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int k, int C, int V) {
   l.pos_c = o;        o = align256(o + slots * sizeof(double));
   l.pos_arg = o;      o = align256(o + (size_t)B * k * sizeof(int32_t));
   l.partials = o;     o = align256(o + slots * (size_t)C * sizeof(Partial));
-  l.seg_mass = o;     o = align256(o + (size_t)B * segments_of(V) * sizeof(float));
+  l.seg_mass = o;     o = align256(o + (size_t)B * segments_of(V) * sizeof(float2));
   l.slice_ref = o;    o = align256(o + (size_t)B * kMaxSlices * sizeof(float));
   l.slice_arg = o;    o = align256(o + (size_t)B * kMaxSlices * sizeof(int32_t));
   l.final_done = o;   o = align256(o + (size_t)B * sizeof(int32_t));

@@ -10,15 +10,16 @@
 //   - greedy, n == L: the argmax of target row L.
 // Sampling is by inverse CDF in ascending vocabulary index with u_L.  The
 // row(s) are split into P slices of 256-entry segments; slice CTA p streams
-// its slice once and writes one mass per segment, then bumps the request's
-// counter.  The last slice CTA to finish forms the segment prefix sums in
-// double, picks the segment holding u_L * total, and re-reads that segment
-// to place the token exactly.
+// its slice once and writes one record per segment, then bumps the
+// request's counter.  The last slice CTA to finish forms the segment prefix
+// sums in double, picks the segment holding u_L * total, and re-reads that
+// segment to place the token exactly.
 //
-// Masses: residual entries max(0, p - q) use the row normalisers from the
-// sweep.  Bonus entries use each slice's own max as reference,
-// 2^(z*sc - ref_p), and the last CTA rescales the slices by 2^(ref_p - ref);
-// the common normaliser cancels in the CDF.
+// Records: a residual segment stores its mass sum max(0, p - q), with p and
+// q normalised by the row normalisers from the sweep.  A bonus segment
+// stores its own max m and s = sum 2^(z*sc - fl(m*sc)); the last CTA weighs
+// it by 2^(fl(m*sc) - REF), REF the largest segment reference, so the row is
+// read once and the common normaliser cancels in the CDF.
 #pragma once
 
 #include "common.cuh"
@@ -41,36 +42,26 @@ struct FinalParams {
 };
 
 constexpr int kFinalWarps = kFinalThreads / 32;
-constexpr int kJobNone = 0, kJobResidual = 1, kJobBonus = 2, kJobGreedyRowL = 3, kJobInvalid = 4;
+constexpr int kJobNone = 0, kJobResidual = 1, kJobBonus = 2, kJobGreedyRowL = 3, kJobInvalid = 4,
+              kJobTargetOnly = 5;
 
 struct FinalShared {
   double warp_d[kFinalWarps + 1];
-  float4 warp_f[kFinalWarps];
-  float scale[kMaxSlices];  // bonus: 2^(ref_p - ref) per slice
-  int job, n, token, cand, last;
+  float warp_f[kFinalWarps];
+  int warp_i[kFinalWarps];
+  double pos_ct[32], pos_cd[32];  // log2 normalisers of the request's positions (k <= 31)
+  int32_t pos_arg[32];
+  int32_t tok[32];                // draft tokens x_0 .. x_{k-1}
+  double cand_excl;
+  float REF;
+  int job, n, cand, token, last;
 };
 
-// Eight consecutive elements e0..e0+7 of a row (entries >= V read as -inf).
-template <typename TIn>
-__device__ __forceinline__ void load8(const TIn* row, int e0, int V, bool vec_ok, float* x) {
-  using Tr = ElemTraits<TIn>;
-  if (vec_ok && e0 + 8 <= V) {
-    const uint4* v = reinterpret_cast<const uint4*>(row + e0);
-    if (Tr::kPerVec == 8) {
-      Tr::unpack(__ldg(v), x);
-    } else {
-      Tr::unpack(__ldg(v), x);
-      Tr::unpack(__ldg(v + 1), x + 4);
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = (e0 + e < V) ? Tr::load(row, e0 + e) : -INFINITY;
-  }
-}
+// ---------------------------------------------------------------------------
+// Segment loads: lane l holds entries 8l .. 8l+7 of a segment as raw bits
+// (one 16-byte vector for bf16, two for fp32).  Entries >= V hold -inf.
+// ---------------------------------------------------------------------------
 
-// One lane's 8 entries of a segment as raw bits (one 16-byte vector for bf16,
-// two for fp32), so that several segments can be in flight before any
-// arithmetic.  Entries >= V hold -inf.
 template <typename TIn>
 struct Seg8 {
   uint4 v[sizeof(TIn) == 2 ? 1 : 2];
@@ -100,30 +91,238 @@ __device__ __forceinline__ void seg_load(Seg8<TIn>& s, const TIn* row, int e0, i
   }
 }
 
+// Entries 2j and 2j+1 of a lane's segment piece as a float pair.
 template <typename TIn>
-__device__ __forceinline__ void seg_unpack(const Seg8<TIn>& s, float* x) {
+__device__ __forceinline__ float2 seg_pair(const Seg8<TIn>& s, int j);
+template <>
+__device__ __forceinline__ float2 seg_pair<uint16_t>(const Seg8<uint16_t>& s, int j) {
+  const uint32_t w = j == 0 ? s.v[0].x : j == 1 ? s.v[0].y : j == 2 ? s.v[0].z : s.v[0].w;
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+template <>
+__device__ __forceinline__ float2 seg_pair<float>(const Seg8<float>& s, int j) {
+  const uint4& v = s.v[j >> 1];
+  return (j & 1) ? make_float2(__uint_as_float(v.z), __uint_as_float(v.w))
+                 : make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+}
+
+__device__ __forceinline__ float2 f32x2_sub(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// How the entries of one request's final row(s) are weighed.  Residual
+// entries: max(0, 2^(zt*sc - a) - 2^(zd*sc - c_d)); target-only entries:
+// 2^(zt*sc - a); a and c_d are row normalisers carried as hi + lo
+// single-precision pairs so that they keep double accuracy.
+struct MassSpec {
+  float sc;
+  float a_hi, a_lo;
+  float cd_hi, cd_lo;
+  bool has_q;
+};
+
+// The 8 entry masses of a lane's segment piece, in index order.  Packed
+// two-lane arithmetic gives each entry exactly the bits of the scalar
+// formula, so the slice pass and the re-scan agree.
+template <typename TIn>
+__device__ __forceinline__ void entry_masses(const Seg8<TIn>& t, const Seg8<TIn>& d,
+                                             const MassSpec& ms, float (&r)[8]) {
+  const float2 sc2 = make_float2(ms.sc, ms.sc);
+  const float2 na2 = make_float2(-ms.a_hi, -ms.a_hi), al2 = make_float2(ms.a_lo, ms.a_lo);
+  const float2 nc2 = make_float2(-ms.cd_hi, -ms.cd_hi), cl2 = make_float2(ms.cd_lo, ms.cd_lo);
 #pragma unroll
-  for (int w = 0; w < (int)(sizeof(s.v) / 16); ++w)
-    ElemTraits<TIn>::unpack(s.v[w], x + w * ElemTraits<TIn>::kPerVec);
+  for (int j = 0; j < 4; ++j) {
+    const float2 pt = ex2x2(f32x2_sub(f32x2_fma(seg_pair(t, j), sc2, na2), al2));
+    if (ms.has_q) {
+      const float2 qd = ex2x2(f32x2_sub(f32x2_fma(seg_pair(d, j), sc2, nc2), cl2));
+      const float2 df = f32x2_sub(pt, qd);
+      r[2 * j] = fmaxf(df.x, 0.0f);
+      r[2 * j + 1] = fmaxf(df.y, 0.0f);
+    } else {
+      r[2 * j] = pt.x;
+      r[2 * j + 1] = pt.y;
+    }
+  }
 }
 
-// Segments a warp keeps in flight per row.
+// Bonus entries relative to the segment reference msr = fl(m*sc), m the
+// segment max (an all -inf segment has no mass).
 template <typename TIn>
-__host__ __device__ constexpr int seg_batch() {
-  return sizeof(TIn) == 2 ? 4 : 2;
+__device__ __forceinline__ void bonus_masses(const Seg8<TIn>& t, float sc, float msr,
+                                             float (&r)[8]) {
+  const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-msr, -msr);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 e = ex2x2(f32x2_fma(seg_pair(t, j), sc2, nm2));
+    r[2 * j] = msr == -INFINITY ? 0.0f : e.x;
+    r[2 * j + 1] = msr == -INFINITY ? 0.0f : e.y;
+  }
 }
 
-// Mass of one entry: 2^(zt*sc - a) for p (a = its log2 normaliser, or a
-// slice reference for the bonus), minus 2^(zd*sc - c_d) for q when there is
-// a draft row, clamped at 0.  a and c_d come as hi + lo single-precision
-// pairs so that the normaliser keeps double accuracy.  The slice pass and
-// the re-scan call this with identical arguments, so both see the same bits.
-__device__ __forceinline__ float entry_mass(float zt, float zd, float sc, float a_hi, float a_lo,
-                                            float cd_hi, float cd_lo, bool has_q) {
-  const float p = ex2(__fsub_rn(fmaf(zt, sc, -a_hi), a_lo));
-  if (!has_q) return p;
-  const float q = ex2(__fsub_rn(fmaf(zd, sc, -cd_hi), cd_lo));
-  return fmaxf(__fsub_rn(p, q), 0.0f);
+template <typename TIn>
+__device__ __forceinline__ float seg8_max(const Seg8<TIn>& t) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 z = seg_pair(t, j);
+    m = fmaxf(m, fmaxf(z.x, z.y));
+  }
+  return m;
+}
+
+// Sum of 8 entries in a fixed order (pairs first).
+__device__ __forceinline__ float sum8(const float (&r)[8]) {
+  const float2 a = f32x2_add(make_float2(r[0], r[1]), make_float2(r[2], r[3]));
+  const float2 b = f32x2_add(make_float2(r[4], r[5]), make_float2(r[6], r[7]));
+  const float2 c = f32x2_add(a, b);
+  return __fadd_rn(c.x, c.y);
+}
+
+__device__ __forceinline__ float warp_sum_f32(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, off));
+  return x;
+}
+
+__device__ __forceinline__ float warp_max_f32(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+  return x;
+}
+
+// 2^(a - b) for single-precision a, b: the difference is taken exactly in
+// double and rounded once; relative error about 1e-7.
+__device__ __forceinline__ float exp2_diff(float a, float b) {
+  return exp2f((float)((double)a - (double)b));
+}
+
+// CDF weight of a segment record: its mass, or for the bonus its sum
+// rescaled from its own reference to REF.
+__device__ __forceinline__ double seg_weight(float2 r, bool bonus, float sc, float REF) {
+  if (!bonus) return (double)r.x;
+  if (r.y == 0.0f) return 0.0;
+  return (double)r.y * (double)exp2_diff(__fmul_rn(r.x, sc), REF);
+}
+
+__device__ __forceinline__ void split_hi_lo(double c, float* hi, float* lo) {
+  *hi = (float)c;
+  *lo = (float)(c - (double)*hi);
+}
+
+// ---------------------------------------------------------------------------
+// Slice passes.  Warp w takes segments s_lo + w, s_lo + w + 8, ... in
+// batches of U; the next batch is loaded before the current one is
+// computed, so that every warp always has loads in flight.
+// ---------------------------------------------------------------------------
+
+template <typename TIn>
+__host__ __device__ constexpr int slice_batch() {
+  return sizeof(TIn) == 2 ? 2 : 1;
+}
+
+// Records of segments [s_lo, s_hi): (mass, 0), or for the bonus (m, s).
+template <typename TIn>
+__device__ void slice_records(const TIn* rt, const TIn* rd, int V, const MassSpec& ms, bool bonus,
+                              int s_lo, int s_hi, float2* rec, bool vec_ok) {
+  constexpr int U = slice_batch<TIn>();
+  constexpr int STEP = kFinalWarps * U;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool has_q = !bonus && ms.has_q;
+  Seg8<TIn> ta[U], da[U], tb[U], db[U];
+  auto load = [&](Seg8<TIn>(&t)[U], Seg8<TIn>(&d)[U], int s0) {
+#pragma unroll
+    for (int q = 0; q < U; ++q) {
+      const int seg = s0 + q * kFinalWarps;
+      if (seg < s_hi) {
+        seg_load(t[q], rt, seg * kSegElems + lane * 8, V, vec_ok);
+        if (has_q) seg_load(d[q], rd, seg * kSegElems + lane * 8, V, vec_ok);
+      }
+    }
+  };
+  auto process = [&](const Seg8<TIn>(&t)[U], const Seg8<TIn>(&d)[U], int s0) {
+#pragma unroll
+    for (int q = 0; q < U; ++q) {
+      const int seg = s0 + q * kFinalWarps;
+      if (seg >= s_hi) break;
+      float r[8];
+      float2 out;
+      if (bonus) {
+        const float m = warp_max_f32(seg8_max(t[q]));
+        bonus_masses(t[q], ms.sc, __fmul_rn(m, ms.sc), r);
+        out = make_float2(m, warp_sum_f32(sum8(r)));
+      } else {
+        entry_masses(t[q], d[q], ms, r);
+        out = make_float2(warp_sum_f32(sum8(r)), 0.0f);
+      }
+      if (lane == 0) __stcg(&rec[seg], out);
+    }
+  };
+  int s0 = s_lo + warp;
+  if (s0 >= s_hi) return;
+  load(ta, da, s0);
+  for (;;) {
+    if (s0 + STEP < s_hi) load(tb, db, s0 + STEP);
+    process(ta, da, s0);
+    s0 += STEP;
+    if (s0 >= s_hi) break;
+    if (s0 + STEP < s_hi) load(ta, da, s0 + STEP);
+    process(tb, db, s0);
+    s0 += STEP;
+    if (s0 >= s_hi) break;
+  }
+}
+
+// Largest entry of segments [s_lo, s_hi) and its lowest index (block-wide).
+template <typename TIn>
+__device__ ArgAcc slice_argmax(const TIn* row, int V, int s_lo, int s_hi, bool vec_ok,
+                               FinalShared& sh) {
+  constexpr int U = 2 * slice_batch<TIn>();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  ArgAcc a;
+  arg_init(a);
+  for (int s0 = s_lo + warp; s0 < s_hi; s0 += kFinalWarps * U) {
+    Seg8<TIn> t[U];
+#pragma unroll
+    for (int q = 0; q < U; ++q) {
+      const int seg = s0 + q * kFinalWarps;
+      if (seg < s_hi) seg_load(t[q], row, seg * kSegElems + lane * 8, V, vec_ok);
+    }
+#pragma unroll
+    for (int q = 0; q < U; ++q) {
+      const int seg = s0 + q * kFinalWarps;
+      if (seg >= s_hi) break;
+      const int e0 = seg * kSegElems + lane * 8;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 z = seg_pair(t[q], j);
+        arg_add(a, z.x, e0 + 2 * j);
+        arg_add(a, z.y, e0 + 2 * j + 1);
+      }
+    }
+  }
+  arg_warp_reduce(a);
+  if (lane == 0) {
+    sh.warp_f[warp] = a.v;
+    sh.warp_i[warp] = a.i;
+  }
+  __syncthreads();
+  ArgAcc r;
+  arg_init(r);
+#pragma unroll
+  for (int w = 0; w < kFinalWarps; ++w) {
+    ArgAcc o;
+    o.v = sh.warp_f[w];
+    o.i = sh.warp_i[w];
+    arg_merge(r, o);
+  }
+  __syncthreads();
+  return r;
 }
 
 // Block-wide exclusive scan of one double per thread; all threads get the total.
@@ -156,193 +355,81 @@ __device__ __forceinline__ double block_exclusive_scan_f64(double x, FinalShared
   return ex;
 }
 
-// Slice bounds in segments.
-__device__ __forceinline__ int slice_lo(int part, int nseg, int P) {
-  return (int)(((long long)part * nseg) / P);
-}
-__device__ __forceinline__ int slice_of(int seg, int nseg, int P) {
-  int p = (int)(((long long)seg * P) / nseg);
-  while (p + 1 < P && slice_lo(p + 1, nseg, P) <= seg) ++p;
-  while (p > 0 && slice_lo(p, nseg, P) > seg) --p;
-  return p;
-}
-
-// Segment masses of segments [s_lo, s_hi) into seg_mass (global): warp w
-// takes segments s_lo + w, s_lo + w + 8, ... (a few at a time, loads first);
-// lane l holds entries 8l..8l+7 of a segment.  rd == nullptr: no draft row.
+// Inverse CDF over the request's segment records (global, nseg entries):
+// the first entry whose cumulative weight exceeds u * total.  Block-wide;
+// returns the token, or -1 if the total weight is not a finite positive
+// number.  rec_sm: nseg float2 of shared memory.
 template <typename TIn>
-__device__ void slice_masses(const TIn* rt, const TIn* rd, int V, float sc, float a_hi, float a_lo,
-                             float cd_hi, float cd_lo, int s_lo, int s_hi, float* seg_mass,
-                             bool vec_ok) {
+__device__ int cdf_pick(const TIn* rt, const TIn* rd, int V, const MassSpec& ms, bool bonus,
+                        double u, const float2* rec, int nseg, bool vec_ok, FinalShared& sh,
+                        float2* rec_sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool has_q = (rd != nullptr);
-  constexpr int U = seg_batch<TIn>();
-  for (int s0 = s_lo + warp; s0 < s_hi; s0 += kFinalWarps * U) {
-    Seg8<TIn> t[U], d[U];
-#pragma unroll
-    for (int q = 0; q < U; ++q) {
-      const int seg = s0 + q * kFinalWarps;
-      if (seg < s_hi) {
-        seg_load(t[q], rt, seg * kSegElems + lane * 8, V, vec_ok);
-        if (has_q) seg_load(d[q], rd, seg * kSegElems + lane * 8, V, vec_ok);
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < U; ++q) {
-      const int seg = s0 + q * kFinalWarps;
-      if (seg >= s_hi) break;
-      float zt[8], zd[8];
-      seg_unpack(t[q], zt);
-      if (has_q) seg_unpack(d[q], zd);
-      float m = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        m = __fadd_rn(m, entry_mass(zt[e], has_q ? zd[e] : 0.f, sc, a_hi, a_lo, cd_hi, cd_lo,
-                                    has_q));
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = __fadd_rn(m, __shfl_xor_sync(0xffffffffu, m, off));
-      if (lane == 0) __stcg(&seg_mass[seg], m);
-    }
+  float refm = -FLT_MAX;
+  for (int s = threadIdx.x; s < nseg; s += kFinalThreads) {
+    const float2 r = __ldcg(&rec[s]);
+    rec_sm[s] = r;
+    if (bonus && r.y > 0.0f) refm = fmaxf(refm, __fmul_rn(r.x, ms.sc));
   }
-}
-
-// Largest entry of segments [s_lo, s_hi) (block-wide; all threads get it).
-template <typename TIn>
-__device__ float slice_max(const TIn* row, int V, int s_lo, int s_hi, bool vec_ok, FinalShared& sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int U = 2 * seg_batch<TIn>();
-  float m = -INFINITY;
-  for (int s0 = s_lo + warp; s0 < s_hi; s0 += kFinalWarps * U) {
-    Seg8<TIn> t[U];
-#pragma unroll
-    for (int q = 0; q < U; ++q) {
-      const int seg = s0 + q * kFinalWarps;
-      if (seg < s_hi) seg_load(t[q], row, seg * kSegElems + lane * 8, V, vec_ok);
-    }
-#pragma unroll
-    for (int q = 0; q < U; ++q) {
-      if (s0 + q * kFinalWarps >= s_hi) break;
-      float z[8];
-      seg_unpack(t[q], z);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) m = fmaxf(m, z[e]);
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  if (lane == 0) sh.warp_f[warp].x = m;
-  __syncthreads();
-  float r = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < kFinalWarps; ++w) r = fmaxf(r, sh.warp_f[w].x);
-  __syncthreads();
-  return r;
-}
-
-// Largest entry of segments [s_lo, s_hi) and its lowest index (block-wide).
-template <typename TIn>
-__device__ ArgAcc slice_argmax(const TIn* row, int V, int s_lo, int s_hi, bool vec_ok,
-                               FinalShared& sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int U = 2 * seg_batch<TIn>();
-  ArgAcc a;
-  arg_init(a);
-  for (int s0 = s_lo + warp; s0 < s_hi; s0 += kFinalWarps * U) {
-    Seg8<TIn> t[U];
-#pragma unroll
-    for (int q = 0; q < U; ++q) {
-      const int seg = s0 + q * kFinalWarps;
-      if (seg < s_hi) seg_load(t[q], row, seg * kSegElems + lane * 8, V, vec_ok);
-    }
-#pragma unroll
-    for (int q = 0; q < U; ++q) {
-      const int seg = s0 + q * kFinalWarps;
-      if (seg >= s_hi) break;
-      float z[8];
-      seg_unpack(t[q], z);
-      const int e0 = seg * kSegElems + lane * 8;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) arg_add(a, z[e], e0 + e);
-    }
-  }
-  arg_warp_reduce(a);
-  if (lane == 0) sh.warp_f[warp] = make_float4(a.v, __int_as_float(a.i), 0.f, 0.f);
-  __syncthreads();
-  ArgAcc r;
-  arg_init(r);
-#pragma unroll
-  for (int w = 0; w < kFinalWarps; ++w) {
-    ArgAcc o;
-    o.v = sh.warp_f[w].x;
-    o.i = __float_as_int(sh.warp_f[w].y);
-    arg_merge(r, o);
+  float REF = 0.0f;
+  if (bonus) {
+    refm = warp_max_f32(refm);
+    if (lane == 0) sh.warp_f[warp] = refm;
   }
   __syncthreads();
-  return r;
-}
-
-// How the masses of one request were formed, for the re-scan.
-struct MassSpec {
-  float sc;
-  float a_hi, a_lo;      // p's normaliser (residual, or p alone)
-  float cd_hi, cd_lo;    // q's normaliser (residual)
-  bool has_q;
-  bool slice_ref;        // bonus: p's reference is the segment's slice reference
-};
-
-// Inverse CDF over the request's segment masses (global, nseg entries, each
-// scaled by sh.scale[slice]): the first entry whose cumulative mass exceeds
-// u * total.  Block-wide; returns the token, or -1 if the total mass is not
-// a finite positive number.
-template <typename TIn>
-__device__ int cdf_pick(const TIn* rt, const TIn* rd, int V, const MassSpec& ms,
-                        const float* slice_ref, int P, double u, const float* seg_mass, int nseg,
-                        bool vec_ok, FinalShared& sh, double* seg_excl, float* seg_val) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int s = threadIdx.x; s < nseg; s += kFinalThreads) seg_val[s] = __ldcg(&seg_mass[s]);
-  __syncthreads();
-  // Exclusive prefix of the scaled segment masses, in double.
+  if (bonus) {
+    REF = -FLT_MAX;
+#pragma unroll
+    for (int w = 0; w < kFinalWarps; ++w) REF = fmaxf(REF, sh.warp_f[w]);
+  }
+  // Exclusive prefix of the weights, in double; thread t owns [sa, sb).
   const int per = (nseg + kFinalThreads - 1) / kFinalThreads;
   const int sa = min(nseg, (int)threadIdx.x * per), sb = min(nseg, sa + per);
   double loc = 0.0;
-  for (int s = sa; s < sb; ++s) loc += (double)seg_val[s] * (double)sh.scale[slice_of(s, nseg, P)];
+  for (int s = sa; s < sb; ++s) loc += seg_weight(rec_sm[s], bonus, ms.sc, REF);
   double total;
   double run = block_exclusive_scan_f64(loc, sh, &total);
-  for (int s = sa; s < sb; ++s) {
-    seg_excl[s] = run;
-    run += (double)seg_val[s] * (double)sh.scale[slice_of(s, nseg, P)];
-  }
   if (!(total > 0.0 && total <= 1.79e308)) return -1;  // uniform across the block
   const double target = u * total;
 
-  // The last segment with positive mass that starts at or before target.
+  // The last segment with positive weight that starts at or before target.
   if (threadIdx.x == 0) sh.cand = -1;
   __syncthreads();
   int cand = -1;
-  for (int s = sa; s < sb; ++s)
-    if (seg_val[s] > 0.0f && sh.scale[slice_of(s, nseg, P)] > 0.0f && seg_excl[s] <= target) cand = s;
+  double cand_excl = 0.0;
+  for (int s = sa; s < sb; ++s) {
+    const double w = seg_weight(rec_sm[s], bonus, ms.sc, REF);
+    if (w > 0.0 && run <= target) {
+      cand = s;
+      cand_excl = run;
+    }
+    run += w;
+  }
   if (cand >= 0) atomicMax(&sh.cand, cand);
   __syncthreads();
   const int j = sh.cand;
+  if (cand >= 0 && cand == j) sh.cand_excl = cand_excl;
+  __syncthreads();
 
-  // Re-read segment j: the first entry whose cumulative mass exceeds the
+  // Re-read segment j: the first entry whose cumulative weight exceeds the
   // target, or the segment's last entry with mass when rounding left the
   // target just past the segment's own sum.
   if (warp == 0) {
-    const int pj = slice_of(j, nseg, P);
-    const double scale = (double)sh.scale[pj];
-    const float a_hi = ms.slice_ref ? __ldcg(&slice_ref[pj]) : ms.a_hi;
-    const float a_lo = ms.slice_ref ? 0.0f : ms.a_lo;
-    const int e0 = j * kSegElems + lane * 8;
-    float zt[8], zd[8];
-    load8(rt, e0, V, vec_ok, zt);
-    if (ms.has_q) load8(rd, e0, V, vec_ok, zd);
-    float r[8], c[8];
+    Seg8<TIn> t, d;
+    seg_load(t, rt, j * kSegElems + lane * 8, V, vec_ok);
+    if (ms.has_q && !bonus) seg_load(d, rd, j * kSegElems + lane * 8, V, vec_ok);
+    float r[8];
+    double scale = 1.0;
+    if (bonus) {
+      const float msr = __fmul_rn(rec_sm[j].x, ms.sc);
+      bonus_masses(t, ms.sc, msr, r);
+      scale = (double)exp2_diff(msr, REF);
+    } else {
+      entry_masses(t, d, ms, r);
+    }
+    float c[8];
     float run_f = 0.0f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      r[e] = entry_mass(zt[e], ms.has_q ? zd[e] : 0.f, ms.sc, a_hi, a_lo, ms.cd_hi, ms.cd_lo,
-                        ms.has_q);
       run_f = __fadd_rn(run_f, r[e]);
       c[e] = run_f;
     }
@@ -354,7 +441,7 @@ __device__ int cdf_pick(const TIn* rt, const TIn* rd, int V, const MassSpec& ms,
     }
     float lex = __shfl_up_sync(0xffffffffu, incl, 1);
     if (lane == 0) lex = 0.0f;
-    const double tprime = target - seg_excl[j];
+    const double tprime = target - sh.cand_excl;
     int first_e = 8, last_pos = -1;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -375,9 +462,14 @@ __device__ int cdf_pick(const TIn* rt, const TIn* rd, int V, const MassSpec& ms,
     if (lane == 0) sh.token = token;
   }
   __syncthreads();
-  const int t = sh.token;
+  const int tk = sh.token;
   __syncthreads();
-  return t;
+  return tk;
+}
+
+// Slice bounds in segments.
+__device__ __forceinline__ int slice_lo(int part, int nseg, int P) {
+  return (int)(((long long)part * nseg) / P);
 }
 
 template <typename TIn>
@@ -385,72 +477,90 @@ __global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) 
   extern __shared__ __align__(16) unsigned char fsm_raw[];
   __shared__ FinalShared sh;
   const int nseg = segments_of(p.V);
-  double* seg_excl = reinterpret_cast<double*>(fsm_raw);
-  float* seg_val = reinterpret_cast<float*>(fsm_raw + (size_t)nseg * sizeof(double));
+  float2* rec_sm = reinterpret_cast<float2*>(fsm_raw);
 
   pdl_wait();
   const int part = blockIdx.x, b = blockIdx.y, P = gridDim.x;
   WsHeader* h = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
-  const int32_t* flags = reinterpret_cast<const int32_t*>(p.ws + p.lay.flags);
-  const uint32_t* acc_bits = reinterpret_cast<const uint32_t*>(p.ws + p.lay.acc_bits);
-  const uint32_t* dec_bits = reinterpret_cast<const uint32_t*>(p.ws + p.lay.dec_bits);
-  const uint32_t* bad_bits = reinterpret_cast<const uint32_t*>(p.ws + p.lay.bad_bits);
-  const double* pos_c = reinterpret_cast<const double*>(p.ws + p.lay.pos_c);
-  const int32_t* pos_arg = reinterpret_cast<const int32_t*>(p.ws + p.lay.pos_arg);
-  float* seg_mass = reinterpret_cast<float*>(p.ws + p.lay.seg_mass) + (size_t)b * nseg;
+  float2* rec = reinterpret_cast<float2*>(p.ws + p.lay.seg_mass) + (size_t)b * nseg;
   float* slice_ref = reinterpret_cast<float*>(p.ws + p.lay.slice_ref) + (size_t)b * kMaxSlices;
   int32_t* slice_arg = reinterpret_cast<int32_t*>(p.ws + p.lay.slice_arg) + (size_t)b * kMaxSlices;
   int32_t* final_done = reinterpret_cast<int32_t*>(p.ws + p.lay.final_done);
-  const int L = p.lengths[b];
-  const float T = p.temperature[b];
+  const int L = __ldg(&p.lengths[b]);
+  const float T = __ldg(&p.temperature[b]);
 
-  // n from the decision masks: the first rejected position, or L.
-  if (threadIdx.x == 0) {
-    const int f = __ldcg(&flags[b]);
-    int job = kJobInvalid, n = -1, token = -1;
-    if (f & kReqValid) {
-      const uint32_t dec = __ldcg(&dec_bits[b]), acc = __ldcg(&acc_bits[b]);
-      const uint32_t bad = __ldcg(&bad_bits[b]);
-      const uint32_t lmask = (L >= 32) ? 0xffffffffu : ((1u << L) - 1u);
-      const uint32_t rej = dec & ~acc & lmask;
-      n = rej ? (__ffs((int)rej) - 1) : L;
-      const uint32_t prefix = (n >= 32) ? 0xffffffffu : ((1u << n) - 1u);
-      if ((dec & acc & prefix) != prefix) {
-        if (part == 0) record_status(h, SPEC_ERR_INTERNAL);
-        n = -1;
-      } else if (bad & (n < L ? ((prefix << 1) | 1u) : lmask)) {
-        if (part == 0) {
-          atomicAdd(&h->bad_requests, 1);
-          atomicMin(&h->first_bad, b);
-          record_status(h, SPEC_ERR_BAD_INPUT);
-        }
-        n = -1;
-      } else if (f & kReqGreedy) {
-        if (n < L) {
-          job = kJobNone;
-          token = __ldcg(&pos_arg[(size_t)b * p.k + n]);
-        } else {
-          job = kJobGreedyRowL;
-        }
-      } else {
-        job = (n < L) ? kJobResidual : kJobBonus;
-      }
+  // One round of independent loads: the request's flags and decision masks
+  // (lane 0) and every position's normalisers, argmax and draft token
+  // (lane t for position t); then n: the first rejected position, or L.
+  if (threadIdx.x < 32) {
+    const int t = threadIdx.x;
+    const double* pos_c = reinterpret_cast<const double*>(p.ws + p.lay.pos_c);
+    const int32_t* pos_arg = reinterpret_cast<const int32_t*>(p.ws + p.lay.pos_arg);
+    double ct = 0.0, cd = 0.0;
+    int g = -1, x = -1;
+    if (t < p.k) {
+      const size_t bi = (size_t)b * p.k + t;
+      ct = __ldcg(&pos_c[bi * 2]);
+      cd = __ldcg(&pos_c[bi * 2 + 1]);
+      g = __ldcg(&pos_arg[bi]);
+      x = __ldg(&p.tokens[bi]);
     }
-    sh.job = job;
-    sh.n = n;
-    sh.token = token;
+    int f = 0;
+    uint32_t dec = 0, acc = 0, bad = 0;
+    if (t == 0) {
+      f = __ldcg(reinterpret_cast<const int32_t*>(p.ws + p.lay.flags) + b);
+      dec = __ldcg(reinterpret_cast<const uint32_t*>(p.ws + p.lay.dec_bits) + b);
+      acc = __ldcg(reinterpret_cast<const uint32_t*>(p.ws + p.lay.acc_bits) + b);
+      bad = __ldcg(reinterpret_cast<const uint32_t*>(p.ws + p.lay.bad_bits) + b);
+    }
+    sh.pos_ct[t] = ct;
+    sh.pos_cd[t] = cd;
+    sh.pos_arg[t] = g;
+    sh.tok[t] = x;
+    __syncwarp();
+    if (t == 0) {
+      int job = kJobInvalid, n = -1, token = -1;
+      if (f & kReqValid) {
+        const uint32_t lmask = (L >= 32) ? 0xffffffffu : ((1u << L) - 1u);
+        const uint32_t rej = dec & ~acc & lmask;
+        n = rej ? (__ffs((int)rej) - 1) : L;
+        const uint32_t prefix = (n >= 32) ? 0xffffffffu : ((1u << n) - 1u);
+        if ((dec & acc & prefix) != prefix) {
+          if (part == 0) record_status(h, SPEC_ERR_INTERNAL);
+          n = -1;
+        } else if (bad & (n < L ? ((prefix << 1) | 1u) : lmask)) {
+          if (part == 0) {
+            atomicAdd(&h->bad_requests, 1);
+            atomicMin(&h->first_bad, b);
+            record_status(h, SPEC_ERR_BAD_INPUT);
+          }
+          n = -1;
+        } else if (f & kReqGreedy) {
+          if (n < L) {
+            job = kJobNone;
+            token = sh.pos_arg[n];
+          } else {
+            job = kJobGreedyRowL;
+          }
+        } else {
+          job = (n < L) ? kJobResidual : kJobBonus;
+        }
+      }
+      sh.job = job;
+      sh.n = n;
+      sh.token = token;
+    }
   }
   __syncthreads();
   const int job = sh.job;
   const int n = sh.n;
   int token = sh.token;
-  __syncthreads();
 
   auto write_outputs = [&](bool invalid, int final_token) {
     for (int j = threadIdx.x; j <= p.k; j += kFinalThreads) {
       int v = -1;
       if (!invalid) {
-        if (j < n) v = p.tokens[(size_t)b * p.k + j];
+        if (j < n) v = sh.tok[j];
         else if (j == n) v = final_token;
       }
       p.out_tokens[(size_t)b * (p.k + 1) + j] = v;
@@ -466,37 +576,26 @@ __global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) 
   const TIn* trow = static_cast<const TIn*>(p.target) + ((size_t)b * (p.k + 1) + n) * (size_t)p.V;
   const TIn* drow = job == kJobResidual
                         ? static_cast<const TIn*>(p.draft) + ((size_t)b * p.k + n) * (size_t)p.V
-                        : nullptr;
+                        : trow;
   const bool vec_ok =
       ((reinterpret_cast<uintptr_t>(trow) | reinterpret_cast<uintptr_t>(drow)) & 15u) == 0;
   const int s_lo = slice_lo(part, nseg, P), s_hi = slice_lo(part + 1, nseg, P);
-  const float sc = job == kJobGreedyRowL ? 0.0f : softmax_scale(T);
   MassSpec ms = {};
-  ms.sc = sc;
+  ms.sc = job == kJobGreedyRowL ? 0.0f : softmax_scale(T);
+  const bool bonus = (job == kJobBonus);
   if (job == kJobResidual) {
-    const double ct = __ldcg(&pos_c[((size_t)b * p.k + n) * 2]);
-    const double cd = __ldcg(&pos_c[((size_t)b * p.k + n) * 2 + 1]);
-    ms.a_hi = (float)ct;
-    ms.a_lo = (float)(ct - (double)ms.a_hi);
-    ms.cd_hi = (float)cd;
-    ms.cd_lo = (float)(cd - (double)ms.cd_hi);
+    split_hi_lo(sh.pos_ct[n], &ms.a_hi, &ms.a_lo);
+    split_hi_lo(sh.pos_cd[n], &ms.cd_hi, &ms.cd_lo);
     ms.has_q = true;
-    slice_masses(trow, drow, p.V, sc, ms.a_hi, ms.a_lo, ms.cd_hi, ms.cd_lo, s_lo, s_hi, seg_mass,
-                 vec_ok);
-  } else if (job == kJobBonus) {
-    // Reference: this slice's max (an all -inf slice keeps -FLT_MAX and zero mass).
-    const float m = slice_max(trow, p.V, s_lo, s_hi, vec_ok, sh);
-    const float ref = (m == -INFINITY) ? -FLT_MAX : __fmul_rn(m, sc);
-    ms.slice_ref = true;
-    slice_masses(trow, static_cast<const TIn*>(nullptr), p.V, sc, ref, 0.0f, 0.0f, 0.0f, s_lo,
-                 s_hi, seg_mass, vec_ok);
-    if (threadIdx.x == 0) __stcg(&slice_ref[part], ref);
-  } else {
+  }
+  if (job == kJobGreedyRowL) {
     const ArgAcc a = slice_argmax(trow, p.V, s_lo, s_hi, vec_ok, sh);
     if (threadIdx.x == 0) {
       __stcg(&slice_ref[part], a.v);
       __stcg(&slice_arg[part], a.i);
     }
+  } else {
+    slice_records(trow, drow, p.V, ms, bonus, s_lo, s_hi, rec, vec_ok);
   }
 
   // ---- the last slice CTA of the request combines ----
@@ -526,33 +625,17 @@ __global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) 
     token = sh.token;
     bad = (token == INT32_MAX);
   } else {
-    // Per-slice scale: 2^(ref_p - max ref) for the bonus, 1 for a residual.
-    if (threadIdx.x < 32) {
-      const int q = threadIdx.x;
-      float r = (job == kJobBonus && q < P) ? __ldcg(&slice_ref[q]) : -FLT_MAX;
-      float rm = r;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) rm = fmaxf(rm, __shfl_xor_sync(0xffffffffu, rm, off));
-      if (q < P && q < kMaxSlices) {
-        sh.scale[q] = job == kJobBonus
-                          ? (r > -FLT_MAX ? exp2f((float)((double)r - (double)rm)) : 0.0f)
-                          : 1.0f;
-      }
-    }
-    __syncthreads();
-    const double u = (double)p.uniforms[(size_t)b * (p.k + 1) + L];
-    token = cdf_pick(trow, drow, p.V, ms, slice_ref, P, u, seg_mass, nseg, vec_ok, sh, seg_excl,
-                     seg_val);
+    const double u = (double)__ldg(&p.uniforms[(size_t)b * (p.k + 1) + L]);
+    token = cdf_pick(trow, drow, p.V, ms, bonus, u, rec, nseg, vec_ok, sh, rec_sm);
     if (token < 0 && job == kJobResidual) {
       // Residual mass zero (p_n == q_n up to rounding): draw from p_n.
       if (threadIdx.x == 0) atomicAdd(&h->residual_zero, 1);
       MassSpec pm = ms;
       pm.has_q = false;
-      slice_masses(trow, static_cast<const TIn*>(nullptr), p.V, sc, pm.a_hi, pm.a_lo, 0.0f, 0.0f,
-                   0, nseg, seg_mass, vec_ok);
+      slice_records(trow, trow, p.V, pm, false, 0, nseg, rec, vec_ok);
+      __threadfence_block();
       __syncthreads();
-      token = cdf_pick(trow, static_cast<const TIn*>(nullptr), p.V, pm, slice_ref, P, u, seg_mass,
-                       nseg, vec_ok, sh, seg_excl, seg_val);
+      token = cdf_pick(trow, trow, p.V, pm, false, u, rec, nseg, vec_ok, sh, rec_sm);
     }
     bad = (token < 0);
   }

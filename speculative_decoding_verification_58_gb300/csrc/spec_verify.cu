@@ -133,7 +133,7 @@ cudaError_t device_info(DeviceInfo** out) {
     if ((e = sweep_blocks<uint16_t, true>(&d.sweep_blocks_per_sm[1][1])) != cudaSuccess) return e;
     if ((e = sweep_blocks<float, false>(&d.sweep_blocks_per_sm[0][0])) != cudaSuccess) return e;
     if ((e = sweep_blocks<uint16_t, false>(&d.sweep_blocks_per_sm[1][0])) != cudaSuccess) return e;
-    const int fsm = (int)(kMaxSegs * (sizeof(double) + sizeof(float)));
+    const int fsm = (int)(kMaxSegs * sizeof(float2));
     if ((e = cudaFuncSetAttribute(final_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   fsm)) != cudaSuccess)
       return e;
@@ -272,7 +272,7 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
   if (P > nseg) P = nseg;
   if (P < 1) P = 1;
   fp.P = P;
-  const size_t fsm = (size_t)nseg * (sizeof(double) + sizeof(float));
+  const size_t fsm = (size_t)nseg * sizeof(float2);
   if (record(ev, 2, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   if (launch(final_kernel<TIn>, dim3(P, B), dim3(kFinalThreads), fsm, stream, pdl, fp) !=
       cudaSuccess)

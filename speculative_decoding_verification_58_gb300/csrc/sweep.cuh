@@ -400,8 +400,11 @@ __device__ __forceinline__ void arg_stage(ArgAcc& a, const uint4 (&v)[kVecPerThr
 // ---------------------------------------------------------------------------
 // Decision for (b, i) once all of its chunks are in (warp-cooperative).
 // ---------------------------------------------------------------------------
+// x and u (token x_i and uniform u_i) were loaded one unit earlier, when
+// the chunk count was taken.
 template <typename TIn>
-__device__ void decide_position(const SweepParams& p, int bi, bool greedy, float sc) {
+__device__ void decide_position(const SweepParams& p, int bi, bool greedy, float sc, int x,
+                                float u_i) {
   const int lane = threadIdx.x & 31;
   const int b = bi / p.k;
   const int i = bi - b * p.k;
@@ -413,7 +416,6 @@ __device__ void decide_position(const SweepParams& p, int bi, bool greedy, float
   uint32_t* acc_bits = reinterpret_cast<uint32_t*>(p.ws + p.lay.acc_bits);
   uint32_t* dec_bits = reinterpret_cast<uint32_t*>(p.ws + p.lay.dec_bits);
   int32_t* first_reject = reinterpret_cast<int32_t*>(p.ws + p.lay.first_reject);
-  const int x = __ldg(&p.tokens[(size_t)b * p.k + i]);
 
   bool accept, row_ok, late;
   if (greedy) {
@@ -424,19 +426,20 @@ __device__ void decide_position(const SweepParams& p, int bi, bool greedy, float
     accept = (g == x);
     if (lane == 0) __stcg(&pos_arg[bi], g);
   } else {
-    // Target chunks then draft chunks: the two slots are adjacent.
-    double ct, cd;
-    bool okt, okd;
-    pair_log2_normalisers(pt, p.nch, sc, &ct, &cd, &okt, &okd, &late);
-    row_ok = okt && okd;
+    // The gathers of z_t[x] and z_d[x] go out first and overlap the partial
+    // loads.  Target chunks then draft chunks: the two slots are adjacent.
     const float zt = ElemTraits<TIn>::load(
         static_cast<const TIn*>(p.target) + ((size_t)b * (p.k + 1) + i) * (size_t)p.V, x);
     const float zd = ElemTraits<TIn>::load(
         static_cast<const TIn*>(p.draft) + ((size_t)b * p.k + i) * (size_t)p.V, x);
+    double ct, cd;
+    bool okt, okd;
+    pair_log2_normalisers(pt, p.nch, sc, &ct, &cd, &okt, &okd, &late);
+    row_ok = okt && okd;
     // log2 p(x) and log2 q(x) in double: z*sc is exact in double.
     const double lp = (double)zt * (double)sc - ct;
     const double lq = (double)zd * (double)sc - cd;
-    const double u = (double)__ldg(&p.uniforms[(size_t)b * (p.k + 1) + i]);
+    const double u = (double)u_i;
     // A token the target gives probability zero is never accepted; a token
     // the drafter gives probability zero (and the target not) always is.
     // 2^d in single precision: near any threshold u the absolute error is
@@ -574,13 +577,14 @@ __device__ void sweep_bookkeeper(const SweepParams& p, SweepSmem& sm, WsHeader* 
   // orders a partial before its count: the deciding CTA instead waits for
   // each partial slot of (b, i) to leave the empty marker, which it does
   // because every counted unit has already issued its store.
-  int pend_bi = -1, pend_old = 0, pend_need = 0;
+  int pend_bi = -1, pend_old = 0, pend_need = 0, pend_x = 0;
   bool pend_greedy = false;
-  float pend_sc = 0.0f;
+  float pend_sc = 0.0f, pend_u = 0.0f;
   auto resolve_pending = [&]() {
     if (!kVerify || pend_bi < 0) return;
     const int old = __shfl_sync(0xffffffffu, pend_old, 0);
-    if (old == pend_need - 1) decide_position<TIn>(p, pend_bi, pend_greedy, pend_sc);
+    if (old == pend_need - 1)
+      decide_position<TIn>(p, pend_bi, pend_greedy, pend_sc, pend_x, pend_u);
     pend_bi = -1;
   };
   for (int u = 0;; ++u) {
@@ -641,6 +645,12 @@ __device__ void sweep_bookkeeper(const SweepParams& p, SweepSmem& sm, WsHeader* 
       pend_need = greedy ? p.nch : 2 * p.nch;
       pend_greedy = greedy;
       pend_sc = meta.sc;
+      // What a decision would need, loaded now so that it is in registers
+      // if this chunk turns out to be the last of (b, i).
+      const int pb = pend_bi / p.k;
+      const int pi = pend_bi - pb * p.k;
+      pend_x = __ldg(&p.tokens[(size_t)pb * p.k + pi]);
+      pend_u = __ldg(&p.uniforms[(size_t)pb * (p.k + 1) + pi]);
     }
   }
 }
