@@ -54,7 +54,22 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int* excl, int* warp_
   return total;
 }
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
+// Fill n 8-byte words at dst with v (dst 16-byte aligned): 16-byte stores,
+// consecutive threads on consecutive addresses.
+__device__ __forceinline__ void fill_u64(unsigned long long* dst, size_t n, unsigned long long v) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  const uint4 v4 = make_uint4((uint32_t)v, (uint32_t)(v >> 32), (uint32_t)v, (uint32_t)(v >> 32));
+  for (size_t j = threadIdx.x; j < n / 2; j += kPlanThreads) d4[j] = v4;
+  if ((n & 1) && threadIdx.x == 0) dst[n - 1] = v;
+}
+
+__device__ __forceinline__ void fill_u32(uint32_t* dst, size_t n, uint32_t v) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  for (size_t j = threadIdx.x; j < n / 4; j += kPlanThreads) d4[j] = make_uint4(v, v, v, v);
+  for (size_t j = (n & ~size_t(3)) + threadIdx.x; j < n; j += kPlanThreads) dst[j] = v;
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   // Dependents may launch now; they wait for this grid's completion before
   // reading anything it writes.
   pdl_launch_dependents();
@@ -65,12 +80,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   int2* rowdesc = reinterpret_cast<int2*>(p.ws + p.lay.rowdesc);
   int32_t* flags = reinterpret_cast<int32_t*>(p.ws + p.lay.flags);
   int32_t* first_reject = reinterpret_cast<int32_t*>(p.ws + p.lay.first_reject);
-  uint32_t* acc_bits = reinterpret_cast<uint32_t*>(p.ws + p.lay.acc_bits);
-  uint32_t* dec_bits = reinterpret_cast<uint32_t*>(p.ws + p.lay.dec_bits);
-  uint32_t* bad_bits = reinterpret_cast<uint32_t*>(p.ws + p.lay.bad_bits);
-  int32_t* done = reinterpret_cast<int32_t*>(p.ws + p.lay.done);
-  Partial* parts = reinterpret_cast<Partial*>(p.ws + p.lay.partials);
-  int32_t* final_done = reinterpret_cast<int32_t*>(p.ws + p.lay.final_done);
 
   if (tid == 0) {
     h->status = SPEC_OK;
@@ -87,28 +96,75 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   }
   const int words = (p.B + 31) >> 5;
   for (int w = tid; w < words; w += kPlanThreads) bad_mask[w] = 0u;
+
+  // Per-call state that does not depend on the inputs, with coalesced
+  // stores: decision masks, chunk and final-pass counters to zero, every
+  // partial slot to the empty marker (the deciding CTA waits for its slots
+  // to leave it).
+  fill_u32(reinterpret_cast<uint32_t*>(p.ws + p.lay.acc_bits), p.B, 0u);
+  fill_u32(reinterpret_cast<uint32_t*>(p.ws + p.lay.dec_bits), p.B, 0u);
+  fill_u32(reinterpret_cast<uint32_t*>(p.ws + p.lay.bad_bits), p.B, 0u);
+  fill_u32(reinterpret_cast<uint32_t*>(p.ws + p.lay.final_done), p.B, 0u);
+  fill_u32(reinterpret_cast<uint32_t*>(p.ws + p.lay.done), (size_t)p.B * p.k, 0u);
+  fill_u64(reinterpret_cast<unsigned long long*>(p.ws + p.lay.partials),
+           (size_t)p.B * p.k * 2 * p.C, kPartialEmpty);
   __syncthreads();
 
   // Pass 1, item j = b*(k+1) + i: the request's scalars (at i = 0: 1 <= L <= k
   // from the length head's clamp, T is 0 or a finite normal float), token x_i
-  // in [0, V) for i < L, uniform u_i in [0, 1) for i <= L when T > 0.
+  // in [0, V) for i < L, uniform u_i in [0, 1) for i <= L when T > 0.  Four
+  // items per thread per round, all loads issued before any is used.
   const int k1 = p.k + 1;
-  for (int j = tid; j < p.B * k1; j += kPlanThreads) {
-    const int b = j / k1;
-    const int i = j - b * k1;
-    const int L = __ldg(&p.lengths[b]);
-    const float T = __ldg(&p.temperature[b]);
-    const int x = i < p.k ? __ldg(&p.tokens[(size_t)b * p.k + i]) : 0;
-    const float u = __ldg(&p.uniforms[j]);
-    bool bad = (i == 0) && !(L >= 1 && L <= p.k && temperature_ok(T));
-    bad = bad || (i < L && i < p.k && (x < 0 || x >= p.V));
-    bad = bad || (T > 0.0f && i <= L && !(u >= 0.0f && u < 1.0f));  // NaN fails
-    if (bad) atomicOr(&bad_mask[b >> 5], 1u << (b & 31));
+  const int items1 = p.B * k1;
+  constexpr int kR = 4;
+  for (int base = 0; base < items1; base += kR * kPlanThreads) {
+    int L[kR], x[kR];
+    float T[kR], u[kR];
+#pragma unroll
+    for (int q = 0; q < kR; ++q) {
+      const int j = base + q * kPlanThreads + tid;
+      L[q] = 0;
+      x[q] = 0;
+      T[q] = 0.0f;
+      u[q] = 0.0f;
+      if (j < items1) {
+        const int b = j / k1;
+        const int i = j - b * k1;
+        L[q] = __ldg(&p.lengths[b]);
+        T[q] = __ldg(&p.temperature[b]);
+        if (i < p.k) x[q] = __ldg(&p.tokens[(size_t)b * p.k + i]);
+        u[q] = __ldg(&p.uniforms[j]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kR; ++q) {
+      const int j = base + q * kPlanThreads + tid;
+      if (j >= items1) break;
+      const int b = j / k1;
+      const int i = j - b * k1;
+      bool bad = (i == 0) && !(L[q] >= 1 && L[q] <= p.k && temperature_ok(T[q]));
+      bad = bad || (i < L[q] && i < p.k && (x[q] < 0 || x[q] >= p.V));
+      bad = bad || (T[q] > 0.0f && i <= L[q] && !(u[q] >= 0.0f && u[q] < 1.0f));  // NaN fails
+      if (bad) atomicOr(&bad_mask[b >> 5], 1u << (b & 31));
+    }
   }
   __syncthreads();
 
-  // Pass 2, item it = i*B + b: rows of (b, i), state resets (one item per
-  // request does the request-level ones), then the position-major layout.
+  // Request-level state.
+  for (int b = tid; b < p.B; b += kPlanThreads) {
+    const bool ok = !((bad_mask[b >> 5] >> (b & 31)) & 1u);
+    const bool greedy = __ldg(&p.temperature[b]) == 0.0f;
+    flags[b] = ok ? (kReqValid | (greedy ? kReqGreedy : 0)) : 0;
+    first_reject[b] = p.k;
+    if (!ok) {
+      atomicAdd(&h->bad_requests, 1);
+      atomicMin(&h->first_bad, b);
+      atomicCAS(&h->status, SPEC_OK, SPEC_ERR_BAD_INPUT);
+    }
+  }
+
+  // Pass 2, item it = i*B + b: the rows of (b, i) in position-major order;
+  // one block-wide scan places their descriptors.
   const int items = p.k * p.B;
   const int per = (items + kPlanThreads - 1) / kPlanThreads;
   const int lo = min(items, tid * per), hi = min(items, lo + per);
@@ -116,23 +172,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
   for (int it = lo; it < hi; ++it) {
     const int i = it / p.B, b = it - i * p.B;
     const bool ok = !((bad_mask[b >> 5] >> (b & 31)) & 1u);
-    const int L = __ldg(&p.lengths[b]);
-    const bool greedy = __ldg(&p.temperature[b]) == 0.0f;
-    done[(size_t)b * p.k + i] = 0;
-    if (i == 0) {
-      flags[b] = ok ? (kReqValid | (greedy ? kReqGreedy : 0)) : 0;
-      first_reject[b] = p.k;
-      acc_bits[b] = 0u;
-      dec_bits[b] = 0u;
-      bad_bits[b] = 0u;
-      final_done[b] = 0;
-      if (!ok) {
-        atomicAdd(&h->bad_requests, 1);
-        atomicMin(&h->first_bad, b);
-        atomicCAS(&h->status, SPEC_OK, SPEC_ERR_BAD_INPUT);
-      }
-    }
-    if (ok && i < L) cnt += greedy ? 1 : 2;
+    if (ok && i < __ldg(&p.lengths[b])) cnt += __ldg(&p.temperature[b]) == 0.0f ? 1 : 2;
   }
   int pos;
   const int total = block_exclusive_scan(cnt, &pos, warp_tot);
@@ -146,10 +186,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanParams p) {
     const int slot = (b * p.k + i) << 1;
     rowdesc[pos++] = make_int2(slot, __float_as_int(sc));
     if (T != 0.0f) rowdesc[pos++] = make_int2(slot | 1, __float_as_int(sc));
-    // The deciding CTA waits for these slots to leave the empty marker.
-    const int ntensor = T != 0.0f ? 2 : 1;
-    unsigned long long* slots = reinterpret_cast<unsigned long long*>(parts + (size_t)slot * p.nch);
-    for (int c = 0; c < ntensor * p.nch; ++c) slots[c] = kPartialEmpty;
   }
   if (tid == 0) {
     h->rows_planned = total;
