@@ -16,7 +16,7 @@ namespace specv {
 // ---------------------------------------------------------------------------
 
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e): exp(x) = 2^(x log2 e)
-constexpr double kLn2 = 0.69314718055994530942;
+constexpr float kLn2f = 0.693147180559945309f;  // ln 2
 
 // Sweep kernel geometry.
 constexpr int kSweepConsumerWarps = 8;
@@ -74,7 +74,7 @@ constexpr unsigned long long kPartialEmpty = 0x7FC0DEAD7FC0DEADull;
 
 struct WsLayout {
   size_t header, rowdesc, flags, first_reject, acc_bits, dec_bits, bad_bits, done, pos_c, pos_arg,
-      partials, seg_mass, slice_ref, slice_arg, final_done, total;
+      partials, seg_mass, slice_ref, slice_arg, final_done, warm, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -110,13 +110,14 @@ __host__ __device__ inline WsLayout ws_layout(int B, int k, int C, int V) {
   l.dec_bits = o;     o = align256(o + (size_t)B * sizeof(uint32_t));
   l.bad_bits = o;     o = align256(o + (size_t)B * sizeof(uint32_t));
   l.done = o;         o = align256(o + (size_t)B * k * sizeof(int32_t));
-  l.pos_c = o;        o = align256(o + slots * sizeof(double));
+  l.pos_c = o;        o = align256(o + (size_t)B * k * sizeof(float4));
   l.pos_arg = o;      o = align256(o + (size_t)B * k * sizeof(int32_t));
   l.partials = o;     o = align256(o + slots * (size_t)C * sizeof(Partial));
   l.seg_mass = o;     o = align256(o + (size_t)B * segments_of(V) * sizeof(float2));
   l.slice_ref = o;    o = align256(o + (size_t)B * kMaxSlices * sizeof(float));
   l.slice_arg = o;    o = align256(o + (size_t)B * kMaxSlices * sizeof(int32_t));
   l.final_done = o;   o = align256(o + (size_t)B * sizeof(int32_t));
+  l.warm = o;         o = align256(o + 2 * (size_t)C * sizeof(Partial));
   l.total = o;
   return l;
 }
@@ -364,10 +365,82 @@ __device__ __forceinline__ void arg_warp_reduce(ArgAcc& a) {
   }
 }
 
-// Double-precision warp sum (fixed butterfly order: all lanes get the same bits).
-__device__ __forceinline__ double warp_sum_f64(double x) {
+// ---------------------------------------------------------------------------
+// Float-float arithmetic: a value carried as an unevaluated sum hi + lo of
+// two floats (about 48 significant bits).  GB300 executes double precision
+// at a small fraction of its single-precision rate (a dependent double FMA
+// costs about 64 cycles, a float-double-float round trip about 190), so the
+// kernels keep their extra precision this way instead.  Built from the
+// error-free transformations TwoSum (Knuth), FastTwoSum (Dekker) and
+// TwoProduct with a fused multiply-add; every operation is an explicitly
+// rounded intrinsic so that the compiler cannot contract or reorder them.
+// ---------------------------------------------------------------------------
+struct FF {
+  float hi, lo;
+};
+
+// a + b = s + e exactly.
+__device__ __forceinline__ FF two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
+}
+
+// a + b = s + e exactly, given |a| >= |b| (or a == 0).
+__device__ __forceinline__ FF fast_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+// a * b = p + e exactly.
+__device__ __forceinline__ FF two_prod(float a, float b) {
+  const float p = __fmul_rn(a, b);
+  return {p, __fmaf_rn(a, b, -p)};
+}
+
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  FF s = two_sum(a.hi, b.hi);
+  const FF t = two_sum(a.lo, b.lo);
+  s.lo = __fadd_rn(s.lo, t.hi);
+  s = fast_two_sum(s.hi, s.lo);
+  s.lo = __fadd_rn(s.lo, t.lo);
+  return fast_two_sum(s.hi, s.lo);
+}
+
+__device__ __forceinline__ FF ff_neg(FF a) { return {-a.hi, -a.lo}; }
+__device__ __forceinline__ FF ff_sub(FF a, FF b) { return ff_add(a, ff_neg(b)); }
+
+__device__ __forceinline__ FF ff_add_f(FF a, float b) {
+  FF s = two_sum(a.hi, b);
+  s.lo = __fadd_rn(s.lo, a.lo);
+  return fast_two_sum(s.hi, s.lo);
+}
+
+__device__ __forceinline__ FF ff_mul_f(FF a, float b) {
+  FF p = two_prod(a.hi, b);
+  p.lo = __fmaf_rn(a.lo, b, p.lo);
+  return fast_two_sum(p.hi, p.lo);
+}
+
+// Comparisons of normalised values (|lo| at most half an ulp of hi).
+__device__ __forceinline__ bool ff_le(FF a, FF b) {
+  return a.hi < b.hi || (a.hi == b.hi && a.lo <= b.lo);
+}
+__device__ __forceinline__ float ff_to_float(FF a) { return __fadd_rn(a.hi, a.lo); }
+
+__device__ __forceinline__ FF ff_shfl_xor(FF a, int off) {
+  return {__shfl_xor_sync(0xffffffffu, a.hi, off), __shfl_xor_sync(0xffffffffu, a.lo, off)};
+}
+
+// Warp sum in a fixed butterfly order (every lane gets the same bits).
+__device__ __forceinline__ FF warp_sum_ff(FF x) {
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  for (int off = 16; off > 0; off >>= 1) {
+    const FF y = ff_shfl_xor(x, off);
+    // Combine in lane order so that both partners compute the same value.
+    x = (threadIdx.x & off) ? ff_add(y, x) : ff_add(x, y);
+  }
   return x;
 }
 
@@ -464,12 +537,18 @@ __device__ __forceinline__ void record_status(WsHeader* h, int code) {
 }
 
 // ---------------------------------------------------------------------------
-// Partials: single 8-byte relaxed stores and loads.
+// Partials: single 8-byte atomic exchanges and relaxed loads.
 // ---------------------------------------------------------------------------
 
+// The partial goes out as an atomic exchange: atomics are performed at L2,
+// so the value is visible to other SMs at once (a plain store may linger in
+// the SM until something drains it, and a deciding CTA would wait for it).
+// Nothing waits for the old value.
 __device__ __forceinline__ void store_partial(Partial* p, float m, uint32_t aux) {
   const unsigned long long v = ((unsigned long long)aux << 32) | __float_as_uint(m);
-  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+  asm volatile("{\n\t.reg .b64 t;\n\tatom.relaxed.gpu.global.exch.b64 t, [%0], %1;\n\t}" ::"l"(p),
+               "l"(v)
+               : "memory");
 }
 
 __device__ __forceinline__ unsigned long long load_u64_relaxed(const void* p) {
@@ -499,37 +578,40 @@ __device__ __forceinline__ bool load_partial(const Partial* p, float* m, uint32_
 
 // ---------------------------------------------------------------------------
 // Combine the chunk partials of one row into its base-2 log normaliser
-// c = fl(M*sc) + log2(S), where M is the row max and
+// c = fl(M*sc) + log2(S) (float-float), where M is the row max and
 // S = sum_v 2^(z_v*sc - fl(M*sc)); log2 p(v) = z_v*sc - c.  Warp-cooperative:
 // every lane returns the same value.  Returns false if the row has no finite
 // mass (all -inf, or a NaN / +inf logit made S non-finite) or if a partial
 // never arrived (*timed_out).
 // ---------------------------------------------------------------------------
 
-// log2 of a positive double: exact exponent, single-precision log2 of the
-// mantissa in [0.5, 1) (absolute error below 1e-7).  Non-positive or
-// non-finite input gives a non-finite result.
-__device__ __forceinline__ double log2_pos(double S) {
-  if (!(S > 0.0) || !(S <= 1.79e308)) return log2f((float)S);
+// log2 of a positive float as an exact exponent plus the single-precision
+// log2 of the mantissa in [0.5, 1) (absolute error below 1e-7), summed in
+// float-float.  Non-positive or non-finite input gives a non-finite result.
+__device__ __forceinline__ FF log2_pos(float S) {
+  if (!(S > 0.0f) || !(S <= FLT_MAX)) return {log2f(S), 0.0f};
   int e;
-  const double mant = frexp(S, &e);
-  return (double)e + (double)log2f((float)mant);
+  const float mant = frexpf(S, &e);
+  return two_sum((float)e, log2f(mant));
 }
 
 // One chunk's sum rescaled to the row reference ms_ref = fl(M*sc):
-// s_c * 2^(fl(m_c*sc) - ms_ref), the difference taken exactly in double and
-// the power in single precision (the dominant chunk gets exactly 1).
-__device__ __forceinline__ double chunk_term(float m_c, uint32_t s_bits, float sc, float ms_ref) {
+// s_c * 2^(fl(m_c*sc) - ms_ref) (the dominant chunk gets exactly 1; the
+// difference is rounded once, which only touches terms far below the max).
+__device__ __forceinline__ float chunk_term(float m_c, uint32_t s_bits, float sc, float ms_ref) {
   const float s_c = __uint_as_float(s_bits);
-  if (s_c > 0.0f) {
-    const float d = (float)((double)__fmul_rn(m_c, sc) - (double)ms_ref);
-    return (double)s_c * (double)exp2f(d);
-  }
-  return s_c == 0.0f ? 0.0 : __longlong_as_double(0x7ff8000000000000ll);  // NaN stays NaN
+  if (s_c > 0.0f) return __fmul_rn(s_c, exp2f(__fsub_rn(__fmul_rn(m_c, sc), ms_ref)));
+  return s_c == 0.0f ? 0.0f : __int_as_float(0x7fc00000);  // NaN stays NaN
+}
+
+// c = ms + log2(S) in float-float; ok iff S is a finite positive number.
+__device__ __forceinline__ bool row_normaliser_from(float ms, float S, FF* c) {
+  *c = ff_add(log2_pos(S), FF{ms, 0.0f});
+  return S > 0.0f && S <= FLT_MAX;
 }
 
 __device__ __forceinline__ bool row_log2_normaliser(const Partial* parts, int nch, float sc,
-                                                    double* c_out, float* max_out,
+                                                    FF* c_out, float* max_out,
                                                     bool* timed_out) {
   const int lane = threadIdx.x & 31;
   bool late = false;
@@ -543,7 +625,7 @@ __device__ __forceinline__ bool row_log2_normaliser(const Partial* parts, int nc
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   const float msM = __fmul_rn(m, sc);
-  double S = 0.0;
+  FF S = {0.0f, 0.0f};
   for (int c = lane; c < nch; c += 32) {
     float mc;
     uint32_t aux;
@@ -551,14 +633,13 @@ __device__ __forceinline__ bool row_log2_normaliser(const Partial* parts, int nc
       late = true;
       continue;
     }
-    S += chunk_term(mc, aux, sc, msM);
+    S = ff_add_f(S, chunk_term(mc, aux, sc, msM));
   }
-  S = warp_sum_f64(S);
+  S = warp_sum_ff(S);
   late = __any_sync(0xffffffffu, late);
   *timed_out = late;
-  *c_out = (double)msM + log2_pos(S);
   *max_out = m;
-  return !late && S > 0.0 && S <= 1.79e308;
+  return row_normaliser_from(msM, ff_to_float(S), c_out) && !late;
 }
 
 // Both rows of a sampling position at once: parts[0, nch) are the target
@@ -568,7 +649,7 @@ __device__ __forceinline__ bool row_log2_normaliser(const Partial* parts, int nc
 constexpr int kMaxPartsPerLane = 8;
 
 __device__ __forceinline__ void pair_log2_normalisers(const Partial* parts, int nch, float sc,
-                                                      double* ct, double* cd, bool* ok_t,
+                                                      FF* ct, FF* cd, bool* ok_t,
                                                       bool* ok_d, bool* timed_out) {
   const int lane = threadIdx.x & 31;
   const int n2 = 2 * nch;
@@ -605,21 +686,19 @@ __device__ __forceinline__ void pair_log2_normalisers(const Partial* parts, int 
     md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, off));
   }
   const float msT = __fmul_rn(mt, sc), msD = __fmul_rn(md, sc);
-  double St = 0.0, Sd = 0.0;
+  FF St = {0.0f, 0.0f}, Sd = {0.0f, 0.0f};
 #pragma unroll
   for (int j = 0; j < kMaxPartsPerLane; ++j) {
     const int e = lane + 32 * j;
-    if (e < nch) St += chunk_term(m[j], a[j], sc, msT);
-    else if (e < n2) Sd += chunk_term(m[j], a[j], sc, msD);
+    if (e < nch) St = ff_add_f(St, chunk_term(m[j], a[j], sc, msT));
+    else if (e < n2) Sd = ff_add_f(Sd, chunk_term(m[j], a[j], sc, msD));
   }
-  St = warp_sum_f64(St);
-  Sd = warp_sum_f64(Sd);
+  St = warp_sum_ff(St);
+  Sd = warp_sum_ff(Sd);
   late = __any_sync(0xffffffffu, late);
   *timed_out = late;
-  *ct = (double)msT + log2_pos(St);
-  *cd = (double)msD + log2_pos(Sd);
-  *ok_t = !late && St > 0.0 && St <= 1.79e308;
-  *ok_d = !late && Sd > 0.0 && Sd <= 1.79e308;
+  *ok_t = row_normaliser_from(msT, ff_to_float(St), ct) && !late;
+  *ok_d = row_normaliser_from(msD, ff_to_float(Sd), cd) && !late;
 }
 
 // Max and lowest index of a greedy row from its chunk partials.

@@ -12,7 +12,7 @@
 // row(s) are split into P slices of 256-entry segments; slice CTA p streams
 // its slice once and writes one record per segment, then bumps the
 // request's counter.  The last slice CTA to finish forms the segment prefix
-// sums in double, picks the segment holding u_L * total, and re-reads that
+// sums in float-float, picks the segment holding u_L * total, and re-reads that
 // segment to place the token exactly.
 //
 // Records: a residual segment stores its mass sum max(0, p - q), with p and
@@ -46,13 +46,13 @@ constexpr int kJobNone = 0, kJobResidual = 1, kJobBonus = 2, kJobGreedyRowL = 3,
               kJobTargetOnly = 5;
 
 struct FinalShared {
-  double warp_d[kFinalWarps + 1];
+  FF warp_ff[kFinalWarps + 1];
   float warp_f[kFinalWarps];
   int warp_i[kFinalWarps];
-  double pos_ct[32], pos_cd[32];  // log2 normalisers of the request's positions (k <= 31)
+  float4 pos_c[32];               // float-float log2 normalisers (target, draft) per position (k <= 31)
   int32_t pos_arg[32];
   int32_t tok[32];                // draft tokens x_0 .. x_{k-1}
-  double cand_excl;
+  FF cand_excl;
   float REF;
   int job, n, cand, token, last;
 };
@@ -119,7 +119,7 @@ __device__ __forceinline__ float2 f32x2_sub(float2 a, float2 b) {
 // How the entries of one request's final row(s) are weighed.  Residual
 // entries: max(0, 2^(zt*sc - a) - 2^(zd*sc - c_d)); target-only entries:
 // 2^(zt*sc - a); a and c_d are row normalisers carried as hi + lo
-// single-precision pairs so that they keep double accuracy.
+// single-precision pairs (float-float) so that they keep their accuracy.
 struct MassSpec {
   float sc;
   float a_hi, a_lo;
@@ -196,23 +196,17 @@ __device__ __forceinline__ float warp_max_f32(float x) {
   return x;
 }
 
-// 2^(a - b) for single-precision a, b: the difference is taken exactly in
-// double and rounded once; relative error about 1e-7.
-__device__ __forceinline__ float exp2_diff(float a, float b) {
-  return exp2f((float)((double)a - (double)b));
-}
+// 2^(a - b) for a <= b: the difference rounded once (it is exact while a
+// and b are within a factor of two), so the relative error stays near 1e-7
+// wherever the power is not negligible.
+__device__ __forceinline__ float exp2_diff(float a, float b) { return exp2f(__fsub_rn(a, b)); }
 
 // CDF weight of a segment record: its mass, or for the bonus its sum
 // rescaled from its own reference to REF.
-__device__ __forceinline__ double seg_weight(float2 r, bool bonus, float sc, float REF) {
-  if (!bonus) return (double)r.x;
-  if (r.y == 0.0f) return 0.0;
-  return (double)r.y * (double)exp2_diff(__fmul_rn(r.x, sc), REF);
-}
-
-__device__ __forceinline__ void split_hi_lo(double c, float* hi, float* lo) {
-  *hi = (float)c;
-  *lo = (float)(c - (double)*hi);
+__device__ __forceinline__ float seg_weight(float2 r, bool bonus, float sc, float REF) {
+  if (!bonus) return r.x;
+  if (r.y == 0.0f) return 0.0f;
+  return __fmul_rn(r.y, exp2_diff(__fmul_rn(r.x, sc), REF));
 }
 
 // ---------------------------------------------------------------------------
@@ -325,32 +319,43 @@ __device__ ArgAcc slice_argmax(const TIn* row, int V, int s_lo, int s_hi, bool v
   return r;
 }
 
-// Block-wide exclusive scan of one double per thread; all threads get the total.
-__device__ __forceinline__ double block_exclusive_scan_f64(double x, FinalShared& sh,
-                                                           double* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  double incl = x;
+__device__ __forceinline__ FF ff_shfl_up(FF a, int off) {
+  return {__shfl_up_sync(0xffffffffu, a.hi, off), __shfl_up_sync(0xffffffffu, a.lo, off)};
+}
+
+// Inclusive warp scan in float-float (lane order).
+__device__ __forceinline__ FF warp_incl_scan_ff(FF x) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += y;
+    const FF y = ff_shfl_up(x, off);
+    if (lane >= off) x = ff_add(y, x);
   }
-  if (lane == 31) sh.warp_d[warp] = incl;
+  return x;
+}
+
+// Block-wide exclusive scan of one float-float per thread; all threads get
+// the total.
+__device__ __forceinline__ FF block_exclusive_scan_ff(FF x, FinalShared& sh, FF* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const FF incl = warp_incl_scan_ff(x);
+  if (lane == 31) sh.warp_ff[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const double w = lane < kFinalWarps ? sh.warp_d[lane] : 0.0;
-    double wi = w;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, wi, off);
-      if (lane >= off) wi += y;
-    }
-    if (lane < kFinalWarps) sh.warp_d[lane] = wi - w;
-    if (lane == kFinalWarps - 1) sh.warp_d[kFinalWarps] = wi;
+    const FF w = lane < kFinalWarps ? sh.warp_ff[lane] : FF{0.0f, 0.0f};
+    const FF wi = warp_incl_scan_ff(w);
+    FF wx = ff_shfl_up(wi, 1);
+    if (lane == 0) wx = FF{0.0f, 0.0f};
+    __syncwarp();
+    if (lane < kFinalWarps) sh.warp_ff[lane] = wx;
+    if (lane == kFinalWarps - 1) sh.warp_ff[kFinalWarps] = wi;
   }
   __syncthreads();
-  const double ex = (incl - x) + sh.warp_d[warp];
-  *total = sh.warp_d[kFinalWarps];
+  // Exclusive prefix within the warp, then the warp's offset.
+  FF ex = ff_shfl_up(incl, 1);
+  if (lane == 0) ex = FF{0.0f, 0.0f};
+  ex = ff_add(sh.warp_ff[warp], ex);
+  *total = sh.warp_ff[kFinalWarps];
   __syncthreads();
   return ex;
 }
@@ -361,7 +366,7 @@ __device__ __forceinline__ double block_exclusive_scan_f64(double x, FinalShared
 // number.  rec_sm: nseg float2 of shared memory.
 template <typename TIn>
 __device__ int cdf_pick(const TIn* rt, const TIn* rd, int V, const MassSpec& ms, bool bonus,
-                        double u, const float2* rec, int nseg, bool vec_ok, FinalShared& sh,
+                        float u, const float2* rec, int nseg, bool vec_ok, FinalShared& sh,
                         float2* rec_sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float refm = -FLT_MAX;
@@ -381,28 +386,28 @@ __device__ int cdf_pick(const TIn* rt, const TIn* rd, int V, const MassSpec& ms,
 #pragma unroll
     for (int w = 0; w < kFinalWarps; ++w) REF = fmaxf(REF, sh.warp_f[w]);
   }
-  // Exclusive prefix of the weights, in double; thread t owns [sa, sb).
+  // Exclusive prefix of the weights, in float-float; thread t owns [sa, sb).
   const int per = (nseg + kFinalThreads - 1) / kFinalThreads;
   const int sa = min(nseg, (int)threadIdx.x * per), sb = min(nseg, sa + per);
-  double loc = 0.0;
-  for (int s = sa; s < sb; ++s) loc += seg_weight(rec_sm[s], bonus, ms.sc, REF);
-  double total;
-  double run = block_exclusive_scan_f64(loc, sh, &total);
-  if (!(total > 0.0 && total <= 1.79e308)) return -1;  // uniform across the block
-  const double target = u * total;
+  FF loc = {0.0f, 0.0f};
+  for (int s = sa; s < sb; ++s) loc = ff_add_f(loc, seg_weight(rec_sm[s], bonus, ms.sc, REF));
+  FF total;
+  FF run = block_exclusive_scan_ff(loc, sh, &total);
+  if (!(total.hi > 0.0f && total.hi <= FLT_MAX)) return -1;  // uniform across the block
+  const FF target = ff_mul_f(total, u);
 
   // The last segment with positive weight that starts at or before target.
   if (threadIdx.x == 0) sh.cand = -1;
   __syncthreads();
   int cand = -1;
-  double cand_excl = 0.0;
+  FF cand_excl = {0.0f, 0.0f};
   for (int s = sa; s < sb; ++s) {
-    const double w = seg_weight(rec_sm[s], bonus, ms.sc, REF);
-    if (w > 0.0 && run <= target) {
+    const float w = seg_weight(rec_sm[s], bonus, ms.sc, REF);
+    if (w > 0.0f && ff_le(run, target)) {
       cand = s;
       cand_excl = run;
     }
-    run += w;
+    run = ff_add_f(run, w);
   }
   if (cand >= 0) atomicMax(&sh.cand, cand);
   __syncthreads();
@@ -418,35 +423,28 @@ __device__ int cdf_pick(const TIn* rt, const TIn* rd, int V, const MassSpec& ms,
     seg_load(t, rt, j * kSegElems + lane * 8, V, vec_ok);
     if (ms.has_q && !bonus) seg_load(d, rd, j * kSegElems + lane * 8, V, vec_ok);
     float r[8];
-    double scale = 1.0;
+    float scale = 1.0f;
     if (bonus) {
       const float msr = __fmul_rn(rec_sm[j].x, ms.sc);
       bonus_masses(t, ms.sc, msr, r);
-      scale = (double)exp2_diff(msr, REF);
+      scale = exp2_diff(msr, REF);
     } else {
       entry_masses(t, d, ms, r);
     }
-    float c[8];
-    float run_f = 0.0f;
+    // Cumulative weight within the segment, in float-float: lane sums, then
+    // an exclusive scan over the lanes, then entry by entry.
+    FF lsum = {0.0f, 0.0f};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      run_f = __fadd_rn(run_f, r[e]);
-      c[e] = run_f;
-    }
-    float incl = run_f;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl = __fadd_rn(incl, y);
-    }
-    float lex = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) lex = 0.0f;
-    const double tprime = target - sh.cand_excl;
+    for (int e = 0; e < 8; ++e) lsum = ff_add_f(lsum, r[e]);
+    const FF lincl = warp_incl_scan_ff(lsum);
+    FF cum = ff_shfl_up(lincl, 1);
+    if (lane == 0) cum = FF{0.0f, 0.0f};
+    const FF tseg = ff_sub(target, sh.cand_excl);
     int first_e = 8, last_pos = -1;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const float cum = __fadd_rn(lex, c[e]);
-      if (first_e == 8 && r[e] > 0.0f && (double)cum * scale > tprime) first_e = e;
+      cum = ff_add_f(cum, r[e]);
+      if (first_e == 8 && r[e] > 0.0f && !ff_le(ff_mul_f(cum, scale), tseg)) first_e = e;
       if (r[e] > 0.0f) last_pos = e;
     }
     const unsigned hit = __ballot_sync(0xffffffffu, first_e < 8);
@@ -494,14 +492,13 @@ __global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) 
   // (lane t for position t); then n: the first rejected position, or L.
   if (threadIdx.x < 32) {
     const int t = threadIdx.x;
-    const double* pos_c = reinterpret_cast<const double*>(p.ws + p.lay.pos_c);
+    const float4* pos_c = reinterpret_cast<const float4*>(p.ws + p.lay.pos_c);
     const int32_t* pos_arg = reinterpret_cast<const int32_t*>(p.ws + p.lay.pos_arg);
-    double ct = 0.0, cd = 0.0;
+    float4 c4 = make_float4(0.f, 0.f, 0.f, 0.f);
     int g = -1, x = -1;
     if (t < p.k) {
       const size_t bi = (size_t)b * p.k + t;
-      ct = __ldcg(&pos_c[bi * 2]);
-      cd = __ldcg(&pos_c[bi * 2 + 1]);
+      c4 = __ldcg(&pos_c[bi]);
       g = __ldcg(&pos_arg[bi]);
       x = __ldg(&p.tokens[bi]);
     }
@@ -513,8 +510,7 @@ __global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) 
       acc = __ldcg(reinterpret_cast<const uint32_t*>(p.ws + p.lay.acc_bits) + b);
       bad = __ldcg(reinterpret_cast<const uint32_t*>(p.ws + p.lay.bad_bits) + b);
     }
-    sh.pos_ct[t] = ct;
-    sh.pos_cd[t] = cd;
+    sh.pos_c[t] = c4;
     sh.pos_arg[t] = g;
     sh.tok[t] = x;
     __syncwarp();
@@ -584,8 +580,11 @@ __global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) 
   ms.sc = job == kJobGreedyRowL ? 0.0f : softmax_scale(T);
   const bool bonus = (job == kJobBonus);
   if (job == kJobResidual) {
-    split_hi_lo(sh.pos_ct[n], &ms.a_hi, &ms.a_lo);
-    split_hi_lo(sh.pos_cd[n], &ms.cd_hi, &ms.cd_lo);
+    const float4 c4 = sh.pos_c[n];
+    ms.a_hi = c4.x;
+    ms.a_lo = c4.y;
+    ms.cd_hi = c4.z;
+    ms.cd_lo = c4.w;
     ms.has_q = true;
   }
   if (job == kJobGreedyRowL) {
@@ -625,7 +624,7 @@ __global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) 
     token = sh.token;
     bad = (token == INT32_MAX);
   } else {
-    const double u = (double)__ldg(&p.uniforms[(size_t)b * (p.k + 1) + L]);
+    const float u = __ldg(&p.uniforms[(size_t)b * (p.k + 1) + L]);
     token = cdf_pick(trow, drow, p.V, ms, bonus, u, rec, nseg, vec_ok, sh, rec_sm);
     if (token < 0 && job == kJobResidual) {
       // Residual mass zero (p_n == q_n up to rounding): draw from p_n.

@@ -108,6 +108,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   fill_u32(reinterpret_cast<uint32_t*>(p.ws + p.lay.done), (size_t)p.B * p.k, 0u);
   fill_u64(reinterpret_cast<unsigned long long*>(p.ws + p.lay.partials),
            (size_t)p.B * p.k * 2 * p.C, kPartialEmpty);
+  // Partials of a made-up position that the sweep's bookkeeping warps decide
+  // once, without effect, to bring the decision code into their instruction
+  // caches: m = 0, s = 1 (or index 0).
+  fill_u64(reinterpret_cast<unsigned long long*>(p.ws + p.lay.warm), 2 * (size_t)p.C,
+           ((unsigned long long)__float_as_uint(1.0f) << 32) | __float_as_uint(0.0f));
   __syncthreads();
 
   // Pass 1, item j = b*(k+1) + i: the request's scalars (at i = 0: 1 <= L <= k

@@ -77,13 +77,13 @@ __global__ void stats_finalize_kernel(const unsigned char* ws, WsLayout lay, int
     }
   } else {
     const float sc = softmax_scale(T);
-    double c;
+    FF c;
     float m;
     bool late;
     const bool ok = row_log2_normaliser(parts, nch, sc, &c, &m, &late);
     if (lane == 0) {
       row_max[r] = m;
-      row_lse[r] = ok ? (float)(c * kLn2) : __int_as_float(0x7fc00000);
+      row_lse[r] = ok ? ff_to_float(ff_mul_f(c, kLn2f)) : __int_as_float(0x7fc00000);
       row_arg[r] = -1;
     }
   }

@@ -20,8 +20,8 @@
 //
 // Verification mode: the CTA that completes the last chunk of (request b,
 // position i) combines the partials, gathers p(x_i) and q(x_i), and applies
-// the accept test u_i < min(1, p(x_i)/q(x_i)) (or argmax == x_i at T == 0) in
-// double precision.  A rejection is published in first_reject[b]; the
+// the accept test u_i < min(1, p(x_i)/q(x_i)) (or argmax == x_i at T == 0)
+// with float-float log-probabilities.  A rejection is published in first_reject[b]; the
 // producer skips chunks of positions behind a known rejection, since only
 // tokens before the first rejection are kept (AdaFlash Section 2.1).
 #pragma once
@@ -67,8 +67,12 @@ struct UnitMeta {
 
 constexpr int kNC = kSweepConsumerWarps;
 constexpr int kNCT = kNC * 32;
-constexpr int kProducerWarp = kNC;
-constexpr int kBookWarp = kNC + 1;
+// The bookkeeping and producer warps come first: a warp scheduler that
+// favours older warps then does not starve them behind the consumers, which
+// are ready to issue most of the time.
+constexpr int kBookWarp = 0;
+constexpr int kProducerWarp = 1;
+constexpr int kFirstConsumerWarp = 2;
 constexpr int kVecPerThread = kStageBytes / 16 / kNCT;  // 16-byte vectors per consumer thread
 static_assert(kSweepThreads == (kNC + 2) * 32, "kNC consumer warps + producer + bookkeeping");
 static_assert(kStageBytes % (16 * kNCT) == 0, "a stage splits evenly over the consumer threads");
@@ -290,6 +294,147 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
 }
 
 // ---------------------------------------------------------------------------
+// Producer for units of two stages or more (lane 0 of the producer warp).
+// It claims one unit at a time, kLookStages stages before the current unit
+// runs out: the claim goes out at that stage, the unit's descriptor load one
+// stage later, so both round trips overlap copies already in flight and the
+// units are streamed in the order they were claimed -- the position-major
+// order of the work list, which makes a rejection known before the rows
+// behind it are read.  Whether a unit is behind a known rejection is looked
+// up before each of its stages (the load goes out before the ring wait).
+// ---------------------------------------------------------------------------
+constexpr int kLookStages = 3;
+
+template <typename TIn, bool kVerify>
+__device__ void sweep_producer_big(const SweepParams& p, SweepSmem& sm, WsHeader* h) {
+  using Tr = ElemTraits<TIn>;
+  if ((threadIdx.x & 31) != 0) return;
+  const int2* rowdesc = reinterpret_cast<const int2*>(p.ws + p.lay.rowdesc);
+  const int32_t* first_reject = reinterpret_cast<const int32_t*>(p.ws + p.lay.first_reject);
+  const int units_total = __ldcg(&h->units_total);
+  volatile int* abort_flag = &sm.abort_flag;
+  const bool recheck = kVerify && p.early_exit;
+  int it = 0;  // stages issued
+  bool ok = true;
+  unsigned long long my_chunks = 0, my_bytes = 0;
+
+  auto acquire = [&](int& s) -> bool {
+    s = it % kStages;
+    const int round = it / kStages;
+    if (round > 0 && !mbar_wait_bounded(&sm.empty[s], (round - 1) & 1, abort_flag)) {
+      sweep_abort(h, sm);
+      return false;
+    }
+    return true;
+  };
+  auto describe = [&](int u) {
+    return u < units_total ? __ldcg(&rowdesc[u / p.nch]) : make_int2(-1, 0);
+  };
+
+  int nxt = atomicAdd(&h->work_next, 1);
+  int2 nrd = describe(nxt);
+  while (nxt < units_total) {
+    const int uu = nxt;
+    const int2 rd = nrd;
+    nxt = -1;
+    bool described = false;
+    const int slot = rd.x;
+    const float sc = __int_as_float(rd.y);
+    const int chunk = uu - (uu / p.nch) * p.nch;
+    const TIn* rowp;
+    int ub = 0, ui = 0;
+    if (kVerify) {
+      const int bi = slot >> 1;
+      ub = bi / p.k;
+      ui = bi - ub * p.k;
+      rowp = (slot & 1) ? static_cast<const TIn*>(p.draft) + ((size_t)ub * p.k + ui) * (size_t)p.V
+                        : static_cast<const TIn*>(p.target) + ((size_t)ub * (p.k + 1) + ui) * (size_t)p.V;
+    } else {
+      rowp = static_cast<const TIn*>(p.target) + (size_t)slot * (size_t)p.V;
+    }
+    const bool greedy = (sc == 0.0f);
+    // Element range of the chunk and its 16-byte aligned core.
+    const int e0 = chunk * p.chunk_elems;
+    const int e1 = min(p.V, e0 + p.chunk_elems);
+    const uintptr_t addr0 = reinterpret_cast<uintptr_t>(rowp + e0);
+    int a0 = e0 + (int)(((16u - (unsigned)(addr0 & 15u)) & 15u) / Tr::kSize);
+    if (a0 > e1) a0 = e1;
+    const int core_bytes = (((e1 - a0) * Tr::kSize) & ~15);
+    const int a1 = a0 + core_bytes / Tr::kSize;
+    const int nstage = core_bytes > 0 ? (core_bytes + kStageBytes - 1) / kStageBytes : 1;
+    const char* src0 = reinterpret_cast<const char*>(rowp + a0);
+    const int look = nstage > kLookStages ? nstage - kLookStages : 0;
+    for (int j = 0; j < nstage; ++j) {
+      const int frj = recheck ? *(volatile const int32_t*)&first_reject[ub] : INT32_MAX;
+      if (j == look) nxt = atomicAdd(&h->work_next, 1);
+      if (j == look + 1) {
+        nrd = describe(nxt);
+        described = true;
+      }
+      int s;
+      if (!acquire(s)) {
+        ok = false;
+        break;
+      }
+      const bool drop = frj < ui;
+      if (drop && j == 0) break;  // nothing issued yet: skip the unit
+      const int off = j * kStageBytes;
+      const int nb = (core_bytes > 0 && !drop) ? min(kStageBytes, core_bytes - off) : 0;
+      StageInfo& I = sm.info[s];
+      I.row = rowp;
+      I.part = slot * p.nch + chunk;
+      I.flags = (j == 0 ? kFlagFirst : 0) | (j == nstage - 1 || drop ? kFlagLast : 0) |
+                (drop ? kFlagDiscard : 0) | (greedy ? kFlagGreedy : 0);
+      I.elem0 = a0 + off / Tr::kSize;
+      I.nbytes = nb;
+      I.head0 = e0;
+      I.headn = a0 - e0;
+      I.tail0 = a1;
+      I.tailn = drop ? 0 : e1 - a1;
+      I.sc = sc;
+      I.slot = slot;
+      if (nb > 0) {
+        mbar_arrive_expect_tx(&sm.full[s], (uint32_t)nb);
+        bulk_g2s(sm.stage[s], src0 + off, (uint32_t)nb, &sm.full[s]);
+      } else {
+        mbar_arrive(&sm.full[s]);
+      }
+      ++it;
+      if (j == 0) {
+        my_chunks += 1;
+        my_bytes += (unsigned long long)(a0 - e0) * Tr::kSize;
+      }
+      my_bytes += (unsigned long long)nb;
+      if (j == nstage - 1) my_bytes += (unsigned long long)(e1 - a1) * Tr::kSize;
+      if (drop) break;
+    }
+    if (!ok) break;
+    // A unit that ended before its look-ahead point claims its successor now.
+    if (nxt < 0) nxt = atomicAdd(&h->work_next, 1);
+    if (!described) nrd = describe(nxt);
+  }
+
+  atomicAdd(&h->chunks_swept, my_chunks);
+  atomicAdd(&h->sweep_bytes, my_bytes);
+  if (ok) {
+    int s;
+    if (acquire(s)) {
+      sm.info[s].flags = kFlagEnd;
+      mbar_arrive(&sm.full[s]);
+      ++it;
+      return;
+    }
+  }
+  // Aborted: wait (bounded) for the copies still in flight into this CTA's
+  // shared memory before the CTA may exit.
+  for (int back = 1; back <= kStages && back <= it; ++back) {
+    const int jt = it - back;
+    int dummy = 0;
+    mbar_wait_bounded(&sm.full[jt % kStages], (jt / kStages) & 1, (volatile int*)&dummy);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // One consumer thread's share of a stage: kVecPerThread 16-byte vectors held
 // in registers.  Vectors past the stage's end are -inf in every element, so
 // they change neither a max nor a sum of exponentials.
@@ -401,16 +546,22 @@ __device__ __forceinline__ void arg_stage(ArgAcc& a, const uint4 (&v)[kVecPerThr
 // Decision for (b, i) once all of its chunks are in (warp-cooperative).
 // ---------------------------------------------------------------------------
 // x and u (token x_i and uniform u_i) were loaded one unit earlier, when
-// the chunk count was taken.
+// the chunk count was taken.  With dry set, the partials come from the
+// workspace's made-up position and nothing is recorded: the call only brings
+// this code into the instruction cache while memory is still quiet (its first
+// real use comes when the sweep has HBM saturated, where every instruction
+// fetch would wait in the queues).  Kept out of line so that both calls run
+// the same code.
 template <typename TIn>
-__device__ void decide_position(const SweepParams& p, int bi, bool greedy, float sc, int x,
-                                float u_i) {
+__device__ __noinline__ void decide_position(const SweepParams& p, int bi, bool greedy, float sc,
+                                             int x, float u_i, bool dry) {
   const int lane = threadIdx.x & 31;
   const int b = bi / p.k;
   const int i = bi - b * p.k;
   const Partial* parts = reinterpret_cast<const Partial*>(p.ws + p.lay.partials);
-  const Partial* pt = parts + (size_t)(bi << 1) * p.nch;
-  double* pos_c = reinterpret_cast<double*>(p.ws + p.lay.pos_c);
+  const Partial* pt =
+      dry ? reinterpret_cast<const Partial*>(p.ws + p.lay.warm) : parts + (size_t)(bi << 1) * p.nch;
+  float4* pos_c = reinterpret_cast<float4*>(p.ws + p.lay.pos_c);
   int32_t* pos_arg = reinterpret_cast<int32_t*>(p.ws + p.lay.pos_arg);
   uint32_t* bad_bits = reinterpret_cast<uint32_t*>(p.ws + p.lay.bad_bits);
   uint32_t* acc_bits = reinterpret_cast<uint32_t*>(p.ws + p.lay.acc_bits);
@@ -424,7 +575,7 @@ __device__ void decide_position(const SweepParams& p, int bi, bool greedy, float
     row_argmax_from_parts(pt, p.nch, &v, &g, &late);
     row_ok = (g != INT32_MAX);
     accept = (g == x);
-    if (lane == 0) __stcg(&pos_arg[bi], g);
+    if (lane == 0 && !dry) __stcg(&pos_arg[bi], g);
   } else {
     // The gathers of z_t[x] and z_d[x] go out first and overlap the partial
     // loads.  Target chunks then draft chunks: the two slots are adjacent.
@@ -432,30 +583,32 @@ __device__ void decide_position(const SweepParams& p, int bi, bool greedy, float
         static_cast<const TIn*>(p.target) + ((size_t)b * (p.k + 1) + i) * (size_t)p.V, x);
     const float zd = ElemTraits<TIn>::load(
         static_cast<const TIn*>(p.draft) + ((size_t)b * p.k + i) * (size_t)p.V, x);
-    double ct, cd;
+    FF ct, cd;
     bool okt, okd;
     pair_log2_normalisers(pt, p.nch, sc, &ct, &cd, &okt, &okd, &late);
     row_ok = okt && okd;
-    // log2 p(x) and log2 q(x) in double: z*sc is exact in double.
-    const double lp = (double)zt * (double)sc - ct;
-    const double lq = (double)zd * (double)sc - cd;
-    const double u = (double)u_i;
     // A token the target gives probability zero is never accepted; a token
     // the drafter gives probability zero (and the target not) always is.
-    // 2^d in single precision: near any threshold u the absolute error is
-    // below 1e-7.
-    const double d = lp - lq;
-    const double ratio = (lp == -INFINITY) ? 0.0 : (d >= 0.0 ? 1.0 : (double)exp2f((float)d));
-    accept = u < fmin(1.0, ratio);
-    if (lane == 0) {
-      __stcg(&pos_c[(size_t)bi * 2], ct);
-      __stcg(&pos_c[(size_t)bi * 2 + 1], cd);
+    // Otherwise d = log2 p(x) - log2 q(x) = (zt*sc - ct) - (zd*sc - cd) in
+    // float-float (the products exact), and the ratio 2^d in single
+    // precision: near any threshold u its absolute error is below 1e-7.
+    float ratio;
+    if (zt == -INFINITY) {
+      ratio = 0.0f;
+    } else if (zd == -INFINITY) {
+      ratio = 1.0f;
+    } else {
+      const FF d = ff_sub(ff_sub(two_prod(zt, sc), ct), ff_sub(two_prod(zd, sc), cd));
+      const float df = ff_to_float(d);
+      ratio = df >= 0.0f ? 1.0f : exp2f(df);
     }
+    accept = u_i < ratio;
+    if (lane == 0 && !dry) __stcg(&pos_c[bi], make_float4(ct.hi, ct.lo, cd.hi, cd.lo));
   }
   // A row without finite mass makes the request invalid if the round reaches
   // it; it also ends the round there so no later row is read for nothing.
   if (!row_ok) accept = false;
-  if (lane == 0) {
+  if (lane == 0 && !dry) {
     if (late) record_status(reinterpret_cast<WsHeader*>(p.ws + p.lay.header), SPEC_ERR_TIMEOUT);
     if (!row_ok) atomicOr(&bad_bits[b], 1u << i);
     if (accept) atomicOr(&acc_bits[b], 1u << i);
@@ -465,14 +618,14 @@ __device__ void decide_position(const SweepParams& p, int bi, bool greedy, float
 }
 
 // ---------------------------------------------------------------------------
-// Consumers: warps 0..kNC-1.
+// Consumers: warps kFirstConsumerWarp .. kFirstConsumerWarp + kNC - 1.
 // ---------------------------------------------------------------------------
 
 // Post this warp's accumulator for the unit (or the end marker) in reduction
 // slot `units % kRedDepth`, once the bookkeeping warp has released it.
 __device__ __forceinline__ bool post_unit(SweepSmem& sm, WsHeader* h, int units, const float4& acc,
                                           const UnitMeta& meta) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = (threadIdx.x >> 5) - kFirstConsumerWarp, lane = threadIdx.x & 31;
   const int rs = units % kRedDepth;
   if (units >= kRedDepth &&
       !mbar_wait_bounded(&sm.red_free[rs], ((units / kRedDepth) - 1) & 1, &sm.abort_flag)) {
@@ -492,9 +645,9 @@ template <typename TIn>
 __device__ void sweep_consumers(SweepSmem& sm, WsHeader* h) {
   using Tr = ElemTraits<TIn>;
   constexpr int EPV = Tr::kPerVec;
-  const int warp = threadIdx.x >> 5;
+  const int warp = (threadIdx.x >> 5) - kFirstConsumerWarp;  // consumer warp 0 .. kNC-1
   const int lane = threadIdx.x & 31;
-  const int ctid = threadIdx.x;
+  const int ctid = threadIdx.x - kFirstConsumerWarp * 32;
   volatile int* abort_flag = &sm.abort_flag;
 
   SoftAcc sa;
@@ -580,11 +733,17 @@ __device__ void sweep_bookkeeper(const SweepParams& p, SweepSmem& sm, WsHeader* 
   int pend_bi = -1, pend_old = 0, pend_need = 0, pend_x = 0;
   bool pend_greedy = false;
   float pend_sc = 0.0f, pend_u = 0.0f;
+  if (kVerify) {
+    // Run both decision paths once, without effect, while the first units
+    // are still streaming in (see decide_position).
+    decide_position<TIn>(p, 0, false, 1.0f, 0, 0.5f, true);
+    decide_position<TIn>(p, 0, true, 0.0f, 0, 0.5f, true);
+  }
   auto resolve_pending = [&]() {
     if (!kVerify || pend_bi < 0) return;
     const int old = __shfl_sync(0xffffffffu, pend_old, 0);
     if (old == pend_need - 1)
-      decide_position<TIn>(p, pend_bi, pend_greedy, pend_sc, pend_x, pend_u);
+      decide_position<TIn>(p, pend_bi, pend_greedy, pend_sc, pend_x, pend_u, false);
     pend_bi = -1;
   };
   for (int u = 0;; ++u) {
@@ -675,13 +834,18 @@ __global__ void __launch_bounds__(kSweepThreads, kSweepMinBlocks) sweep_kernel(S
   // Everything below reads what the plan kernel wrote.
   pdl_wait();
   WsHeader* h = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
-  // Warps 0..kNC-1 consume, warp kNC produces, warp kNC+1 keeps the books;
-  // the mbarrier counts and reduction slots are sized for exactly this split.
+  // Warp 0 keeps the books, warp 1 produces, warps 2..kNC+1 consume; the
+  // mbarrier counts and reduction slots are sized for exactly this split.
   const int warp = threadIdx.x >> 5;
-  if (warp < kNC) {
+  if (warp >= kFirstConsumerWarp) {
     sweep_consumers<TIn>(sm, h);
   } else if (warp == kProducerWarp) {
-    sweep_producer<TIn, kVerify>(p, sm, h);
+    // Units of two stages or more get the one-unit look-ahead producer;
+    // smaller ones the batched one, which keeps enough bytes in flight.
+    if (p.chunk_elems * (int)sizeof(TIn) >= 2 * kStageBytes)
+      sweep_producer_big<TIn, kVerify>(p, sm, h);
+    else
+      sweep_producer<TIn, kVerify>(p, sm, h);
   } else if (warp == kBookWarp) {
     sweep_bookkeeper<TIn, kVerify>(p, sm, h);
   }
