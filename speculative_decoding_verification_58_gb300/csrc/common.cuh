@@ -433,16 +433,27 @@ __device__ __forceinline__ FF ff_shfl_xor(FF a, int off) {
   return {__shfl_xor_sync(0xffffffffu, a.hi, off), __shfl_xor_sync(0xffffffffu, a.lo, off)};
 }
 
-// Warp sum in a fixed butterfly order (every lane gets the same bits).
-__device__ __forceinline__ FF warp_sum_ff(FF x) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
+// Sum over the aligned groups of 2^levels lanes, in a fixed butterfly order
+// (every lane of a group gets the same bits).
+__device__ __forceinline__ FF group_sum_ff(FF x, int levels) {
+  for (int l = 0; l < levels; ++l) {
+    const int off = 1 << l;
     const FF y = ff_shfl_xor(x, off);
     // Combine in lane order so that both partners compute the same value.
     x = (threadIdx.x & off) ? ff_add(y, x) : ff_add(x, y);
   }
   return x;
 }
+
+__device__ __forceinline__ float group_max(float x, int levels) {
+  for (int l = 0; l < levels; ++l) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1 << l));
+  return x;
+}
+
+__device__ __forceinline__ FF warp_sum_ff(FF x) { return group_sum_ff(x, 5); }
+
+// Shuffle levels that cover lanes 0 .. n-1 (n <= 32).
+__device__ __forceinline__ int levels_for(int n) { return n <= 1 ? 0 : 32 - __clz(n - 1); }
 
 // ---------------------------------------------------------------------------
 // Inline PTX: mbarrier, bulk async copy, programmatic dependent launch.
@@ -659,6 +670,35 @@ __device__ __forceinline__ void pair_log2_normalisers(const Partial* parts, int 
     *ok_t = row_log2_normaliser(parts, nch, sc, ct, &mt, &lt);
     *ok_d = row_log2_normaliser(parts + nch, nch, sc, cd, &md, &ld);
     *timed_out = lt || ld;
+    return;
+  }
+  if (n2 <= 32) {
+    // One partial per lane (target chunks on lanes 0 .. nch-1, draft chunks
+    // after them): reductions over just the lanes that hold data.
+    const int lv = levels_for(n2);
+    float mc = -FLT_MAX;
+    uint32_t ac = 0u;
+    bool late1 = false;
+    if (lane < n2 && !load_partial(&parts[lane], &mc, &ac)) {
+      late1 = true;
+      mc = -FLT_MAX;
+      ac = 0u;
+    }
+    const bool is_t = lane < nch, is_d = lane >= nch && lane < n2;
+    // Lanes 0 .. 2^lv - 1 form the group that holds every partial; lane 0's
+    // results go to the whole warp.
+    const float mt = __shfl_sync(0xffffffffu, group_max(is_t ? mc : -FLT_MAX, lv), 0);
+    const float md = __shfl_sync(0xffffffffu, group_max(is_d ? mc : -FLT_MAX, lv), 0);
+    const float msT = __fmul_rn(mt, sc), msD = __fmul_rn(md, sc);
+    const float term = (is_t || is_d) ? chunk_term(mc, ac, sc, is_t ? msT : msD) : 0.0f;
+    FF St = group_sum_ff(FF{is_t ? term : 0.0f, 0.0f}, lv);
+    FF Sd = group_sum_ff(FF{is_d ? term : 0.0f, 0.0f}, lv);
+    St = FF{__shfl_sync(0xffffffffu, St.hi, 0), __shfl_sync(0xffffffffu, St.lo, 0)};
+    Sd = FF{__shfl_sync(0xffffffffu, Sd.hi, 0), __shfl_sync(0xffffffffu, Sd.lo, 0)};
+    const bool late = __any_sync(0xffffffffu, late1);
+    *timed_out = late;
+    *ok_t = row_normaliser_from(msT, ff_to_float(St), ct) && !late;
+    *ok_d = row_normaliser_from(msD, ff_to_float(Sd), cd) && !late;
     return;
   }
   float m[kMaxPartsPerLane];
