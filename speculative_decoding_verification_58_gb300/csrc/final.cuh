@@ -478,6 +478,9 @@ __global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) 
   float2* rec_sm = reinterpret_cast<float2*>(fsm_raw);
 
   pdl_wait();
+  // The next call's plan kernel may launch now; it waits for this grid to
+  // finish before it touches the workspace.
+  pdl_launch_dependents();
   const int part = blockIdx.x, b = blockIdx.y, P = gridDim.x;
   WsHeader* h = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
   float2* rec = reinterpret_cast<float2*>(p.ws + p.lay.seg_mass) + (size_t)b * nseg;

@@ -70,6 +70,9 @@ __device__ __forceinline__ void fill_u32(uint32_t* dst, size_t n, uint32_t v) {
 }
 
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
+  // This kernel may itself be launched early, behind the previous kernel on
+  // the stream: nothing is read or written before that kernel has finished.
+  pdl_wait();
   // Dependents may launch now; they wait for this grid's completion before
   // reading anything it writes.
   pdl_launch_dependents();

@@ -225,7 +225,7 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
   // With timing events between the kernels there is nothing to overlap.
   const bool pdl = (ev == nullptr);
   if (record(ev, 0, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (launch(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, false, pp) != cudaSuccess)
+  if (launch(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, pdl, pp) != cudaSuccess)
     return SPEC_ERR_CUDA;
 
   SweepParams sp;
