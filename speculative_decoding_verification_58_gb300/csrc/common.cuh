@@ -57,7 +57,9 @@ struct WsHeader {
   int32_t pad0;
   unsigned long long sweep_bytes;
   unsigned long long final_bytes;
-  int32_t pad[46];
+  int32_t sweep_exited;     // sweep CTAs that have finished
+  int32_t final_ctas_done;  // final-pass CTAs that have finished
+  int32_t pad[44];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte block");
 
@@ -73,7 +75,7 @@ struct __align__(8) Partial {
 constexpr unsigned long long kPartialEmpty = 0x7FC0DEAD7FC0DEADull;
 
 struct WsLayout {
-  size_t header, rowdesc, flags, first_reject, acc_bits, dec_bits, bad_bits, done, pos_c, pos_arg,
+  size_t header, rowdesc, flags, first_reject, state, bad_bits, done, pos_c, pos_arg,
       partials, seg_mass, slice_ref, slice_arg, final_done, warm, total;
 };
 
@@ -106,8 +108,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int k, int C, int V) {
   l.rowdesc = o;      o = align256(o + slots * sizeof(int2));
   l.flags = o;        o = align256(o + (size_t)B * sizeof(int32_t));
   l.first_reject = o; o = align256(o + (size_t)B * sizeof(int32_t));
-  l.acc_bits = o;     o = align256(o + (size_t)B * sizeof(uint32_t));
-  l.dec_bits = o;     o = align256(o + (size_t)B * sizeof(uint32_t));
+  l.state = o;        o = align256(o + (size_t)B * sizeof(unsigned long long));
   l.bad_bits = o;     o = align256(o + (size_t)B * sizeof(uint32_t));
   l.done = o;         o = align256(o + (size_t)B * k * sizeof(int32_t));
   l.pos_c = o;        o = align256(o + (size_t)B * k * sizeof(float4));
@@ -541,6 +542,28 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Release: this thread's earlier writes are visible to whoever acquires the
+// value this atomic leaves (or a later one in the word's modification order).
+__device__ __forceinline__ void atom_or_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("{\n\t.reg .b64 t;\n\tatom.release.gpu.global.or.b64 t, [%0], %1;\n\t}" ::"l"(p),
+               "l"(v)
+               : "memory");
+}
+
+// A request's decision word: bit i of the low half = position i decided,
+// bit i of the high half = position i accepted.  One atomic sets both, so a
+// reader never sees one without the other.
+__device__ __forceinline__ unsigned long long decision_bits(int i, bool accept) {
+  const unsigned long long bit = 1ull << i;
+  return accept ? (bit | (bit << 32)) : bit;
 }
 
 __device__ __forceinline__ void record_status(WsHeader* h, int code) {

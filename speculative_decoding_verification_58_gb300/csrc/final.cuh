@@ -34,7 +34,8 @@ struct FinalParams {
   const float* uniforms;
   const float* temperature;
   int B, k, V;
-  int P;  // slice CTAs per request (gridDim.x)
+  int P;           // slice CTAs per request (gridDim.x)
+  int sweep_grid;  // CTAs of the sweep grid this pass follows
   int32_t* out_tokens;
   int32_t* num_accepted;
   unsigned char* ws;
@@ -470,17 +471,13 @@ __device__ __forceinline__ int slice_lo(int part, int nseg, int P) {
   return (int)(((long long)part * nseg) / P);
 }
 
+// One slice CTA's work.  The CTA may start while the sweep is still running
+// (it takes SMs the sweep has left): it first waits, bounded, until its
+// request's outcome is known -- every position up to the first rejection
+// (or all L) decided -- acquiring the deciders' writes with the mask.
 template <typename TIn>
-__global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) {
-  extern __shared__ __align__(16) unsigned char fsm_raw[];
-  __shared__ FinalShared sh;
+__device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh, float2* rec_sm) {
   const int nseg = segments_of(p.V);
-  float2* rec_sm = reinterpret_cast<float2*>(fsm_raw);
-
-  pdl_wait();
-  // The next call's plan kernel may launch now; it waits for this grid to
-  // finish before it touches the workspace.
-  pdl_launch_dependents();
   const int part = blockIdx.x, b = blockIdx.y, P = gridDim.x;
   WsHeader* h = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
   float2* rec = reinterpret_cast<float2*>(p.ws + p.lay.seg_mass) + (size_t)b * nseg;
@@ -490,11 +487,34 @@ __global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) 
   const int L = __ldg(&p.lengths[b]);
   const float T = __ldg(&p.temperature[b]);
 
-  // One round of independent loads: the request's flags and decision masks
-  // (lane 0) and every position's normalisers, argmax and draft token
-  // (lane t for position t); then n: the first rejected position, or L.
+  // Warp 0: wait for the outcome (flags and masks, every lane the same),
+  // then one round of loads of every position's normalisers, argmax and
+  // draft token (lane t for position t); n: the first rejected position, or L.
   if (threadIdx.x < 32) {
     const int t = threadIdx.x;
+    const uint32_t lmask = (L >= 32) ? 0xffffffffu : ((1u << L) - 1u);
+    int f = 0;
+    uint32_t dec = 0, acc = 0, bad = 0;
+    bool late = false;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+      f = __ldcg(reinterpret_cast<const int32_t*>(p.ws + p.lay.flags) + b);
+      const unsigned long long st =
+          ld_acquire_u64(reinterpret_cast<const unsigned long long*>(p.ws + p.lay.state) + b);
+      dec = (uint32_t)st;
+      acc = (uint32_t)(st >> 32);
+      bad = __ldcg(reinterpret_cast<const uint32_t*>(p.ws + p.lay.bad_bits) + b);
+      if (!(f & kReqValid)) break;
+      const uint32_t rej = dec & ~acc & lmask;
+      const int nn = rej ? (__ffs((int)rej) - 1) : L;
+      const uint32_t pre = (nn >= 32) ? 0xffffffffu : ((1u << nn) - 1u);
+      if ((dec & acc & pre) == pre) break;
+      if (global_ns() - t0 > kWaitLimitNs) {
+        late = true;
+        break;
+      }
+      __nanosleep(256);
+    }
     const float4* pos_c = reinterpret_cast<const float4*>(p.ws + p.lay.pos_c);
     const int32_t* pos_arg = reinterpret_cast<const int32_t*>(p.ws + p.lay.pos_arg);
     float4 c4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -505,13 +525,9 @@ __global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) 
       g = __ldcg(&pos_arg[bi]);
       x = __ldg(&p.tokens[bi]);
     }
-    int f = 0;
-    uint32_t dec = 0, acc = 0, bad = 0;
-    if (t == 0) {
-      f = __ldcg(reinterpret_cast<const int32_t*>(p.ws + p.lay.flags) + b);
-      dec = __ldcg(reinterpret_cast<const uint32_t*>(p.ws + p.lay.dec_bits) + b);
-      acc = __ldcg(reinterpret_cast<const uint32_t*>(p.ws + p.lay.acc_bits) + b);
-      bad = __ldcg(reinterpret_cast<const uint32_t*>(p.ws + p.lay.bad_bits) + b);
+    if (late) {
+      if (t == 0 && part == 0) record_status(h, SPEC_ERR_TIMEOUT);
+      f = 0;  // no outcome: the request reports -1
     }
     sh.pos_c[t] = c4;
     sh.pos_arg[t] = g;
@@ -520,7 +536,6 @@ __global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) 
     if (t == 0) {
       int job = kJobInvalid, n = -1, token = -1;
       if (f & kReqValid) {
-        const uint32_t lmask = (L >= 32) ? 0xffffffffu : ((1u << L) - 1u);
         const uint32_t rej = dec & ~acc & lmask;
         n = rej ? (__ffs((int)rej) - 1) : L;
         const uint32_t prefix = (n >= 32) ? 0xffffffffu : ((1u << n) - 1u);
@@ -652,6 +667,35 @@ __global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) 
     }
   }
   write_outputs(bad, token);
+}
+
+template <typename TIn>
+__global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) {
+  extern __shared__ __align__(16) unsigned char fsm_raw[];
+  __shared__ FinalShared sh;
+  // The next call's plan kernel may launch now; it waits for this grid to
+  // finish before it touches the workspace.
+  pdl_launch_dependents();
+  final_body<TIn>(p, sh, reinterpret_cast<float2*>(fsm_raw));
+  // The grid must not finish before the sweep grid has (the next call's plan
+  // waits only for this one): the last CTA out waits, bounded, for every
+  // sweep CTA to have counted itself out.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    WsHeader* h = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
+    __threadfence();
+    const int total = (int)(gridDim.x * gridDim.y);
+    if (atomicAdd(&h->final_ctas_done, 1) == total - 1) {
+      const unsigned long long t0 = global_ns();
+      while (*(volatile int32_t*)&h->sweep_exited < p.sweep_grid) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+          record_status(h, SPEC_ERR_TIMEOUT);
+          break;
+        }
+        __nanosleep(256);
+      }
+    }
+  }
 }
 
 }  // namespace specv

@@ -96,6 +96,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     h->residual_zero = 0;
     h->sweep_bytes = 0;
     h->final_bytes = 0;
+    h->sweep_exited = 0;
+    h->final_ctas_done = 0;
   }
   const int words = (p.B + 31) >> 5;
   for (int w = tid; w < words; w += kPlanThreads) bad_mask[w] = 0u;
@@ -104,8 +106,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   // stores: decision masks, chunk and final-pass counters to zero, every
   // partial slot to the empty marker (the deciding CTA waits for its slots
   // to leave it).
-  fill_u32(reinterpret_cast<uint32_t*>(p.ws + p.lay.acc_bits), p.B, 0u);
-  fill_u32(reinterpret_cast<uint32_t*>(p.ws + p.lay.dec_bits), p.B, 0u);
+  fill_u64(reinterpret_cast<unsigned long long*>(p.ws + p.lay.state), p.B, 0ull);
   fill_u32(reinterpret_cast<uint32_t*>(p.ws + p.lay.bad_bits), p.B, 0u);
   fill_u32(reinterpret_cast<uint32_t*>(p.ws + p.lay.final_done), p.B, 0u);
   fill_u32(reinterpret_cast<uint32_t*>(p.ws + p.lay.done), (size_t)p.B * p.k, 0u);

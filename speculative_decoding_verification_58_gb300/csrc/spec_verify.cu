@@ -264,6 +264,7 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
   fp.num_accepted = num_accepted;
   fp.ws = ws;
   fp.lay = lay;
+  fp.sweep_grid = (int)grid;
   const int nseg = segments_of(V);
   // Slices per request: one wave of four CTAs per SM over the batch, each
   // slice at least one segment.

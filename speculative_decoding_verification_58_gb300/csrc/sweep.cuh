@@ -564,8 +564,7 @@ __device__ __noinline__ void decide_position(const SweepParams& p, int bi, bool 
   float4* pos_c = reinterpret_cast<float4*>(p.ws + p.lay.pos_c);
   int32_t* pos_arg = reinterpret_cast<int32_t*>(p.ws + p.lay.pos_arg);
   uint32_t* bad_bits = reinterpret_cast<uint32_t*>(p.ws + p.lay.bad_bits);
-  uint32_t* acc_bits = reinterpret_cast<uint32_t*>(p.ws + p.lay.acc_bits);
-  uint32_t* dec_bits = reinterpret_cast<uint32_t*>(p.ws + p.lay.dec_bits);
+  unsigned long long* state = reinterpret_cast<unsigned long long*>(p.ws + p.lay.state);
   int32_t* first_reject = reinterpret_cast<int32_t*>(p.ws + p.lay.first_reject);
 
   bool accept, row_ok, late;
@@ -611,9 +610,13 @@ __device__ __noinline__ void decide_position(const SweepParams& p, int bi, bool 
   if (lane == 0 && !dry) {
     if (late) record_status(reinterpret_cast<WsHeader*>(p.ws + p.lay.header), SPEC_ERR_TIMEOUT);
     if (!row_ok) atomicOr(&bad_bits[b], 1u << i);
-    if (accept) atomicOr(&acc_bits[b], 1u << i);
-    atomicOr(&dec_bits[b], 1u << i);
+    // The early-exit hint first, so that producers see it as soon as possible.
     if (!accept) atomicMin(&first_reject[b], i);
+    // An accept only sets its bits.  A rejection (or a row without mass)
+    // releases with them: a final-pass CTA that sees the bit also sees this
+    // position's normalisers, argmax and bad-row bit, written above.
+    if (accept) atomicOr(&state[b], decision_bits(i, true));
+    else atom_or_release_u64(&state[b], decision_bits(i, false));
   }
 }
 
@@ -833,6 +836,9 @@ __global__ void __launch_bounds__(kSweepThreads, kSweepMinBlocks) sweep_kernel(S
   __syncthreads();
   // Everything below reads what the plan kernel wrote.
   pdl_wait();
+  // The final pass may launch now: its CTAs take the SMs this grid leaves
+  // during its tail and each waits for its own request's decisions.
+  if (kVerify) pdl_launch_dependents();
   WsHeader* h = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
   // Warp 0 keeps the books, warp 1 produces, warps 2..kNC+1 consume; the
   // mbarrier counts and reduction slots are sized for exactly this split.
@@ -848,6 +854,13 @@ __global__ void __launch_bounds__(kSweepThreads, kSweepMinBlocks) sweep_kernel(S
       sweep_producer<TIn, kVerify>(p, sm, h);
   } else if (warp == kBookWarp) {
     sweep_bookkeeper<TIn, kVerify>(p, sm, h);
+  }
+  // Count the CTA out once all its work is done, so that the final pass can
+  // hold its own completion until every sweep CTA has finished.
+  __syncthreads();
+  if (kVerify && threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(&h->sweep_exited, 1);
   }
 }
 
