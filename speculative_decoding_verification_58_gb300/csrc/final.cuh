@@ -273,6 +273,123 @@ __device__ void slice_records(const TIn* rt, const TIn* rd, int V, const MassSpe
   }
 }
 
+// The same records, with the slice streamed through shared memory by bulk
+// copies (rows 16-byte aligned): a ring of kFinalStages pieces, each S
+// segments of the target row and, for a residual, the same S segments of the
+// draft row after them.  Thread 0 keeps kFinalStages pieces in flight; every
+// warp takes the piece's segments w, w + 8, ... and computes exactly what
+// slice_records computes.  Far more bytes in flight per CTA than register
+// loads allow, which is what a request finishing alone, at the end of a
+// round, needs.  Returns false if a wait ran out.
+constexpr int kFinalStages = 3;
+constexpr int kFinalStageBytes = 16384;
+
+struct FinalRing {
+  uint64_t full[kFinalStages];
+  int abort_flag;
+};
+
+template <typename TIn>
+__device__ bool slice_records_staged(const TIn* rt, const TIn* rd, int V, const MassSpec& ms,
+                                     bool bonus, int s_lo, int s_hi, float2* rec,
+                                     unsigned char* ring, FinalRing& fr) {
+  constexpr int SB = kSegElems * (int)sizeof(TIn);  // bytes of one segment of one row
+  constexpr int NV = SB / 512;                      // 16-byte vectors per lane per segment
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool has_q = !bonus && ms.has_q;
+  const int R = has_q ? 2 : 1;
+  const int S = kFinalStageBytes / (R * SB);
+  const int npieces = (s_hi - s_lo + S - 1) / S;
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < kFinalStages; ++j) mbar_init(&fr.full[j], 1);
+    fr.abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // Bytes of segments [g0, g1) of one row (the row's last segment may be
+  // short; V * size is a multiple of 16, so every size is).
+  auto piece_bytes = [&](int j) {
+    const int g0 = s_lo + j * S, g1 = min(s_hi, g0 + S);
+    return (uint32_t)((min((long long)V, (long long)g1 * kSegElems) - (long long)g0 * kSegElems) *
+                      (long long)sizeof(TIn));
+  };
+  auto issue = [&](int j) {
+    const int slot = j % kFinalStages;
+    const int g0 = s_lo + j * S;
+    const uint32_t nb = piece_bytes(j);
+    unsigned char* dst = ring + slot * kFinalStageBytes;
+    mbar_arrive_expect_tx(&fr.full[slot], nb * R);
+    bulk_g2s(dst, rt + (size_t)g0 * kSegElems, nb, &fr.full[slot]);
+    if (has_q) bulk_g2s(dst + S * SB, rd + (size_t)g0 * kSegElems, nb, &fr.full[slot]);
+  };
+  if (threadIdx.x == 0)
+    for (int j = 0; j < kFinalStages && j < npieces; ++j) issue(j);
+  bool ok = true;
+  for (int j = 0; j < npieces; ++j) {
+    const int slot = j % kFinalStages;
+    if (!mbar_wait_bounded(&fr.full[slot], (uint32_t)(j / kFinalStages) & 1u, &fr.abort_flag))
+      ok = false;
+    const int g0 = s_lo + j * S, nseg = min(s_hi - g0, S);
+    const uint4* buf = reinterpret_cast<const uint4*>(ring + slot * kFinalStageBytes);
+    if (ok) {
+      for (int ls = warp; ls < nseg; ls += kFinalWarps) {
+        const int seg = g0 + ls;
+        const int e0 = seg * kSegElems + lane * 8;
+        Seg8<TIn> t, d;
+#pragma unroll
+        for (int w = 0; w < NV; ++w) t.v[w] = buf[ls * SB / 16 + lane * NV + w];
+        if (has_q) {
+#pragma unroll
+          for (int w = 0; w < NV; ++w) d.v[w] = buf[(S + ls) * SB / 16 + lane * NV + w];
+        }
+        // Entries past the end of the row are not in the stage.
+        if (e0 + 8 > V) {
+          uint32_t* tw = reinterpret_cast<uint32_t*>(t.v);
+          uint32_t* dw = reinterpret_cast<uint32_t*>(d.v);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            if (e0 + e < V) continue;
+            if (sizeof(TIn) == 2) {
+              const uint32_t hi = (e & 1) ? 0xFF800000u : 0u, keep = (e & 1) ? 0x0000FFFFu : 0xFFFF0000u;
+              const uint32_t lo = (e & 1) ? 0u : 0x0000FF80u;
+              tw[e / 2] = (tw[e / 2] & keep) | hi | lo;
+              dw[e / 2] = (dw[e / 2] & keep) | hi | lo;
+            } else {
+              tw[e] = 0xFF800000u;
+              dw[e] = 0xFF800000u;
+            }
+          }
+        }
+        float r[8];
+        float2 out;
+        if (bonus) {
+          const float m = warp_max_f32(seg8_max(t));
+          bonus_masses(t, ms.sc, __fmul_rn(m, ms.sc), r);
+          out = make_float2(m, warp_sum_f32(sum8(r)));
+        } else {
+          entry_masses(t, d, ms, r);
+          out = make_float2(warp_sum_f32(sum8(r)), 0.0f);
+        }
+        if (lane == 0) __stcg(&rec[seg], out);
+      }
+    }
+    // Everyone is done with this piece: the slot can take piece j + stages.
+    __syncthreads();
+    if (threadIdx.x == 0 && ok && j + kFinalStages < npieces) issue(j + kFinalStages);
+  }
+  ok = __syncthreads_and(ok);
+  if (!ok && threadIdx.x == 0) {
+    // A wait ran out: let the copies still in flight land (bounded) before
+    // the shared memory is given back.
+    int dummy = 0;
+    for (int j = 0; j < npieces; ++j)
+      mbar_wait_bounded(&fr.full[j % kFinalStages], (uint32_t)(j / kFinalStages) & 1u,
+                        (volatile int*)&dummy);
+  }
+  __syncthreads();
+  return ok;
+}
+
 // Largest entry of segments [s_lo, s_hi) and its lowest index (block-wide).
 template <typename TIn>
 __device__ ArgAcc slice_argmax(const TIn* row, int V, int s_lo, int s_hi, bool vec_ok,
@@ -476,7 +593,8 @@ __device__ __forceinline__ int slice_lo(int part, int nseg, int P) {
 // request's outcome is known -- every position up to the first rejection
 // (or all L) decided -- acquiring the deciders' writes with the mask.
 template <typename TIn>
-__device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh, float2* rec_sm) {
+__device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh, float2* rec_sm,
+                                           FinalRing& fr) {
   const int nseg = segments_of(p.V);
   const int part = blockIdx.x, b = blockIdx.y, P = gridDim.x;
   WsHeader* h = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
@@ -612,7 +730,15 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
       __stcg(&slice_arg[part], a.i);
     }
   } else {
-    slice_records(trow, drow, p.V, ms, bonus, s_lo, s_hi, rec, vec_ok);
+    // Aligned rows stream through shared memory; others load directly.
+    if (vec_ok && ((size_t)p.V * sizeof(TIn)) % 16 == 0) {
+      if (!slice_records_staged(trow, drow, p.V, ms, bonus, s_lo, s_hi, rec,
+                                reinterpret_cast<unsigned char*>(rec_sm), fr) &&
+          threadIdx.x == 0)
+        record_status(h, SPEC_ERR_TIMEOUT);
+    } else {
+      slice_records(trow, drow, p.V, ms, bonus, s_lo, s_hi, rec, vec_ok);
+    }
   }
 
   // ---- the last slice CTA of the request combines ----
@@ -671,12 +797,15 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
 
 template <typename TIn>
 __global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) {
-  extern __shared__ __align__(16) unsigned char fsm_raw[];
+  extern __shared__ __align__(128) unsigned char fsm_raw[];
   __shared__ FinalShared sh;
+  __shared__ FinalRing fr;
   // The next call's plan kernel may launch now; it waits for this grid to
   // finish before it touches the workspace.
   pdl_launch_dependents();
-  final_body<TIn>(p, sh, reinterpret_cast<float2*>(fsm_raw));
+  // fsm_raw holds the slice ring first and the combine's segment records
+  // after it.
+  final_body<TIn>(p, sh, reinterpret_cast<float2*>(fsm_raw), fr);
   // The grid must not finish before the sweep grid has (the next call's plan
   // waits only for this one): the last CTA out waits, bounded, for every
   // sweep CTA to have counted itself out.

@@ -6,6 +6,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -133,7 +134,7 @@ cudaError_t device_info(DeviceInfo** out) {
     if ((e = sweep_blocks<uint16_t, true>(&d.sweep_blocks_per_sm[1][1])) != cudaSuccess) return e;
     if ((e = sweep_blocks<float, false>(&d.sweep_blocks_per_sm[0][0])) != cudaSuccess) return e;
     if ((e = sweep_blocks<uint16_t, false>(&d.sweep_blocks_per_sm[1][0])) != cudaSuccess) return e;
-    const int fsm = (int)(kMaxSegs * sizeof(float2));
+    const int fsm = (int)std::max(kMaxSegs * sizeof(float2), (size_t)kFinalStages * kFinalStageBytes);
     if ((e = cudaFuncSetAttribute(final_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   fsm)) != cudaSuccess)
       return e;
@@ -273,7 +274,9 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
   if (P > nseg) P = nseg;
   if (P < 1) P = 1;
   fp.P = P;
-  const size_t fsm = (size_t)nseg * sizeof(float2);
+  // Dynamic shared memory: the slice ring, later reused for the combine's
+  // segment records.
+  const size_t fsm = std::max((size_t)nseg * sizeof(float2), (size_t)kFinalStages * kFinalStageBytes);
   if (record(ev, 2, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   if (launch(final_kernel<TIn>, dim3(P, B), dim3(kFinalThreads), fsm, stream, pdl, fp) !=
       cudaSuccess)
