@@ -232,6 +232,59 @@ def spec_verify(target_logits, draft_logits, draft_tokens, lengths, uniforms, te
     return out_tokens, num_accepted
 
 
+class Verifier:
+    """``spec_verify`` bound to one fixed set of device buffers.
+
+    A serving loop verifies into the same buffers every round; this object
+    checks their shapes, dtypes and devices once, at construction, and keeps
+    the C call's argument tuple, so that each round costs the host one ctypes
+    call (the Python checks of ``spec_verify`` cost more than a short round
+    on the GPU).  The buffers' contents may change between calls; the
+    tensors themselves must stay alive and keep their storage.
+    """
+
+    def __init__(self, target_logits, draft_logits, draft_tokens, lengths, uniforms, temperature,
+                 *, workspace=None, out_tokens=None, num_accepted=None, stream=None,
+                 full_sweep: bool = False):
+        torch = _torch()
+        B, k1, V = target_logits.shape
+        k = k1 - 1
+        dev = target_logits.device
+        dt = _dtype_code(target_logits)
+        _need(target_logits, "target_logits", target_logits.dtype, (B, k + 1, V), dev)
+        _need(draft_logits, "draft_logits", target_logits.dtype, (B, k, V), dev)
+        _need(draft_tokens, "draft_tokens", torch.int32, (B, k), dev)
+        _need(lengths, "lengths", torch.int32, (B,), dev)
+        _need(uniforms, "uniforms", torch.float32, (B, k + 1), dev)
+        _need(temperature, "temperature", torch.float32, (B,), dev)
+        if workspace is None:
+            workspace = alloc_workspace(B, k, V, dev)
+        if out_tokens is None:
+            out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+        if num_accepted is None:
+            num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+        _need(out_tokens, "out_tokens", torch.int32, (B, k + 1), dev)
+        _need(num_accepted, "num_accepted", torch.int32, (B,), dev)
+        # Keep every buffer referenced for as long as the bound call exists.
+        self._keep = (target_logits, draft_logits, draft_tokens, lengths, uniforms, temperature,
+                      workspace)
+        self.workspace, self.out_tokens, self.num_accepted = workspace, out_tokens, num_accepted
+        self._fn = lib().spec_verify_ex
+        self._args = (target_logits.data_ptr(), draft_logits.data_ptr(), dt,
+                      draft_tokens.data_ptr(), lengths.data_ptr(), uniforms.data_ptr(),
+                      temperature.data_ptr(), B, k, V, out_tokens.data_ptr(),
+                      num_accepted.data_ptr(), workspace.data_ptr(),
+                      workspace.numel() * workspace.element_size(), _stream_ptr(stream),
+                      SPEC_FLAG_FULL_SWEEP if full_sweep else 0)
+
+    def __call__(self):
+        """Enqueue one round on the bound stream; returns (out_tokens, num_accepted)."""
+        code = self._fn(*self._args)
+        if code != SPEC_OK:
+            raise SpecVerifyError(code, "spec_verify")
+        return self.out_tokens, self.num_accepted
+
+
 def spec_verify_static(target_logits, draft_logits, draft_tokens, lengths, uniforms, temperature,
                        *, out_tokens=None, num_accepted=None, stream=None):
     """spec_verify for callers that cannot allocate: no workspace argument.

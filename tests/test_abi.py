@@ -90,3 +90,20 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(sv, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         sv.lib()
+
+
+def test_bound_call_checks_buffers_once_at_construction():
+    torch = pytest.importorskip("torch")
+    B, k, V = 2, 3, 16
+    t = torch.zeros(B, k + 1, V)
+    good = dict(target_logits=t, draft_logits=torch.zeros(B, k, V),
+                draft_tokens=torch.zeros(B, k, dtype=torch.int32),
+                lengths=torch.ones(B, dtype=torch.int32), uniforms=torch.zeros(B, k + 1),
+                temperature=torch.ones(B))
+    for key, bad in (("draft_logits", torch.zeros(B, k + 1, V)),
+                     ("draft_tokens", torch.zeros(B, k, dtype=torch.int64)),
+                     ("uniforms", torch.zeros(B, k)),
+                     ("temperature", torch.ones(B + 1)),
+                     ("draft_logits", torch.zeros(B, k, V, dtype=torch.bfloat16))):
+        with pytest.raises((TypeError, ValueError)):
+            sv.Verifier(**{**good, key: bad})

@@ -239,3 +239,21 @@ def test_host_argument_errors_launch_nothing():
     bad = list(args); bad[0] += 1
     assert L.spec_verify(*bad) == sv.SPEC_ERR_INVALID_ARG
     torch.cuda.synchronize()
+
+
+def test_bound_call_matches_spec_verify_and_sees_new_contents():
+    a = synth.make_inputs("zipf_mixed_temp", 32, 16, 9000, "bf16", seed=21)
+    b = synth.make_inputs("zipf_mixed_temp", 32, 16, 9000, "bf16", seed=22)
+    d = sv.to_device(a)
+    call = sv.Verifier(**d)
+    for inp in (a, b):
+        # Same buffers, new contents: the bound call reads what is there now.
+        for key, t in sv.to_device(inp).items():
+            d[key].copy_(t)
+        out, n = call()
+        want_out, want_n = sv.spec_verify(**d)
+        np.testing.assert_array_equal(out.cpu().numpy(), want_out.cpu().numpy())
+        np.testing.assert_array_equal(n.cpu().numpy(), want_n.cpu().numpy())
+        o = oracle.verify(inp.target, inp.draft, inp.tokens, inp.lengths, inp.uniforms,
+                          inp.temperature)
+        compare(out.cpu().numpy(), n.cpu().numpy(), o, inp.temperature, "bound call")
