@@ -147,6 +147,42 @@ spec_status_t spec_verify_timed(const void* target_logits, const void* draft_log
                                 void* ev_plan, void* ev_sweep, void* ev_final, void* ev_end);
 
 /*
+ * Verification over a packed (ragged) batch.  AdaFlash Section 3.3,
+ * "Adaptive Request Scheduling": with per-request verification lengths
+ * k_b, the serving engine packs the candidates into one verification batch
+ * of total length sum_b k_b rather than padding every request to k.  The
+ * logits then come as flat row buffers:
+ *
+ *   target_rows   [rows_t, V]  dtype; request b's target rows are
+ *                              target_row_start[b] + 0 .. L_b (L_b + 1 rows:
+ *                              one per draft position and one for the bonus)
+ *   draft_rows    [rows_d, V]  dtype; request b's draft rows are
+ *                              draft_row_start[b] + 0 .. L_b - 1.  May be NULL
+ *                              when rows_d == 0 (all requests greedy).
+ *   target_row_start, draft_row_start
+ *                 [B]          int32 (device).  Any placement is allowed
+ *                              (order, gaps, shared rows); the rows named must lie
+ *                              inside their buffer.  A greedy request's draft
+ *                              rows are never read and its draft_row_start is
+ *                              not checked.
+ *   rows_t, rows_d             row counts of the two buffers: 1 <= rows_t and
+ *                              0 <= rows_d, both <= INT32_MAX.
+ *
+ * Everything else (tokens [B, k], uniforms [B, k+1], outputs, workspace,
+ * flags) is as for spec_verify_ex; the results are identical to spec_verify
+ * on the same rows laid out padded.  A request whose rows fall outside a
+ * buffer is invalid (num_accepted = -1, SPEC_ERR_BAD_INPUT recorded).
+ */
+spec_status_t spec_verify_packed(const void* target_rows, long long rows_t,
+                                 const void* draft_rows, long long rows_d, spec_dtype_t dtype,
+                                 const int32_t* target_row_start,
+                                 const int32_t* draft_row_start, const int32_t* draft_tokens,
+                                 const int32_t* lengths, const float* uniforms,
+                                 const float* temperature, int B, int k, int V,
+                                 int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                                 size_t workspace_bytes, void* stream, unsigned flags);
+
+/*
  * spec_verify for callers that cannot allocate device memory.  (The paper
  * has no counterpart: this is a deployment convenience.)  Some callers are
  * handed only their input and output buffers -- for example an operator

@@ -139,3 +139,53 @@ def row_stats(logits, temperature_per_row):
                              _ptr(mx, ctypes.c_double), _ptr(lse, ctypes.c_double),
                              _ptr(arg, ctypes.c_int32))
     return mx, lse, arg
+
+
+def verify_packed(target_rows, draft_rows, target_row_start, draft_row_start, draft_tokens,
+                  lengths, uniforms, temperature) -> OracleResult:
+    """The oracle on a packed batch (AdaFlash Section 3.3: a verification batch of
+    total length sum_b k_b instead of B x k).
+
+    Request b's target rows are ``target_rows[target_row_start[b] + i]`` for
+    i = 0..L_b and its draft rows ``draft_rows[draft_row_start[b] + i]`` for
+    i < L_b.  A request whose rows fall outside a buffer is invalid (the draft
+    rows of a greedy request are not used and not checked).  The rows are
+    gathered into the padded layout, the positions no request owns filled with
+    NaN (the rule never reads them), and ``verify`` runs on that.
+    """
+    tr, dt = _logits(target_rows)
+    dr, dt2 = _logits(draft_rows) if np.asarray(draft_rows).size else (None, dt)
+    if dt != dt2:
+        raise TypeError("target and draft rows must have the same dtype")
+    tok = np.ascontiguousarray(draft_tokens, dtype=np.int32)
+    B, k = tok.shape
+    V = tr.shape[1]
+    lens = np.asarray(lengths, np.int32).reshape(B)
+    temp = np.asarray(temperature, np.float32).reshape(B)
+    t0 = np.asarray(target_row_start, np.int64).reshape(B)
+    d0 = np.asarray(draft_row_start, np.int64).reshape(B)
+    rows_t, rows_d = tr.shape[0], (0 if dr is None else dr.shape[0])
+    nan = np.float32(np.nan) if dt == F32 else np.uint16(0x7FC0)
+    target = np.full((B, k + 1, V), nan, dtype=tr.dtype)
+    draft = np.full((B, k, V), nan, dtype=tr.dtype)
+    placed = np.zeros(B, bool)
+    for b in range(B):
+        L = int(lens[b])
+        if not 1 <= L <= k:
+            continue  # verify() rejects the length itself
+        ok = 0 <= t0[b] and t0[b] + L + 1 <= rows_t
+        if temp[b] != 0:
+            ok = ok and 0 <= d0[b] and d0[b] + L <= rows_d
+        if not ok:
+            continue
+        placed[b] = True
+        target[b, :L + 1] = tr[t0[b]:t0[b] + L + 1]
+        if temp[b] != 0:
+            draft[b, :L] = dr[d0[b]:d0[b] + L]
+    res = verify(target, draft, tok, lens, uniforms, temp)
+    for b in range(B):
+        if 1 <= lens[b] <= k and not placed[b] and res.num_accepted[b] >= 0:
+            res.num_accepted[b] = -1
+            res.out_tokens[b] = -1
+            res.bad_requests += 1
+    return res

@@ -10,6 +10,8 @@ every call raises.
 The functions keep the C names:
 
 ``spec_verify(...)``                 batched verification (asynchronous)
+``spec_verify_packed(...)``          the same over a packed (ragged) batch of rows
+``Verifier(...)``                    spec_verify bound to fixed buffers (one C call per round)
 ``spec_verify_workspace_bytes(...)`` workspace size for (B, k, V)
 ``spec_verify_report(ws)``           what the device recorded for the last call
 ``spec_verify_device_status(ws)``    just the recorded status
@@ -40,7 +42,7 @@ SPEC_FLAG_FULL_SWEEP = 1
 
 # Every entry point include/spec_verify.h declares.
 EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_ex", "spec_verify_timed",
-           "spec_verify_report",
+           "spec_verify_packed", "spec_verify_report",
            "spec_verify_device_status", "spec_row_stats_workspace_bytes", "spec_row_stats",
            "spec_status_string", "spec_abi_version", "spec_verify_static")
 SPEC_STATIC_SCRATCH_BYTES = 8 << 20
@@ -98,6 +100,10 @@ def lib() -> ctypes.CDLL:
     L.spec_verify_ex.restype = ci
     L.spec_verify_timed.argtypes = L.spec_verify_ex.argtypes + [vp, vp, vp, vp]
     L.spec_verify_timed.restype = ci
+    L.spec_verify_packed.argtypes = [vp, ctypes.c_longlong, vp, ctypes.c_longlong, ci, i32p, i32p,
+                                     i32p, i32p, f32p, f32p, ci, ci, ci, i32p, i32p, vp, csz, vp,
+                                     ctypes.c_uint]
+    L.spec_verify_packed.restype = ci
     L.spec_verify_static.argtypes = [vp, vp, ci, i32p, i32p, f32p, f32p, ci, ci, ci, i32p, i32p, vp]
     L.spec_verify_static.restype = ci
     L.spec_verify_report.argtypes = [vp, vp, ctypes.POINTER(_Report)]
@@ -232,6 +238,50 @@ def spec_verify(target_logits, draft_logits, draft_tokens, lengths, uniforms, te
     return out_tokens, num_accepted
 
 
+def spec_verify_packed(target_rows, draft_rows, target_row_start, draft_row_start, draft_tokens,
+                       lengths, uniforms, temperature, *, workspace=None, out_tokens=None,
+                       num_accepted=None, stream=None, full_sweep: bool = False):
+    """Verification over a packed batch (AdaFlash Section 3.3: total length sum_b k_b).
+
+    ``target_rows`` [rows_t, V] and ``draft_rows`` [rows_d, V] (float32 or
+    bfloat16, same); request b reads target rows ``target_row_start[b] + 0..L_b``
+    and draft rows ``draft_row_start[b] + 0..L_b-1`` (int32 [B] each).
+    ``draft_tokens`` int32 [B, k] fixes k.  Other arguments and the results are
+    those of ``spec_verify``.
+    """
+    torch = _torch()
+    rows_t, V = target_rows.shape
+    B, k = draft_tokens.shape
+    dev = target_rows.device
+    dt = _dtype_code(target_rows)
+    rows_d = draft_rows.shape[0]
+    _need(target_rows, "target_rows", target_rows.dtype, (rows_t, V), dev)
+    _need(draft_rows, "draft_rows", target_rows.dtype, (rows_d, V), dev)
+    _need(target_row_start, "target_row_start", torch.int32, (B,), dev)
+    _need(draft_row_start, "draft_row_start", torch.int32, (B,), dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, k), dev)
+    _need(lengths, "lengths", torch.int32, (B,), dev)
+    _need(uniforms, "uniforms", torch.float32, (B, k + 1), dev)
+    _need(temperature, "temperature", torch.float32, (B,), dev)
+    if workspace is None:
+        workspace = alloc_workspace(B, k, V, dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    if num_accepted is None:
+        num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, k + 1), dev)
+    _need(num_accepted, "num_accepted", torch.int32, (B,), dev)
+    code = lib().spec_verify_packed(
+        target_rows.data_ptr(), rows_t, draft_rows.data_ptr() if rows_d else None, rows_d, dt,
+        target_row_start.data_ptr(), draft_row_start.data_ptr(), draft_tokens.data_ptr(),
+        lengths.data_ptr(), uniforms.data_ptr(), temperature.data_ptr(), B, k, V,
+        out_tokens.data_ptr(), num_accepted.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream),
+        SPEC_FLAG_FULL_SWEEP if full_sweep else 0)
+    _check(code, "spec_verify_packed")
+    return out_tokens, num_accepted
+
+
 class Verifier:
     """``spec_verify`` bound to one fixed set of device buffers.
 
@@ -355,6 +405,23 @@ def spec_row_stats(logits, temperature, *, stream=None):
                                 mx.data_ptr(), lse.data_ptr(), arg.data_ptr(), ws.data_ptr(), n,
                                 _stream_ptr(stream)), "spec_row_stats")
     return mx, lse, arg
+
+
+def _logits_to_device(a, device):
+    torch = _torch()
+    import numpy as np
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(a).to(device)
+
+
+def to_device_packed(packed, device="cuda"):
+    """Copy a ``synth.PackedRows`` layout to the device (the packed entry's row buffers)."""
+    torch = _torch()
+    return dict(target_rows=_logits_to_device(packed.target_rows, device),
+                draft_rows=_logits_to_device(packed.draft_rows, device),
+                target_row_start=torch.from_numpy(packed.target_row_start).to(device),
+                draft_row_start=torch.from_numpy(packed.draft_row_start).to(device))
 
 
 def to_device(inputs, device="cuda"):

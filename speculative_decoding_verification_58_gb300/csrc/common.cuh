@@ -76,7 +76,7 @@ constexpr unsigned long long kPartialEmpty = 0x7FC0DEAD7FC0DEADull;
 
 struct WsLayout {
   size_t header, rowdesc, flags, first_reject, state, bad_bits, done, pos_c, pos_arg,
-      partials, seg_mass, slice_ref, slice_arg, final_done, warm, total;
+      partials, seg_mass, slice_ref, slice_arg, final_done, rowbase, warm, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -105,7 +105,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int k, int C, int V) {
   size_t o = 0;
   size_t slots = (size_t)B * (size_t)k * 2;
   l.header = o;       o = align256(o + sizeof(WsHeader));
-  l.rowdesc = o;      o = align256(o + slots * sizeof(int2));
+  l.rowdesc = o;      o = align256(o + slots * sizeof(int4));
   l.flags = o;        o = align256(o + (size_t)B * sizeof(int32_t));
   l.first_reject = o; o = align256(o + (size_t)B * sizeof(int32_t));
   l.state = o;        o = align256(o + (size_t)B * sizeof(unsigned long long));
@@ -118,6 +118,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int k, int C, int V) {
   l.slice_ref = o;    o = align256(o + (size_t)B * kMaxSlices * sizeof(float));
   l.slice_arg = o;    o = align256(o + (size_t)B * kMaxSlices * sizeof(int32_t));
   l.final_done = o;   o = align256(o + (size_t)B * sizeof(int32_t));
+  l.rowbase = o;      o = align256(o + (size_t)B * sizeof(int2));
   l.warm = o;         o = align256(o + 2 * (size_t)C * sizeof(Partial));
   l.total = o;
   return l;

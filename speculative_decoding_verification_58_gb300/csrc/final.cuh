@@ -705,9 +705,12 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
   }
 
   // ---- this slice's share of the row(s) ----
-  const TIn* trow = static_cast<const TIn*>(p.target) + ((size_t)b * (p.k + 1) + n) * (size_t)p.V;
+  // Row n of the request in either buffer: its first rows come from the
+  // plan kernel (padded or packed layout).
+  const int2 rb = __ldcg(reinterpret_cast<const int2*>(p.ws + p.lay.rowbase) + b);
+  const TIn* trow = static_cast<const TIn*>(p.target) + ((size_t)rb.x + n) * (size_t)p.V;
   const TIn* drow = job == kJobResidual
-                        ? static_cast<const TIn*>(p.draft) + ((size_t)b * p.k + n) * (size_t)p.V
+                        ? static_cast<const TIn*>(p.draft) + ((size_t)rb.y + n) * (size_t)p.V
                         : trow;
   const bool vec_ok =
       ((reinterpret_cast<uintptr_t>(trow) | reinterpret_cast<uintptr_t>(drow)) & 15u) == 0;

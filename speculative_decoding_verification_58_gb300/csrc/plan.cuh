@@ -7,6 +7,13 @@
 // checked with independent loads, invalid requests land in a shared bitmask;
 // (2) every (position, request) item is counted, its request's state reset,
 // and one block-wide scan places the row descriptors.
+//
+// Row addressing: request b's target rows are rows t0_b + 0..L_b of the
+// target buffer and its draft rows d0_b + 0..L_b-1 of the draft buffer.  The
+// padded layout [B, k+1, V] / [B, k, V] has t0_b = b(k+1), d0_b = bk; the
+// packed layout (AdaFlash Section 3.3, a verification batch of total length
+// sum_b k_b) takes t0_b, d0_b from the caller and checks them against the
+// buffers' row counts.  Each descriptor carries its absolute row.
 #pragma once
 
 #include "common.cuh"
@@ -18,6 +25,9 @@ struct PlanParams {
   const int32_t* lengths;     // [B]
   const float* uniforms;      // [B, k+1]
   const float* temperature;   // [B]
+  const int32_t* t_start;     // [B] packed layout: first target row of b (null: padded)
+  const int32_t* d_start;     // [B] packed layout: first draft row of b
+  long long rows_t, rows_d;   // packed layout: rows in the target / draft buffers
   int B, k, V, C, chunk_elems, nch;
   unsigned char* ws;
   WsLayout lay;
@@ -80,7 +90,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __shared__ int warp_tot[33];
   const int tid = threadIdx.x;
   WsHeader* h = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
-  int2* rowdesc = reinterpret_cast<int2*>(p.ws + p.lay.rowdesc);
+  int4* rowdesc = reinterpret_cast<int4*>(p.ws + p.lay.rowdesc);
+  int2* rowbase = reinterpret_cast<int2*>(p.ws + p.lay.rowbase);
   int32_t* flags = reinterpret_cast<int32_t*>(p.ws + p.lay.flags);
   int32_t* first_reject = reinterpret_cast<int32_t*>(p.ws + p.lay.first_reject);
 
@@ -120,14 +131,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __syncthreads();
 
   // Pass 1, item j = b*(k+1) + i: the request's scalars (at i = 0: 1 <= L <= k
-  // from the length head's clamp, T is 0 or a finite normal float), token x_i
-  // in [0, V) for i < L, uniform u_i in [0, 1) for i <= L when T > 0.  Four
-  // items per thread per round, all loads issued before any is used.
+  // from the length head's clamp, T is 0 or a finite normal float, packed
+  // rows inside their buffers), token x_i in [0, V) for i < L, uniform u_i
+  // in [0, 1) for i <= L when T > 0.  Four items per thread per round, all
+  // loads issued before any is used.
   const int k1 = p.k + 1;
   const int items1 = p.B * k1;
   constexpr int kR = 4;
   for (int base = 0; base < items1; base += kR * kPlanThreads) {
-    int L[kR], x[kR];
+    int L[kR], x[kR], t0[kR], d0[kR];
     float T[kR], u[kR];
 #pragma unroll
     for (int q = 0; q < kR; ++q) {
@@ -136,6 +148,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       x[q] = 0;
       T[q] = 0.0f;
       u[q] = 0.0f;
+      t0[q] = 0;
+      d0[q] = 0;
       if (j < items1) {
         const int b = j / k1;
         const int i = j - b * k1;
@@ -143,6 +157,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
         T[q] = __ldg(&p.temperature[b]);
         if (i < p.k) x[q] = __ldg(&p.tokens[(size_t)b * p.k + i]);
         u[q] = __ldg(&p.uniforms[j]);
+        if (i == 0 && p.t_start != nullptr) {
+          t0[q] = __ldg(&p.t_start[b]);
+          d0[q] = __ldg(&p.d_start[b]);
+        }
       }
     }
 #pragma unroll
@@ -152,6 +170,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       const int b = j / k1;
       const int i = j - b * k1;
       bool bad = (i == 0) && !(L[q] >= 1 && L[q] <= p.k && temperature_ok(T[q]));
+      // Packed rows: target rows t0 .. t0+L exist, and draft rows d0 .. d0+L-1
+      // unless the request is greedy (its draft rows are never read).
+      bad = bad || (i == 0 && p.t_start != nullptr &&
+                    !(t0[q] >= 0 && (long long)t0[q] + L[q] + 1 <= p.rows_t &&
+                      (T[q] == 0.0f || (d0[q] >= 0 && (long long)d0[q] + L[q] <= p.rows_d))));
       bad = bad || (i < L[q] && i < p.k && (x[q] < 0 || x[q] >= p.V));
       bad = bad || (T[q] > 0.0f && i <= L[q] && !(u[q] >= 0.0f && u[q] < 1.0f));  // NaN fails
       if (bad) atomicOr(&bad_mask[b >> 5], 1u << (b & 31));
@@ -165,6 +188,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     const bool greedy = __ldg(&p.temperature[b]) == 0.0f;
     flags[b] = ok ? (kReqValid | (greedy ? kReqGreedy : 0)) : 0;
     first_reject[b] = p.k;
+    rowbase[b] = p.t_start != nullptr ? make_int2(__ldg(&p.t_start[b]), __ldg(&p.d_start[b]))
+                                      : make_int2(b * (p.k + 1), b * p.k);
     if (!ok) {
       atomicAdd(&h->bad_requests, 1);
       atomicMin(&h->first_bad, b);
@@ -193,8 +218,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     const float T = __ldg(&p.temperature[b]);
     const float sc = T == 0.0f ? 0.0f : softmax_scale(T);
     const int slot = (b * p.k + i) << 1;
-    rowdesc[pos++] = make_int2(slot, __float_as_int(sc));
-    if (T != 0.0f) rowdesc[pos++] = make_int2(slot | 1, __float_as_int(sc));
+    const int trow = (p.t_start != nullptr ? __ldg(&p.t_start[b]) : b * (p.k + 1)) + i;
+    rowdesc[pos++] = make_int4(slot, __float_as_int(sc), trow, 0);
+    if (T != 0.0f) {
+      const int drow = (p.t_start != nullptr ? __ldg(&p.d_start[b]) : b * p.k) + i;
+      rowdesc[pos++] = make_int4(slot | 1, __float_as_int(sc), drow, 0);
+    }
   }
   if (tid == 0) {
     h->rows_planned = total;

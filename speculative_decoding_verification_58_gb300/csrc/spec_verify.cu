@@ -24,19 +24,19 @@ WsLayout stats_layout(int rows, int C) {
   WsLayout l = {};
   l.header = 0;
   l.rowdesc = align256(sizeof(WsHeader));
-  l.partials = l.rowdesc + align256((size_t)rows * sizeof(int2));
+  l.partials = l.rowdesc + align256((size_t)rows * sizeof(int4));
   l.total = l.partials + align256((size_t)rows * C * sizeof(Partial));
   return l;
 }
 
-// Row descriptors {row, bits of log2(e)/T} for the sweep, and the header.
+// Row descriptors {row, bits of log2(e)/T, row, 0} for the sweep, and the header.
 __global__ void stats_plan_kernel(unsigned char* ws, WsLayout lay, int rows, int nch,
                                   int chunk_elems, const float* temperature) {
   pdl_launch_dependents();
-  int2* rowdesc = reinterpret_cast<int2*>(ws + lay.rowdesc);
+  int4* rowdesc = reinterpret_cast<int4*>(ws + lay.rowdesc);
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x) {
     const float T = temperature[r];
-    rowdesc[r] = make_int2(r, __float_as_int(T == 0.0f ? 0.0f : softmax_scale(T)));
+    rowdesc[r] = make_int4(r, __float_as_int(T == 0.0f ? 0.0f : softmax_scale(T)), r, 0);
   }
   if (blockIdx.x != 0 || threadIdx.x != 0) return;
   WsHeader* h = reinterpret_cast<WsHeader*>(ws + lay.header);
@@ -200,7 +200,9 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
                            const float* uniforms, const float* temperature, int B, int k, int V,
                            int32_t* out_tokens, int32_t* num_accepted, void* workspace,
                            cudaStream_t stream, unsigned flags, int dtype_index,
-                           void* const* ev) {
+                           void* const* ev, const int32_t* t_start = nullptr,
+                           const int32_t* d_start = nullptr, long long rows_t = 0,
+                           long long rows_d = 0) {
   DeviceInfo* d = nullptr;
   if (device_info(&d) != cudaSuccess) return SPEC_ERR_CUDA;
   const long long slots = 2LL * B * k;
@@ -215,6 +217,10 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
   pp.lengths = lengths;
   pp.uniforms = uniforms;
   pp.temperature = temperature;
+  pp.t_start = t_start;
+  pp.d_start = d_start;
+  pp.rows_t = rows_t;
+  pp.rows_d = rows_d;
   pp.B = B;
   pp.k = k;
   pp.V = V;
@@ -353,16 +359,28 @@ size_t spec_verify_workspace_bytes(int B, int k, int V) {
   return ws_layout(B, k, chunks_per_row(slots, V), V).total;
 }
 
+// Padded layout: t_start == nullptr.  Packed layout: t_start / d_start give
+// each request's first row in buffers of rows_t / rows_d rows; a draft buffer
+// of zero rows may be null (then only greedy requests are valid).
 static spec_status_t verify_entry(const void* target_logits, const void* draft_logits,
                              spec_dtype_t dtype, const int32_t* draft_tokens,
                              const int32_t* lengths, const float* uniforms,
                              const float* temperature, int B, int k, int V, int32_t* out_tokens,
                              int32_t* num_accepted, void* workspace, size_t workspace_bytes,
-                             void* stream, unsigned flags, void* const* ev) {
+                             void* stream, unsigned flags, void* const* ev,
+                             const int32_t* t_start = nullptr, const int32_t* d_start = nullptr,
+                             long long rows_t = 0, long long rows_d = 0) {
   if (B < 1 || k < 1 || V < 1) return SPEC_ERR_INVALID_ARG;
   if (!sizes_ok(B, k, V)) return SPEC_ERR_UNSUPPORTED;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
   if ((flags & ~SPEC_FLAG_FULL_SWEEP) != 0) return SPEC_ERR_INVALID_ARG;
+  const bool packed = (t_start != nullptr);
+  if (packed) {
+    if (!d_start || !aligned(t_start, 4) || !aligned(d_start, 4)) return SPEC_ERR_INVALID_ARG;
+    if (rows_t < 1 || rows_t > INT32_MAX || rows_d < 0 || rows_d > INT32_MAX)
+      return SPEC_ERR_INVALID_ARG;
+    if (rows_d == 0 && !draft_logits) draft_logits = target_logits;  // never read
+  }
   if (!target_logits || !draft_logits || !draft_tokens || !lengths || !uniforms || !temperature ||
       !out_tokens || !num_accepted)
     return SPEC_ERR_INVALID_ARG;
@@ -379,10 +397,24 @@ static spec_status_t verify_entry(const void* target_logits, const void* draft_l
   if (dtype == SPEC_F32)
     return verify_typed<float>(target_logits, draft_logits, draft_tokens, lengths, uniforms,
                                temperature, B, k, V, out_tokens, num_accepted, workspace, s, flags, 0,
-                               ev);
+                               ev, t_start, d_start, rows_t, rows_d);
   return verify_typed<uint16_t>(target_logits, draft_logits, draft_tokens, lengths, uniforms,
                                 temperature, B, k, V, out_tokens, num_accepted, workspace, s, flags,
-                                1, ev);
+                                1, ev, t_start, d_start, rows_t, rows_d);
+}
+
+spec_status_t spec_verify_packed(const void* target_rows, long long rows_t, const void* draft_rows,
+                                 long long rows_d, spec_dtype_t dtype,
+                                 const int32_t* target_row_start, const int32_t* draft_row_start,
+                                 const int32_t* draft_tokens, const int32_t* lengths,
+                                 const float* uniforms, const float* temperature, int B, int k,
+                                 int V, int32_t* out_tokens, int32_t* num_accepted,
+                                 void* workspace, size_t workspace_bytes, void* stream,
+                                 unsigned flags) {
+  if (!target_row_start || !draft_row_start) return SPEC_ERR_INVALID_ARG;
+  return verify_entry(target_rows, draft_rows, dtype, draft_tokens, lengths, uniforms,
+                      temperature, B, k, V, out_tokens, num_accepted, workspace, workspace_bytes,
+                      stream, flags, nullptr, target_row_start, draft_row_start, rows_t, rows_d);
 }
 
 spec_status_t spec_verify_ex(const void* target_logits, const void* draft_logits,

@@ -109,7 +109,7 @@ template <typename TIn, bool kVerify>
 __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h) {
   using Tr = ElemTraits<TIn>;
   const int lane = threadIdx.x & 31;
-  const int2* rowdesc = reinterpret_cast<const int2*>(p.ws + p.lay.rowdesc);
+  const int4* rowdesc = reinterpret_cast<const int4*>(p.ws + p.lay.rowdesc);
   const int32_t* first_reject = reinterpret_cast<const int32_t*>(p.ws + p.lay.first_reject);
   const int units_total = __ldcg(&h->units_total);
   const int small_after = units_total - 4 * kClaim * (int)gridDim.x;
@@ -139,11 +139,11 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
     return v;  // lane 0 only; broadcast when needed
   };
   auto describe = [&](int base, int want) {
-    int2 rd = make_int2(-1, 0);
+    int4 rd = make_int4(-1, 0, 0, 0);
     if (lane < want && base + lane < units_total) rd = __ldcg(&rowdesc[(base + lane) / p.nch]);
     return rd;
   };
-  auto check = [&](int2 rd) {  // first known rejection of the unit's request, or k
+  auto check = [&](int4 rd) {  // first known rejection of the unit's request, or k
     int fr = INT32_MAX;
     if (kVerify && p.early_exit && rd.x >= 0) {
       const int b = (rd.x >> 1) / p.k;
@@ -154,11 +154,11 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
 
   int wantC = want_at(0);
   int baseC = __shfl_sync(0xffffffffu, claim(wantC), 0);
-  int2 rdC = describe(baseC, wantC);
+  int4 rdC = describe(baseC, wantC);
   int frC = check(rdC);
   int wantB = want_at(baseC + wantC);
   int baseB = __shfl_sync(0xffffffffu, claim(wantB), 0);
-  int2 rdB = describe(baseB, wantB);
+  int4 rdB = describe(baseB, wantB);
   int wantA = want_at(baseB + wantB);
   int atomA = claim(wantA);
 
@@ -166,7 +166,7 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
     // Advance the look-ahead: skip flag for B, descriptors for A, a new claim.
     const int frB = check(rdB);
     const int baseA = __shfl_sync(0xffffffffu, atomA, 0);
-    const int2 rdA = describe(baseA, wantA);
+    const int4 rdA = describe(baseA, wantA);
     const int wantN = want_at(baseA + wantA);
     const int atomN = claim(wantN);
 
@@ -183,20 +183,12 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
       const int uu = baseC + l;
       const int slot = __shfl_sync(0xffffffffu, rdC.x, l);
       const float sc = __int_as_float(__shfl_sync(0xffffffffu, rdC.y, l));
+      const int lrow = __shfl_sync(0xffffffffu, rdC.z, l);
       if (lane == 0) {
-        const int row = uu / p.nch;
-        const int chunk = uu - row * p.nch;
-        const TIn* rowp;
-        if (kVerify) {
-          const int bi = slot >> 1;
-          const int b = bi / p.k;
-          const int i = bi - b * p.k;
-          rowp = (slot & 1)
-                     ? static_cast<const TIn*>(p.draft) + ((size_t)b * p.k + i) * (size_t)p.V
-                     : static_cast<const TIn*>(p.target) + ((size_t)b * (p.k + 1) + i) * (size_t)p.V;
-        } else {
-          rowp = static_cast<const TIn*>(p.target) + (size_t)slot * (size_t)p.V;
-        }
+        const int chunk = uu - (uu / p.nch) * p.nch;
+        // The descriptor's row is absolute within its buffer (target or draft).
+        const TIn* rowp = static_cast<const TIn*>((kVerify && (slot & 1)) ? p.draft : p.target) +
+                          (size_t)lrow * (size_t)p.V;
         const bool greedy = (sc == 0.0f);
         // Element range of the chunk and its 16-byte aligned core.
         const int e0 = chunk * p.chunk_elems;
@@ -309,7 +301,7 @@ template <typename TIn, bool kVerify>
 __device__ void sweep_producer_big(const SweepParams& p, SweepSmem& sm, WsHeader* h) {
   using Tr = ElemTraits<TIn>;
   if ((threadIdx.x & 31) != 0) return;
-  const int2* rowdesc = reinterpret_cast<const int2*>(p.ws + p.lay.rowdesc);
+  const int4* rowdesc = reinterpret_cast<const int4*>(p.ws + p.lay.rowdesc);
   const int32_t* first_reject = reinterpret_cast<const int32_t*>(p.ws + p.lay.first_reject);
   const int units_total = __ldcg(&h->units_total);
   volatile int* abort_flag = &sm.abort_flag;
@@ -328,30 +320,28 @@ __device__ void sweep_producer_big(const SweepParams& p, SweepSmem& sm, WsHeader
     return true;
   };
   auto describe = [&](int u) {
-    return u < units_total ? __ldcg(&rowdesc[u / p.nch]) : make_int2(-1, 0);
+    return u < units_total ? __ldcg(&rowdesc[u / p.nch]) : make_int4(-1, 0, 0, 0);
   };
 
   int nxt = atomicAdd(&h->work_next, 1);
-  int2 nrd = describe(nxt);
+  int4 nrd = describe(nxt);
   while (nxt < units_total) {
     const int uu = nxt;
-    const int2 rd = nrd;
+    const int4 rd = nrd;
     nxt = -1;
     bool described = false;
     const int slot = rd.x;
     const float sc = __int_as_float(rd.y);
     const int chunk = uu - (uu / p.nch) * p.nch;
-    const TIn* rowp;
     int ub = 0, ui = 0;
     if (kVerify) {
       const int bi = slot >> 1;
       ub = bi / p.k;
       ui = bi - ub * p.k;
-      rowp = (slot & 1) ? static_cast<const TIn*>(p.draft) + ((size_t)ub * p.k + ui) * (size_t)p.V
-                        : static_cast<const TIn*>(p.target) + ((size_t)ub * (p.k + 1) + ui) * (size_t)p.V;
-    } else {
-      rowp = static_cast<const TIn*>(p.target) + (size_t)slot * (size_t)p.V;
     }
+    // The descriptor's row is absolute within its buffer (target or draft).
+    const TIn* rowp = static_cast<const TIn*>((kVerify && (slot & 1)) ? p.draft : p.target) +
+                      (size_t)rd.z * (size_t)p.V;
     const bool greedy = (sc == 0.0f);
     // Element range of the chunk and its 16-byte aligned core.
     const int e0 = chunk * p.chunk_elems;
@@ -545,8 +535,8 @@ __device__ __forceinline__ void arg_stage(ArgAcc& a, const uint4 (&v)[kVecPerThr
 // ---------------------------------------------------------------------------
 // Decision for (b, i) once all of its chunks are in (warp-cooperative).
 // ---------------------------------------------------------------------------
-// x and u (token x_i and uniform u_i) were loaded one unit earlier, when
-// the chunk count was taken.  With dry set, the partials come from the
+// x, u and rb (token x_i, uniform u_i and the request's first target and
+// draft rows) were loaded one unit earlier, when the chunk count was taken.  With dry set, the partials come from the
 // workspace's made-up position and nothing is recorded: the call only brings
 // this code into the instruction cache while memory is still quiet (its first
 // real use comes when the sweep has HBM saturated, where every instruction
@@ -554,7 +544,7 @@ __device__ __forceinline__ void arg_stage(ArgAcc& a, const uint4 (&v)[kVecPerThr
 // the same code.
 template <typename TIn>
 __device__ __noinline__ void decide_position(const SweepParams& p, int bi, bool greedy, float sc,
-                                             int x, float u_i, bool dry) {
+                                             int x, float u_i, int2 rb, bool dry) {
   const int lane = threadIdx.x & 31;
   const int b = bi / p.k;
   const int i = bi - b * p.k;
@@ -578,10 +568,13 @@ __device__ __noinline__ void decide_position(const SweepParams& p, int bi, bool 
   } else {
     // The gathers of z_t[x] and z_d[x] go out first and overlap the partial
     // loads.  Target chunks then draft chunks: the two slots are adjacent.
-    const float zt = ElemTraits<TIn>::load(
-        static_cast<const TIn*>(p.target) + ((size_t)b * (p.k + 1) + i) * (size_t)p.V, x);
-    const float zd = ElemTraits<TIn>::load(
-        static_cast<const TIn*>(p.draft) + ((size_t)b * p.k + i) * (size_t)p.V, x);
+    // The dry run gathers from the workspace instead, which always exists.
+    const TIn* trow = dry ? reinterpret_cast<const TIn*>(p.ws + p.lay.warm)
+                          : static_cast<const TIn*>(p.target) + ((size_t)rb.x + i) * (size_t)p.V;
+    const TIn* drow = dry ? reinterpret_cast<const TIn*>(p.ws + p.lay.warm)
+                          : static_cast<const TIn*>(p.draft) + ((size_t)rb.y + i) * (size_t)p.V;
+    const float zt = ElemTraits<TIn>::load(trow, x);
+    const float zd = ElemTraits<TIn>::load(drow, x);
     FF ct, cd;
     bool okt, okd;
     pair_log2_normalisers(pt, p.nch, sc, &ct, &cd, &okt, &okd, &late);
@@ -736,17 +729,18 @@ __device__ void sweep_bookkeeper(const SweepParams& p, SweepSmem& sm, WsHeader* 
   int pend_bi = -1, pend_old = 0, pend_need = 0, pend_x = 0;
   bool pend_greedy = false;
   float pend_sc = 0.0f, pend_u = 0.0f;
+  int2 pend_rb = make_int2(0, 0);
   if (kVerify) {
     // Run both decision paths once, without effect, while the first units
     // are still streaming in (see decide_position).
-    decide_position<TIn>(p, 0, false, 1.0f, 0, 0.5f, true);
-    decide_position<TIn>(p, 0, true, 0.0f, 0, 0.5f, true);
+    decide_position<TIn>(p, 0, false, 1.0f, 0, 0.5f, make_int2(0, 0), true);
+    decide_position<TIn>(p, 0, true, 0.0f, 0, 0.5f, make_int2(0, 0), true);
   }
   auto resolve_pending = [&]() {
     if (!kVerify || pend_bi < 0) return;
     const int old = __shfl_sync(0xffffffffu, pend_old, 0);
     if (old == pend_need - 1)
-      decide_position<TIn>(p, pend_bi, pend_greedy, pend_sc, pend_x, pend_u, false);
+      decide_position<TIn>(p, pend_bi, pend_greedy, pend_sc, pend_x, pend_u, pend_rb, false);
     pend_bi = -1;
   };
   for (int u = 0;; ++u) {
@@ -813,6 +807,7 @@ __device__ void sweep_bookkeeper(const SweepParams& p, SweepSmem& sm, WsHeader* 
       const int pi = pend_bi - pb * p.k;
       pend_x = __ldg(&p.tokens[(size_t)pb * p.k + pi]);
       pend_u = __ldg(&p.uniforms[(size_t)pb * (p.k + 1) + pi]);
+      pend_rb = __ldcg(reinterpret_cast<const int2*>(p.ws + p.lay.rowbase) + pb);
     }
   }
 }

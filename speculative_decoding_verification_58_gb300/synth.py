@@ -198,3 +198,43 @@ def make_workload(name: str, seed: int | None = None, threads: int | None = None
         cfg["seed"] = seed
     return make_inputs(cfg["recipe"], cfg["B"], cfg["k"], cfg["V"], cfg["dtype"], cfg["seed"],
                        threads=threads)
+
+
+@dataclass
+class PackedRows:
+    """A batch laid out as the packed C-ABI entry takes it (row buffers + first rows)."""
+
+    target_rows: np.ndarray       # [rows_t, V] same dtype as SpecInputs.target
+    draft_rows: np.ndarray        # [rows_d, V]
+    target_row_start: np.ndarray  # [B] int32
+    draft_row_start: np.ndarray   # [B] int32
+
+
+def pack_rows(inp: SpecInputs, order=None, gap: int = 0) -> PackedRows:
+    """Copy each request's rows into flat buffers, requests in ``order``.
+
+    Request b contributes its target rows 0..L_b and draft rows 0..L_b-1 (a
+    verification batch of total length sum_b L_b, AdaFlash Section 3.3).
+    ``gap`` rows of filler (copies of row 0 of the batch) go after every request, so
+    that placements need not be contiguous.  Only copies rows: no arithmetic.
+    """
+    B = inp.B
+    order = np.arange(B) if order is None else np.asarray(order)
+    t_start = np.zeros(B, np.int32)
+    d_start = np.zeros(B, np.int32)
+    trows, drows = [], []
+    nt = nd = 0
+    for b in order:
+        L = int(inp.lengths[b])
+        t_start[b], d_start[b] = nt, nd
+        trows.append(inp.target[b, :L + 1])
+        drows.append(inp.draft[b, :L])
+        nt += L + 1
+        nd += L
+        if gap:
+            trows.append(np.repeat(inp.target[0, :1], gap, axis=0))
+            drows.append(np.repeat(inp.target[0, :1], gap, axis=0))
+            nt += gap
+            nd += gap
+    return PackedRows(np.ascontiguousarray(np.concatenate(trows)),
+                      np.ascontiguousarray(np.concatenate(drows)), t_start, d_start)
