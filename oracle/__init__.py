@@ -62,6 +62,10 @@ def _load():
     lib.oracle_row_stats.argtypes = [vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int, f32p,
                                      f64p, f64p, i32p]
     lib.oracle_row_stats.restype = None
+    lib.oracle_opd_stats.argtypes = [vp, vp, ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_double, ctypes.c_double, i32p, f64p,
+                                     f64p, f64p, f64p]
+    lib.oracle_opd_stats.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -189,3 +193,40 @@ def verify_packed(target_rows, draft_rows, target_row_start, draft_row_start, dr
             res.out_tokens[b] = -1
             res.bad_requests += 1
     return res
+
+
+@dataclass
+class OpdResult:
+    x_star: np.ndarray    # int32 [B, k]: argmax of p per position, -1 past L_b
+    hard: np.ndarray      # float64 [B, k]: -log q(x_star)
+    rkl: np.ndarray       # float64 [B, k]: sum_y q log(q/p)
+    rkl_clip: np.ndarray  # float64 [B, k]: sum_y min(q log(q/p), delta)
+    loss: np.ndarray      # float64 [B]: alpha * mean hard + (1 - alpha) * mean rkl_clip
+    bad_requests: int
+
+
+def opd_stats(target_logits, draft_logits, lengths, delta=0.01, alpha=0.8) -> OpdResult:
+    """OPD supervision statistics per verified position (AdaFlash Section 3.1).
+
+    Same buffers as ``verify``: target [B, k+1, V], draft [B, k, V]; positions
+    i < lengths[b].  Defaults are the paper's delta = 0.01 and alpha = 0.8.
+    """
+    tl, dt = _logits(target_logits)
+    dl, dt2 = _logits(draft_logits)
+    if dt != dt2:
+        raise TypeError("target and draft logits must have the same dtype")
+    B, k1, V = tl.shape
+    k = k1 - 1
+    if dl.shape != (B, k, V):
+        raise ValueError(f"draft logits shape {dl.shape} != {(B, k, V)}")
+    lens = np.ascontiguousarray(lengths, dtype=np.int32).reshape(B)
+    xs = np.empty((B, k), np.int32)
+    hard = np.empty((B, k), np.float64)
+    rkl = np.empty((B, k), np.float64)
+    clip = np.empty((B, k), np.float64)
+    loss = np.empty(B, np.float64)
+    bad = _load().oracle_opd_stats(tl.ctypes.data, dl.ctypes.data, dt, _ptr(lens, ctypes.c_int32),
+                                   B, k, V, float(delta), float(alpha), _ptr(xs, ctypes.c_int32),
+                                   _ptr(hard, ctypes.c_double), _ptr(rkl, ctypes.c_double),
+                                   _ptr(clip, ctypes.c_double), _ptr(loss, ctypes.c_double))
+    return OpdResult(xs, hard, rkl, clip, loss, int(bad))

@@ -289,3 +289,56 @@ extern "C" void oracle_row_stats(const void* logits, int dtype, int64_t rows, in
     }
   }
 }
+
+// ---------------------------------------------------------------------------
+// OPD supervision statistics (AdaFlash Section 3.1), one position at a time:
+// both softmaxes at temperature 1 in double, then the three sums in index
+// order exactly as the formulas are written.
+// ---------------------------------------------------------------------------
+extern "C" int oracle_opd_stats(const void* target_logits, const void* draft_logits, int dtype,
+                                const int32_t* lengths, int B, int k, int V, double delta,
+                                double alpha, int32_t* x_star, double* hard, double* rkl,
+                                double* rkl_clip, double* loss) {
+  int bad = 0;
+  for (int b = 0; b < B; ++b) {
+    const int L = lengths[b];
+    const bool ok_len = L >= 1 && L <= k;
+    if (!ok_len) ++bad;
+    double sum_hard = 0.0, sum_clip = 0.0;
+    for (int i = 0; i < k; ++i) {
+      const size_t o = (size_t)b * k + i;
+      x_star[o] = -1;
+      hard[o] = rkl[o] = rkl_clip[o] = kNaN;
+      if (!ok_len || i >= L) continue;
+      Row t{target_logits, dtype, ((size_t)b * (k + 1) + i) * (size_t)V, V};
+      Row d{draft_logits, dtype, ((size_t)b * k + i) * (size_t)V, V};
+      Softmax sp = row_softmax(t, 1.0), sq = row_softmax(d, 1.0);
+      double mt;
+      int arg;
+      row_argmax(t, &mt, &arg);
+      if (!sp.ok || !sq.ok) {
+        sum_hard = sum_clip = kNaN;
+        continue;
+      }
+      x_star[o] = arg;
+      hard[o] = -log_prob(d, sq, 1.0, arg);
+      double kl = 0.0, kl_clip = 0.0;
+      for (int y = 0; y < V; ++y) {
+        const double q = prob(d, sq, 1.0, y);
+        const double p = prob(t, sp, 1.0, y);
+        double term;
+        if (q == 0.0) term = 0.0;          // 0 log 0 = 0
+        else if (p == 0.0) term = kInf;    // mass where the target has none
+        else term = q * std::log(q / p);
+        kl += term;
+        kl_clip += std::fmin(term, delta);
+      }
+      rkl[o] = kl;
+      rkl_clip[o] = kl_clip;
+      sum_hard += hard[o];
+      sum_clip += kl_clip;
+    }
+    loss[b] = ok_len ? alpha * (sum_hard / L) + (1.0 - alpha) * (sum_clip / L) : kNaN;
+  }
+  return bad;
+}

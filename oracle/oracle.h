@@ -103,6 +103,31 @@ void oracle_row_stats(const void* logits, int dtype, int64_t rows, int V,
                       const float* temperature_per_row,
                       double* row_max, double* row_lse, int32_t* row_arg);
 
+/*
+ * On-policy distillation (OPD) supervision statistics, AdaFlash Section 3.1
+ * ("Mixture OPD Loss with Reverse-KL" and "Entry-wise Divergence Clipping"),
+ * worked through in the AdaFlash reading notes' numerical example for one
+ * toy position.  For request b and every verified position i < L_b, with
+ * p = softmax(target row i) and q = softmax(draft row i) (the models' own
+ * distributions, temperature 1):
+ *   x_star[b][i]   = argmax_y p(y)              (lowest index on ties)
+ *   hard[b][i]     = -log q(x_star)             (hard-label cross-entropy term)
+ *   rkl[b][i]      = sum_y q(y) log(q(y)/p(y))  (reverse KL, unclipped)
+ *   rkl_clip[b][i] = sum_y min{ q(y) log(q(y)/p(y)), delta }
+ *   loss[b]        = alpha * mean_{i<L_b} hard + (1 - alpha) * mean_{i<L_b} rkl_clip
+ * Readings: 0 log 0 = 0 (an entry with q = 0 adds nothing); an entry with
+ * q > 0 and p = 0 adds +inf (so delta after clipping); the pages average over
+ * the k positions of a block, and with per-request lengths the average runs
+ * over the L_b positions that were verified.  Positions i >= L_b get
+ * x_star = -1 and NaN.  An invalid length makes the whole request NaN / -1;
+ * a row without finite mass makes its position (and the loss) NaN.
+ * Returns the number of requests with an invalid length.
+ */
+int oracle_opd_stats(const void* target_logits, const void* draft_logits, int dtype,
+                     const int32_t* lengths, int B, int k, int V, double delta, double alpha,
+                     int32_t* x_star, double* hard, double* rkl, double* rkl_clip,
+                     double* loss);
+
 #ifdef __cplusplus
 }
 #endif

@@ -464,3 +464,91 @@ def test_subnormal_temperature_is_invalid():
                       np.zeros((1, k), np.int32), np.array([1], np.int32),
                       np.zeros((1, k + 1), np.float32), np.array([1e-39], np.float32))
     assert r.num_accepted[0] == -1
+
+
+# ---------------------------------------------------------------------------
+# OPD supervision statistics (AdaFlash Section 3.1)
+# ---------------------------------------------------------------------------
+
+def _opd_one(p, q, delta, alpha, dtype=np.float64):
+    """One position whose softmaxes are p and q: logits log p, log q (float32)."""
+    V = len(p)
+    t = np.zeros((1, 2, V), np.float32)
+    d = np.zeros((1, 1, V), np.float32)
+    with np.errstate(divide="ignore"):
+        t[0, 0] = np.log(np.asarray(p, dtype))
+        d[0, 0] = np.log(np.asarray(q, dtype))
+    return oracle.opd_stats(t, d, np.array([1], np.int32), delta=delta, alpha=alpha)
+
+
+def test_opd_worked_example_of_the_notes():
+    g = json.load(open(os.path.join(GOLDEN, "opd_worked_example.json")))
+    tol = g["printed_tolerance"]
+    r = _opd_one(g["p_target"], g["q_draft"], g["delta"], g["alpha"])
+    assert r.x_star[0, 0] == g["printed"]["x_star"]
+    assert abs(r.hard[0, 0] - g["printed"]["hard"]) < tol
+    assert abs(r.rkl[0, 0] - g["printed"]["rkl"]) < tol
+    entries = g["printed"]["rkl_entries"]
+    # Clipped at delta = 0.01: the negative entry stays, the three others become delta.
+    assert abs(r.rkl_clip[0, 0] - (entries[0] + 3 * g["delta"])) < tol
+    unclipped = _opd_one(g["p_target"], g["q_draft"], 1e300, g["alpha"])
+    assert abs(unclipped.loss[0] - g["printed"]["opd_unclipped"]) < tol
+    assert abs(r.loss[0] - (g["alpha"] * r.hard[0, 0] + (1 - g["alpha"]) * r.rkl_clip[0, 0])) < 1e-12
+
+
+def test_opd_reverse_kl_matches_scipy_entropy_and_gibbs():
+    stats = pytest.importorskip("scipy.stats")
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(7)
+    B, k, V = 3, 4, 333
+    t = (rng.standard_normal((B, k + 1, V)) * 2).astype(np.float32)
+    d = (t[:, :k] + rng.standard_normal((B, k, V))).astype(np.float32)
+    lens = np.array([4, 1, 3], np.int32)
+    r = oracle.opd_stats(t, d, lens, delta=0.05, alpha=0.3)
+    for b in range(B):
+        for i in range(k):
+            if i >= lens[b]:
+                assert r.x_star[b, i] == -1 and np.isnan(r.hard[b, i]) and np.isnan(r.rkl[b, i])
+                continue
+            p = special.softmax(t[b, i].astype(np.float64))
+            q = special.softmax(d[b, i].astype(np.float64))
+            assert abs(r.rkl[b, i] - stats.entropy(q, p)) < 1e-12 * max(1, stats.entropy(q, p))
+            assert r.rkl[b, i] >= 0                               # Gibbs' inequality
+            assert r.rkl_clip[b, i] <= r.rkl[b, i] + 1e-15        # clipping only lowers
+            assert r.x_star[b, i] == int(np.argmax(t[b, i]))
+            ce = special.logsumexp(d[b, i].astype(np.float64)) - float(d[b, i, r.x_star[b, i]])
+            assert abs(r.hard[b, i] - ce) < 1e-12 * max(1, ce)
+        L = lens[b]
+        mix = 0.3 * r.hard[b, :L].mean() + 0.7 * r.rkl_clip[b, :L].mean()
+        assert abs(r.loss[b] - mix) < 1e-12
+    # A threshold above every entry clips nothing; alpha 1 and 0 pick one term.
+    big = oracle.opd_stats(t, d, lens, delta=1e300, alpha=0.0)
+    np.testing.assert_allclose(big.rkl_clip, big.rkl, rtol=0, atol=0)
+    one = oracle.opd_stats(t, d, lens, delta=0.05, alpha=1.0)
+    for b in range(B):
+        assert abs(one.loss[b] - r.hard[b, :lens[b]].mean()) < 1e-12
+
+
+def test_opd_special_cases():
+    # p == q: no divergence anywhere; the hard term is the drafter's cross-entropy on its own mode.
+    p = np.array([0.1, 0.6, 0.2, 0.1])
+    r = _opd_one(p, p, 0.01, 0.8)
+    assert abs(r.rkl[0, 0]) < 1e-12 and abs(r.rkl_clip[0, 0]) < 1e-12
+    assert r.x_star[0, 0] == 1 and abs(r.hard[0, 0] + np.log(0.6)) < 1e-6
+    # Argmax ties go to the lowest index.
+    r = _opd_one([0.4, 0.1, 0.4, 0.1], [0.25] * 4, 0.01, 0.8)
+    assert r.x_star[0, 0] == 0
+    # q = 0 entries add nothing (0 log 0 = 0); q > 0 where p = 0 is an infinite entry, clipped to delta.
+    r = _opd_one([0.5, 0.5, 0.0], [0.5, 0.5, 0.0], 0.01, 0.8)
+    assert abs(r.rkl[0, 0]) < 1e-12
+    r = _opd_one([0.5, 0.5, 0.0], [0.4, 0.4, 0.2], 0.01, 0.8)
+    assert r.rkl[0, 0] == np.inf
+    want = 2 * 0.4 * np.log(0.4 / 0.5) + 0.01
+    assert abs(r.rkl_clip[0, 0] - want) < 1e-6
+    # An invalid length makes the request NaN; a row without finite mass, its position.
+    t = np.zeros((2, 3, 5), np.float32)
+    d = np.zeros((2, 2, 5), np.float32)
+    d[1, 0] = np.nan
+    r = oracle.opd_stats(t, d, np.array([3, 2], np.int32))
+    assert r.bad_requests == 1 and np.isnan(r.loss[0]) and np.all(r.x_star[0] == -1)
+    assert np.isnan(r.hard[1, 0]) and np.isnan(r.loss[1]) and r.x_star[1, 1] == 0
