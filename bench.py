@@ -51,6 +51,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-full-sweep", action="store_true")
     ap.add_argument("--no-packed", action="store_true")
+    ap.add_argument("--no-opd", action="store_true")
     return ap.parse_args()
 
 
@@ -377,6 +378,30 @@ def run_ours(args, world, rank, local):
         del rows, pargs
         torch.cuda.empty_cache()
 
+    # OPD supervision statistics (AdaFlash Section 3.1) on the same buffers:
+    # both rows of every verified position read once.
+    opd = None
+    if not args.no_opd:
+        st = sv.spec_opd_stats(d["target_logits"], d["draft_logits"], d["lengths"], stream=stream)
+        for _ in range(3):
+            sv.spec_opd_stats(d["target_logits"], d["draft_logits"], d["lengths"], out=st,
+                              stream=stream)
+        torch.cuda.synchronize(dev)
+        o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        oreps = max(10, min(args.steps, 100))
+        o0.record(stream)
+        for _ in range(oreps):
+            sv.spec_opd_stats(d["target_logits"], d["draft_logits"], d["lengths"], out=st,
+                              stream=stream)
+        o1.record(stream)
+        torch.cuda.synchronize(dev)
+        oms = o0.elapsed_time(o1) / oreps
+        positions = int(inp.lengths.sum())
+        obytes = positions * 2 * inp.V * esize
+        opd = {"ms_per_call": oms, "positions": positions, "positions_per_s": positions / (oms * 1e-3),
+               "bytes_per_call": obytes, "gbs": obytes / (oms * 1e-3) / 1e9,
+               "loss_mean": float(st.loss.float().mean().item())}
+
     # End to end through the public API: pinned host inputs in, results out, every step.
     import numpy as _np
     host = {}
@@ -448,6 +473,9 @@ def run_ours(args, world, rank, local):
         result["full_sweep"] = full
     if packed is not None:
         result["packed"] = packed
+    if opd is not None:
+        opd["frac"] = opd["gbs"] / hbm_peak
+        result["opd"] = opd
 
     if world == 1 and not args.no_cpu_baseline:
         import oracle

@@ -264,6 +264,36 @@ spec_status_t spec_row_stats(const void* logits, spec_dtype_t dtype, int rows, i
                              int32_t* row_arg, void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/*
+ * On-policy distillation (OPD) supervision statistics over the same batch
+ * buffers as spec_verify (AdaFlash Section 3.1, "Mixture OPD Loss with
+ * Reverse-KL" and "Entry-wise Divergence Clipping"; the AdaFlash reading
+ * notes work one toy position through).  For every request b and verified
+ * position i < L_b, with p = softmax(target row i) and q = softmax(draft row
+ * i) at temperature 1 (the models' own distributions):
+ *
+ *   x_star   [B, k] int32 out: argmax_y p(y), lowest index on ties
+ *   hard     [B, k] float out: -log q(x_star)                (hard-label term)
+ *   rkl      [B, k] float out: sum_y q(y) log(q(y)/p(y))     (reverse KL)
+ *   rkl_clip [B, k] float out: sum_y min{q(y) log(q(y)/p(y)), delta}
+ *   loss     [B]    float out: alpha * mean_{i<L_b} hard + (1 - alpha) * mean_{i<L_b} rkl_clip
+ *
+ * target_logits [B, k+1, V] and draft_logits [B, k, V] (dtype) and lengths
+ * [B] (int32 in [1, k]) are device buffers as for spec_verify.  An entry
+ * with q = 0 adds nothing (0 log 0 = 0); one with q > 0 where p = 0 adds
+ * +inf to rkl and delta to rkl_clip.  Positions i >= L_b get x_star = -1 and
+ * NaN; an invalid L_b makes the whole request -1 / NaN (loss NaN); a row
+ * without finite mass (NaN, +inf, all -inf) makes its position NaN.
+ * delta must be finite and > 0 (the paper uses 0.01), alpha in [0, 1] (0.8).
+ * Needs no workspace.  Every logit is used twice (normalisers first, then the
+ * sums); the second read is arranged to come from L2.  Asynchronous on
+ * `stream`; returns SPEC_OK once enqueued.
+ */
+spec_status_t spec_opd_stats(const void* target_logits, const void* draft_logits,
+                             spec_dtype_t dtype, const int32_t* lengths, int B, int k, int V,
+                             float delta, float alpha, int32_t* x_star, float* hard, float* rkl,
+                             float* rkl_clip, float* loss, void* stream);
+
 /* Static description of a status code. */
 const char* spec_status_string(spec_status_t status);
 

@@ -16,6 +16,7 @@ The functions keep the C names:
 ``spec_verify_report(ws)``           what the device recorded for the last call
 ``spec_verify_device_status(ws)``    just the recorded status
 ``spec_row_stats(...)``              the row sweep alone: max, logsumexp, argmax
+``spec_opd_stats(...)``              OPD supervision statistics (hard label, reverse KL, clipped)
 ``spec_status_string(code)``
 """
 
@@ -44,7 +45,7 @@ SPEC_FLAG_FULL_SWEEP = 1
 EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_ex", "spec_verify_timed",
            "spec_verify_packed", "spec_verify_report",
            "spec_verify_device_status", "spec_row_stats_workspace_bytes", "spec_row_stats",
-           "spec_status_string", "spec_abi_version", "spec_verify_static")
+           "spec_status_string", "spec_abi_version", "spec_verify_static", "spec_opd_stats")
 SPEC_STATIC_SCRATCH_BYTES = 8 << 20
 
 
@@ -114,6 +115,9 @@ def lib() -> ctypes.CDLL:
     L.spec_row_stats_workspace_bytes.restype = csz
     L.spec_row_stats.argtypes = [vp, ci, ci, ci, f32p, f32p, f32p, i32p, vp, csz, vp]
     L.spec_row_stats.restype = ci
+    L.spec_opd_stats.argtypes = [vp, vp, ci, i32p, ci, ci, ci, ctypes.c_float, ctypes.c_float,
+                                 i32p, f32p, f32p, f32p, f32p, vp]
+    L.spec_opd_stats.restype = ci
     L.spec_status_string.argtypes = [ci]
     L.spec_status_string.restype = ctypes.c_char_p
     L.spec_abi_version.argtypes = []
@@ -422,6 +426,48 @@ def to_device_packed(packed, device="cuda"):
                 draft_rows=_logits_to_device(packed.draft_rows, device),
                 target_row_start=torch.from_numpy(packed.target_row_start).to(device),
                 draft_row_start=torch.from_numpy(packed.draft_row_start).to(device))
+
+
+@dataclass
+class OpdStats:
+    x_star: object    # int32 [B, k]
+    hard: object      # float32 [B, k]
+    rkl: object       # float32 [B, k]
+    rkl_clip: object  # float32 [B, k]
+    loss: object      # float32 [B]
+
+
+def spec_opd_stats(target_logits, draft_logits, lengths, *, delta: float = 0.01,
+                   alpha: float = 0.8, out=None, stream=None) -> OpdStats:
+    """OPD supervision statistics (AdaFlash Section 3.1) on the verification buffers.
+
+    target [B, k+1, V], draft [B, k, V] (float32 or bfloat16), lengths int32 [B].
+    Per verified position: target argmax, -log q(argmax), reverse KL and its
+    entry-wise clipped form; per request the alpha mixture loss.  ``out`` may
+    be an ``OpdStats`` of preallocated tensors.
+    """
+    torch = _torch()
+    B, k1, V = target_logits.shape
+    k = k1 - 1
+    dev = target_logits.device
+    dt = _dtype_code(target_logits)
+    _need(target_logits, "target_logits", target_logits.dtype, (B, k + 1, V), dev)
+    _need(draft_logits, "draft_logits", target_logits.dtype, (B, k, V), dev)
+    _need(lengths, "lengths", torch.int32, (B,), dev)
+    if out is None:
+        f = dict(dtype=torch.float32, device=dev)
+        out = OpdStats(torch.empty((B, k), dtype=torch.int32, device=dev), torch.empty((B, k), **f),
+                       torch.empty((B, k), **f), torch.empty((B, k), **f), torch.empty(B, **f))
+    _need(out.x_star, "x_star", torch.int32, (B, k), dev)
+    for name in ("hard", "rkl", "rkl_clip"):
+        _need(getattr(out, name), name, torch.float32, (B, k), dev)
+    _need(out.loss, "loss", torch.float32, (B,), dev)
+    _check(lib().spec_opd_stats(target_logits.data_ptr(), draft_logits.data_ptr(), dt,
+                                lengths.data_ptr(), B, k, V, float(delta), float(alpha),
+                                out.x_star.data_ptr(), out.hard.data_ptr(), out.rkl.data_ptr(),
+                                out.rkl_clip.data_ptr(), out.loss.data_ptr(), _stream_ptr(stream)),
+           "spec_opd_stats")
+    return out
 
 
 def to_device(inputs, device="cuda"):

@@ -141,6 +141,7 @@ struct ElemTraits<float> {
   static constexpr int kSize = 4;
   static constexpr int kPerVec = 4;  // elements per 16-byte vector
   static __device__ __forceinline__ float load(const float* p, long long i) { return __ldg(p + i); }
+  static __device__ __forceinline__ float to_float(float x) { return x; }
   static __device__ __forceinline__ void unpack(const uint4& v, float* x) {
     x[0] = __uint_as_float(v.x);
     x[1] = __uint_as_float(v.y);
@@ -155,6 +156,7 @@ struct ElemTraits<uint16_t> {
   static __device__ __forceinline__ float load(const uint16_t* p, long long i) {
     return bf16_to_f32(__ldg(p + i));
   }
+  static __device__ __forceinline__ float to_float(uint16_t x) { return bf16_to_f32(x); }
   static __device__ __forceinline__ void unpack(const uint4& v, float* x) {
     x[0] = __uint_as_float(v.x << 16);
     x[1] = __uint_as_float(v.x & 0xffff0000u);
@@ -247,6 +249,16 @@ __device__ __forceinline__ float2 f32x2_add(float2 a, float2 b) {
   asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
       "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
       "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 f32x2_mul(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
       : "=f"(d.x), "=f"(d.y)
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;

@@ -11,6 +11,7 @@
 
 #include "common.cuh"
 #include "final.cuh"
+#include "opd.cuh"
 #include "plan.cuh"
 #include "sweep.cuh"
 
@@ -99,6 +100,8 @@ struct DeviceInfo {
   int sms = 0;
   int sweep_blocks_per_sm[2][2] = {{0, 0}, {0, 0}};  // [dtype][verify]
   size_t final_smem_optin = 0;
+  bool opd_ready = false;
+  int opd_clusters[2][4] = {};  // [dtype][cluster size - 1]: co-resident OPD clusters
 };
 
 constexpr int kMaxDevices = 64;
@@ -331,6 +334,92 @@ spec_status_t row_stats_typed(const void* logits, int rows, int V, const float* 
 
 size_t row_stats_ws_bytes(int rows, int V) { return stats_layout(rows, chunks_per_row(rows, V)).total; }
 
+// ---------------------------------------------------------------------------
+// OPD statistics: cluster shape and launch.
+// ---------------------------------------------------------------------------
+// Clusters of four CTAs (each a quarter of the vocabulary) for large rows,
+// two for medium ones, single CTAs for small vocabularies.
+int opd_cluster_size(int V) { return V >= 65536 ? 4 : (V > 16384 ? 2 : 1); }
+
+template <typename TIn>
+cudaError_t opd_prepare() {
+  return cudaFuncSetAttribute(opd_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)sizeof(OpdSmem));
+}
+
+template <typename TIn>
+cudaError_t opd_max_clusters(int cs, int* out) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs * 64);
+  cfg.blockDim = dim3(kOpdThreads);
+  cfg.dynamicSmemBytes = sizeof(OpdSmem);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(out, opd_kernel<TIn>, &cfg);
+}
+
+template <typename TIn>
+spec_status_t opd_typed(const void* target, const void* draft, const int32_t* lengths, int B,
+                        int k, int V, float delta, float alpha, int32_t* x_star, float* hard,
+                        float* rkl, float* rkl_clip, float* loss, cudaStream_t stream,
+                        int dtype_index, bool vec_ok) {
+  DeviceInfo* d = nullptr;
+  if (device_info(&d) != cudaSuccess) return SPEC_ERR_CUDA;
+  const int cs = opd_cluster_size(V);
+  int* slot = &d->opd_clusters[dtype_index][cs - 1];
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (!d->opd_ready) {
+      if (opd_prepare<float>() != cudaSuccess || opd_prepare<uint16_t>() != cudaSuccess)
+        return SPEC_ERR_CUDA;
+      d->opd_ready = true;
+    }
+    if (*slot == 0) {
+      int n = 0;
+      if (opd_max_clusters<TIn>(cs, &n) != cudaSuccess || n < 1) return SPEC_ERR_CUDA;
+      *slot = n;
+    }
+  }
+  const long long clusters = std::min<long long>((long long)B * k, *slot);
+  OpdParams op;
+  op.target = target;
+  op.draft = draft;
+  op.lengths = lengths;
+  op.B = B;
+  op.k = k;
+  op.V = V;
+  op.slice = (((V + cs - 1) / cs) + 7) & ~7;
+  op.vec_ok = vec_ok ? 1 : 0;
+  op.delta = delta;
+  op.x_star = x_star;
+  op.hard = hard;
+  op.rkl = rkl;
+  op.rkl_clip = rkl_clip;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(clusters * cs));
+  cfg.blockDim = dim3(kOpdThreads);
+  cfg.dynamicSmemBytes = sizeof(OpdSmem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, opd_kernel<TIn>, op) != cudaSuccess) return SPEC_ERR_CUDA;
+  const int wpb = 8;
+  if (launch(opd_loss_kernel, dim3((B + wpb - 1) / wpb), dim3(wpb * 32), 0, stream, true, lengths,
+             (const float*)hard, (const float*)rkl_clip, B, k, alpha, loss) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
 }  // namespace specv
 
 using namespace specv;
@@ -479,6 +568,34 @@ spec_status_t spec_verify_device_status(const void* workspace, void* stream) {
   spec_status_t st = spec_verify_report(workspace, stream, &r);
   if (st != SPEC_OK) return st;
   return (spec_status_t)r.status;
+}
+
+spec_status_t spec_opd_stats(const void* target_logits, const void* draft_logits,
+                             spec_dtype_t dtype, const int32_t* lengths, int B, int k, int V,
+                             float delta, float alpha, int32_t* x_star, float* hard, float* rkl,
+                             float* rkl_clip, float* loss, void* stream) {
+  if (B < 1 || k < 1 || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (!sizes_ok(B, k, V)) return SPEC_ERR_UNSUPPORTED;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (!(delta > 0.0f && delta <= FLT_MAX) || !(alpha >= 0.0f && alpha <= 1.0f))
+    return SPEC_ERR_INVALID_ARG;
+  if (!target_logits || !draft_logits || !lengths || !x_star || !hard || !rkl || !rkl_clip ||
+      !loss)
+    return SPEC_ERR_INVALID_ARG;
+  const size_t esize = dtype == SPEC_F32 ? 4 : 2;
+  if (!aligned(target_logits, esize) || !aligned(draft_logits, esize) || !aligned(lengths, 4) ||
+      !aligned(x_star, 4) || !aligned(hard, 4) || !aligned(rkl, 4) || !aligned(rkl_clip, 4) ||
+      !aligned(loss, 4))
+    return SPEC_ERR_INVALID_ARG;
+  const bool vec_ok = aligned(target_logits, 16) && aligned(draft_logits, 16) &&
+                      ((size_t)V * esize) % 16 == 0;
+  if (use_device_of(target_logits) != cudaSuccess) return SPEC_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == SPEC_F32)
+    return opd_typed<float>(target_logits, draft_logits, lengths, B, k, V, delta, alpha, x_star,
+                            hard, rkl, rkl_clip, loss, s, 0, vec_ok);
+  return opd_typed<uint16_t>(target_logits, draft_logits, lengths, B, k, V, delta, alpha, x_star,
+                             hard, rkl, rkl_clip, loss, s, 1, vec_ok);
 }
 
 size_t spec_row_stats_workspace_bytes(int rows, int V) {
