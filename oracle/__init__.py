@@ -66,6 +66,9 @@ def _load():
                                      ctypes.c_int, ctypes.c_double, ctypes.c_double, i32p, f64p,
                                      f64p, f64p, f64p]
     lib.oracle_opd_stats.restype = ctypes.c_int
+    lib.oracle_d3d_select.argtypes = [i32p, i32p, i32p, i32p, i32p, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, i32p, i32p]
+    lib.oracle_d3d_select.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -230,3 +233,25 @@ def opd_stats(target_logits, draft_logits, lengths, delta=0.01, alpha=0.8) -> Op
                                    _ptr(hard, ctypes.c_double), _ptr(rkl, ctypes.c_double),
                                    _ptr(clip, ctypes.c_double), _ptr(loss, ctypes.c_double))
     return OpdResult(xs, hard, rkl, clip, loss, int(bad))
+
+
+def d3d_select(num_accepted, out_tokens, branch_pos, branch_tok, branch_block):
+    """D3D branch selection (D3D paper, Methodology, asynchronous inference).
+
+    Returns (hit [B] int32: matching branch index or -1, next_block [B, blk]
+    int32: that branch's block or -1s, hits: number of requests that hit).
+    """
+    n = np.ascontiguousarray(num_accepted, dtype=np.int32)
+    out = np.ascontiguousarray(out_tokens, dtype=np.int32)
+    pos = np.ascontiguousarray(branch_pos, dtype=np.int32)
+    tok = np.ascontiguousarray(branch_tok, dtype=np.int32)
+    blocks = np.ascontiguousarray(branch_block, dtype=np.int32)
+    B, k1 = out.shape
+    NB, blk = blocks.shape[1], blocks.shape[2]
+    hit = np.empty(B, np.int32)
+    nxt = np.empty((B, blk), np.int32)
+    hits = _load().oracle_d3d_select(_ptr(n, ctypes.c_int32), _ptr(out, ctypes.c_int32),
+                                     _ptr(pos, ctypes.c_int32), _ptr(tok, ctypes.c_int32),
+                                     _ptr(blocks, ctypes.c_int32), B, k1 - 1, NB, blk,
+                                     _ptr(hit, ctypes.c_int32), _ptr(nxt, ctypes.c_int32))
+    return hit, nxt, int(hits)

@@ -342,3 +342,34 @@ extern "C" int oracle_opd_stats(const void* target_logits, const void* draft_log
   }
   return bad;
 }
+
+// ---------------------------------------------------------------------------
+// D3D branch selection: compare every branch's assumption with the verified
+// outcome, first match wins.
+// ---------------------------------------------------------------------------
+extern "C" int oracle_d3d_select(const int32_t* num_accepted, const int32_t* out_tokens,
+                                 const int32_t* branch_pos, const int32_t* branch_tok,
+                                 const int32_t* branch_block, int B, int k, int NB, int blk,
+                                 int32_t* hit, int32_t* next_block) {
+  int hits = 0;
+  for (int b = 0; b < B; ++b) {
+    const int n = num_accepted[b];
+    int found = -1;
+    if (n >= 0 && n <= k) {
+      const int token = out_tokens[(size_t)b * (k + 1) + n];
+      for (int j = 0; j < NB; ++j) {
+        const size_t o = (size_t)b * NB + j;
+        if (branch_pos[o] >= 0 && branch_pos[o] == n && branch_tok[o] == token) {
+          found = j;
+          break;
+        }
+      }
+    }
+    hit[b] = found;
+    for (int t = 0; t < blk; ++t)
+      next_block[(size_t)b * blk + t] =
+          found >= 0 ? branch_block[((size_t)b * NB + found) * blk + t] : -1;
+    if (found >= 0) ++hits;
+  }
+  return hits;
+}

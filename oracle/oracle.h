@@ -128,6 +128,30 @@ int oracle_opd_stats(const void* target_logits, const void* draft_logits, int dt
                      int32_t* x_star, double* hard, double* rkl, double* rkl_clip,
                      double* loss);
 
+/*
+ * D3D branch selection after verification ("D3D: Decoupled Diffusion
+ * Drafting for Asynchronous Speculative Decoding", Methodology, asynchronous
+ * inference): while the target verifies a block, a packed drafter pass
+ * prepares successor blocks for selected rejection positions and the
+ * full-acceptance case; a branch whose assumed verified prefix matches the
+ * actual one is a cache hit and its block is reused, otherwise the next
+ * block must be drafted synchronously.
+ *
+ * Branch j of request b assumes that the round emits token branch_tok[b][j]
+ * at position branch_pos[b][j] after accepting the drafts before it (a
+ * rejection at that position, or the bonus token when the position is L_b).
+ * The verified outcome of request b is n = num_accepted[b] and the token
+ * out_tokens[b][n].  Branch j matches when branch_pos == n and branch_tok ==
+ * out_tokens[b][n]; the lowest matching index is the hit.  A request with
+ * n < 0 (invalid) never hits; branch_pos < 0 marks an unused slot.
+ * Outputs: hit[b] = index or -1; next_block[b][0..blk) = the hit branch's
+ * block, or -1s; returns the number of hits.
+ */
+int oracle_d3d_select(const int32_t* num_accepted, const int32_t* out_tokens,
+                      const int32_t* branch_pos, const int32_t* branch_tok,
+                      const int32_t* branch_block, int B, int k, int NB, int blk, int32_t* hit,
+                      int32_t* next_block);
+
 #ifdef __cplusplus
 }
 #endif

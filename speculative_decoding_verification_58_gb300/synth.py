@@ -238,3 +238,41 @@ def pack_rows(inp: SpecInputs, order=None, gap: int = 0) -> PackedRows:
             nd += gap
     return PackedRows(np.ascontiguousarray(np.concatenate(trows)),
                       np.ascontiguousarray(np.concatenate(drows)), t_start, d_start)
+
+
+@dataclass
+class D3DBranches:
+    """Successor blocks prepared during verification (D3D asynchronous inference)."""
+
+    pos: np.ndarray    # [B, NB] int32: first-rejection position each branch assumes (-1: unused)
+    tok: np.ndarray    # [B, NB] int32: token the branch assumes is emitted there
+    block: np.ndarray  # [B, NB, blk] int32: the successor block drafted for it
+
+
+def d3d_branch_count(C: int, F: int) -> int:
+    """Branches per request for position coverage C and token fan-out F: (C - 1) F + 2."""
+    return (C - 1) * F + 2
+
+
+def make_d3d_branches(lengths: np.ndarray, V: int, C: int = 12, F: int = 2, blk: int = 16,
+                      seed: int = 0) -> D3DBranches:
+    """Seeded branch tables laid out like the D3D packed budget B [(C - 1) F + 2].
+
+    F candidate tokens for each of the C - 1 earliest rejection positions
+    (slots past a request's length stay unused), then two for full acceptance
+    (position L_b).  Tokens and blocks are uniform draws: a stand-in for the
+    drafter's guesses, with no verification arithmetic.
+    """
+    B = len(lengths)
+    NB = d3d_branch_count(C, F)
+    rng = np.random.default_rng(seed)
+    pos = np.full((B, NB), -1, np.int32)
+    for b in range(B):
+        L = int(lengths[b])
+        for j in range((C - 1) * F):
+            if j // F < L:
+                pos[b, j] = j // F
+        pos[b, NB - 2:] = L
+    tok = rng.integers(0, V, (B, NB)).astype(np.int32)
+    block = rng.integers(0, V, (B, NB, blk)).astype(np.int32)
+    return D3DBranches(pos, tok, block)

@@ -27,6 +27,7 @@ import pytest
 import torch
 
 import oracle
+from speculative_decoding_verification_58_gb300 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -552,3 +553,67 @@ def test_opd_special_cases():
     r = oracle.opd_stats(t, d, np.array([3, 2], np.int32))
     assert r.bad_requests == 1 and np.isnan(r.loss[0]) and np.all(r.x_star[0] == -1)
     assert np.isnan(r.hard[1, 0]) and np.isnan(r.loss[1]) and r.x_star[1, 1] == 0
+
+
+# ---------------------------------------------------------------------------
+# D3D branch selection (D3D paper, Methodology, asynchronous inference)
+# ---------------------------------------------------------------------------
+
+def test_d3d_budget_layout_of_the_paper():
+    # Main D3D configuration: block size 16, coverage C = 12, fan-out F = 2;
+    # packed budget N_async = B [(C - 1) F + 2] tokens.
+    assert synth.d3d_branch_count(12, 2) * 16 == 16 * ((12 - 1) * 2 + 2) == 384
+    br = synth.make_d3d_branches(np.array([16, 3], np.int32), 1000, C=12, F=2, blk=16, seed=1)
+    assert br.pos.shape == (2, 24) and br.block.shape == (2, 24, 16)
+    assert list(br.pos[0, :22]) == [j // 2 for j in range(22)] and list(br.pos[0, 22:]) == [16, 16]
+    assert list(br.pos[1, :6]) == [0, 0, 1, 1, 2, 2] and np.all(br.pos[1, 6:22] == -1)
+
+
+def _outcome(B, k, V, rng):
+    """Made-up verification outcomes: n in [0, L], n + 1 tokens then -1."""
+    L = rng.integers(1, k + 1, B).astype(np.int32)
+    n = np.array([rng.integers(0, l + 1) for l in L], np.int32)
+    out = np.full((B, k + 1), -1, np.int32)
+    for b in range(B):
+        out[b, :n[b] + 1] = rng.integers(0, V, n[b] + 1)
+    return L, n, out
+
+
+def test_d3d_select_finds_the_planted_branch_and_only_it():
+    rng = np.random.default_rng(3)
+    B, k, V, C, F, blk = 64, 16, 500, 12, 2, 16
+    L, n, out = _outcome(B, k, V, rng)
+    br = synth.make_d3d_branches(L, V, C, F, blk, seed=4)
+    NB = br.pos.shape[1]
+    want = np.full(B, -1, np.int32)
+    for b in range(B):
+        tok_n = out[b, n[b]]
+        # No accidental matches: every branch assumes another token.
+        br.tok[b][br.tok[b] == tok_n] = (tok_n + 1) % V
+        if b % 4 != 3:  # plant the verified outcome in a random slot (3 in 4 requests)
+            s = int(rng.integers(0, NB))
+            br.pos[b, s], br.tok[b, s] = n[b], tok_n
+            want[b] = s
+    n[5] = -1  # an invalid request never hits
+    want[5] = -1
+    hit, nxt, hits = oracle.d3d_select(n, out, br.pos, br.tok, br.block)
+    np.testing.assert_array_equal(hit, want)
+    assert hits == int((want >= 0).sum())
+    for b in range(B):
+        if want[b] >= 0:
+            np.testing.assert_array_equal(nxt[b], br.block[b, want[b]])
+        else:
+            assert np.all(nxt[b] == -1)
+
+
+def test_d3d_select_tie_and_unused_slots():
+    n = np.array([2, 0], np.int32)
+    out = np.array([[7, 8, 9, -1], [4, -1, -1, -1]], np.int32)
+    pos = np.array([[1, 2, 2, -1], [-1, 0, 0, 0]], np.int32)
+    tok = np.array([[9, 9, 9, 9], [4, 5, 4, 4]], np.int32)
+    blocks = np.arange(2 * 4 * 3, dtype=np.int32).reshape(2, 4, 3)
+    hit, nxt, hits = oracle.d3d_select(n, out, pos, tok, blocks)
+    # Request 0: slots 1 and 2 both match, the lowest wins; request 1: slot 0
+    # is unused although its token matches, slot 2 is the first real match.
+    assert list(hit) == [1, 2] and hits == 2
+    np.testing.assert_array_equal(nxt, blocks[[0, 1], [1, 2]])
