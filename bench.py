@@ -52,6 +52,7 @@ def parse_args():
     ap.add_argument("--no-full-sweep", action="store_true")
     ap.add_argument("--no-packed", action="store_true")
     ap.add_argument("--no-opd", action="store_true")
+    ap.add_argument("--no-d3d", action="store_true")
     return ap.parse_args()
 
 
@@ -402,6 +403,30 @@ def run_ours(args, world, rank, local):
                "bytes_per_call": obytes, "gbs": obytes / (oms * 1e-3) / 1e9,
                "loss_mean": float(st.loss.float().mean().item())}
 
+    # D3D branch selection on this round's outcome: the paper's main budget
+    # (block 16, coverage C = 12, fan-out F = 2, 24 branches per request).
+    d3d = None
+    if not args.no_d3d:
+        br = synth.make_d3d_branches(inp.lengths, inp.V, C=12, F=2, blk=16, seed=seed + 7)
+        tb = {key: torch.from_numpy(getattr(br, key)).to(dev) for key in ("pos", "tok", "block")}
+        hit, nxt, hits = sv.spec_d3d_select(nacc, out, tb["pos"], tb["tok"], tb["block"],
+                                            stream=stream)
+        for _ in range(3):
+            sv.spec_d3d_select(nacc, out, tb["pos"], tb["tok"], tb["block"], hit=hit,
+                               next_block=nxt, hits=hits, stream=stream)
+        torch.cuda.synchronize(dev)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(kreps):
+            sv.spec_d3d_select(nacc, out, tb["pos"], tb["tok"], tb["block"], hit=hit,
+                               next_block=nxt, hits=hits, stream=stream)
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        d3d = {"us_per_call": g0.elapsed_time(g1) / kreps * 1000, "requests": inp.B,
+               "branches_per_request": int(br.pos.shape[1]), "block": 16,
+               "hit_rate": int(hits.item()) / inp.B,
+               "note": "branch tokens are uniform draws, so hits are rare; latency-bound"}
+
     # End to end through the public API: pinned host inputs in, results out, every step.
     import numpy as _np
     host = {}
@@ -476,6 +501,8 @@ def run_ours(args, world, rank, local):
     if opd is not None:
         opd["frac"] = opd["gbs"] / hbm_peak
         result["opd"] = opd
+    if d3d is not None:
+        result["d3d"] = d3d
 
     if world == 1 and not args.no_cpu_baseline:
         import oracle

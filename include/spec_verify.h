@@ -294,6 +294,38 @@ spec_status_t spec_opd_stats(const void* target_logits, const void* draft_logits
                              float delta, float alpha, int32_t* x_star, float* hard, float* rkl,
                              float* rkl_clip, float* loss, void* stream);
 
+/*
+ * D3D branch selection after a verification round ("D3D: Decoupled
+ * Diffusion Drafting for Asynchronous Speculative Decoding", Methodology,
+ * asynchronous inference).  While the target verifies a block, a packed
+ * drafter pass prepares successor blocks for selected rejection positions and
+ * the full-acceptance case (position coverage C, token fan-out F: a budget of
+ * block * [(C - 1) F + 2] tokens).  A prepared branch whose assumed verified
+ * prefix matches the actual one is a cache hit and its block is reused;
+ * otherwise the next block must be drafted synchronously.
+ *
+ *   num_accepted  [B]          int32: n from spec_verify (-1: invalid, never a hit)
+ *   out_tokens    [B, k+1]     int32: from spec_verify; out_tokens[b][n] is the
+ *                              token the round emitted after its accepted drafts
+ *   branch_pos    [B, NB]      int32: position at which branch j assumes that token
+ *                              (a rejection there, or L_b for full acceptance);
+ *                              < 0 marks an unused slot
+ *   branch_tok    [B, NB]      int32: the token branch j assumes at that position
+ *   branch_block  [B, NB, blk] int32: the successor block prepared for branch j
+ *   hit           [B]          int32 out: lowest j whose (pos, tok) equals
+ *                              (n, out_tokens[b][n]), or -1 on a miss
+ *   next_block    [B, blk]     int32 out: branch_block[b][hit], or all -1 on a miss
+ *   hits          [1]          int32 out (may be NULL): number of requests that hit
+ *
+ * All device buffers; nothing is allocated.  Launched with programmatic
+ * dependent launch, so it may directly follow spec_verify on `stream`.
+ * Host-detectable errors return before anything is enqueued.
+ */
+spec_status_t spec_d3d_select(const int32_t* num_accepted, const int32_t* out_tokens,
+                              const int32_t* branch_pos, const int32_t* branch_tok,
+                              const int32_t* branch_block, int B, int k, int NB, int blk,
+                              int32_t* hit, int32_t* next_block, int32_t* hits, void* stream);
+
 /* Static description of a status code. */
 const char* spec_status_string(spec_status_t status);
 

@@ -17,6 +17,7 @@ The functions keep the C names:
 ``spec_verify_device_status(ws)``    just the recorded status
 ``spec_row_stats(...)``              the row sweep alone: max, logsumexp, argmax
 ``spec_opd_stats(...)``              OPD supervision statistics (hard label, reverse KL, clipped)
+``spec_d3d_select(...)``             D3D branch selection: reuse a prepared successor block
 ``spec_status_string(code)``
 """
 
@@ -45,7 +46,8 @@ SPEC_FLAG_FULL_SWEEP = 1
 EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_ex", "spec_verify_timed",
            "spec_verify_packed", "spec_verify_report",
            "spec_verify_device_status", "spec_row_stats_workspace_bytes", "spec_row_stats",
-           "spec_status_string", "spec_abi_version", "spec_verify_static", "spec_opd_stats")
+           "spec_status_string", "spec_abi_version", "spec_verify_static", "spec_opd_stats",
+           "spec_d3d_select")
 SPEC_STATIC_SCRATCH_BYTES = 8 << 20
 
 
@@ -118,6 +120,9 @@ def lib() -> ctypes.CDLL:
     L.spec_opd_stats.argtypes = [vp, vp, ci, i32p, ci, ci, ci, ctypes.c_float, ctypes.c_float,
                                  i32p, f32p, f32p, f32p, f32p, vp]
     L.spec_opd_stats.restype = ci
+    L.spec_d3d_select.argtypes = [i32p, i32p, i32p, i32p, i32p, ci, ci, ci, ci, i32p, i32p, i32p,
+                                  vp]
+    L.spec_d3d_select.restype = ci
     L.spec_status_string.argtypes = [ci]
     L.spec_status_string.restype = ctypes.c_char_p
     L.spec_abi_version.argtypes = []
@@ -468,6 +473,41 @@ def spec_opd_stats(target_logits, draft_logits, lengths, *, delta: float = 0.01,
                                 out.rkl_clip.data_ptr(), out.loss.data_ptr(), _stream_ptr(stream)),
            "spec_opd_stats")
     return out
+
+
+def spec_d3d_select(num_accepted, out_tokens, branch_pos, branch_tok, branch_block, *,
+                    hit=None, next_block=None, hits=None, stream=None):
+    """D3D branch selection (D3D paper, Methodology, asynchronous inference).
+
+    num_accepted int32 [B], out_tokens int32 [B, k+1] (spec_verify's outputs);
+    branch_pos, branch_tok int32 [B, NB]; branch_block int32 [B, NB, blk].
+    Returns (hit [B], next_block [B, blk], hits [1]) device tensors.
+    """
+    torch = _torch()
+    B, k1 = out_tokens.shape
+    NB, blk = branch_block.shape[1], branch_block.shape[2]
+    dev = out_tokens.device
+    i32 = torch.int32
+    _need(num_accepted, "num_accepted", i32, (B,), dev)
+    _need(out_tokens, "out_tokens", i32, (B, k1), dev)
+    _need(branch_pos, "branch_pos", i32, (B, NB), dev)
+    _need(branch_tok, "branch_tok", i32, (B, NB), dev)
+    _need(branch_block, "branch_block", i32, (B, NB, blk), dev)
+    if hit is None:
+        hit = torch.empty(B, dtype=i32, device=dev)
+    if next_block is None:
+        next_block = torch.empty((B, blk), dtype=i32, device=dev)
+    if hits is None:
+        hits = torch.empty(1, dtype=i32, device=dev)
+    _need(hit, "hit", i32, (B,), dev)
+    _need(next_block, "next_block", i32, (B, blk), dev)
+    _need(hits, "hits", i32, (1,), dev)
+    _check(lib().spec_d3d_select(num_accepted.data_ptr(), out_tokens.data_ptr(),
+                                 branch_pos.data_ptr(), branch_tok.data_ptr(),
+                                 branch_block.data_ptr(), B, k1 - 1, NB, blk, hit.data_ptr(),
+                                 next_block.data_ptr(), hits.data_ptr(), _stream_ptr(stream)),
+           "spec_d3d_select")
+    return hit, next_block, hits
 
 
 def to_device(inputs, device="cuda"):

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "d3d.cuh"
 #include "final.cuh"
 #include "opd.cuh"
 #include "plan.cuh"
@@ -596,6 +597,32 @@ spec_status_t spec_opd_stats(const void* target_logits, const void* draft_logits
                             hard, rkl, rkl_clip, loss, s, 0, vec_ok);
   return opd_typed<uint16_t>(target_logits, draft_logits, lengths, B, k, V, delta, alpha, x_star,
                              hard, rkl, rkl_clip, loss, s, 1, vec_ok);
+}
+
+spec_status_t spec_d3d_select(const int32_t* num_accepted, const int32_t* out_tokens,
+                              const int32_t* branch_pos, const int32_t* branch_tok,
+                              const int32_t* branch_block, int B, int k, int NB, int blk,
+                              int32_t* hit, int32_t* next_block, int32_t* hits, void* stream) {
+  if (B < 1 || k < 1 || NB < 1 || blk < 1) return SPEC_ERR_INVALID_ARG;
+  if (B > SPEC_MAX_B || k > SPEC_MAX_K) return SPEC_ERR_UNSUPPORTED;
+  if ((long long)B * NB * blk >= (1LL << 40)) return SPEC_ERR_UNSUPPORTED;
+  if (!num_accepted || !out_tokens || !branch_pos || !branch_tok || !branch_block || !hit ||
+      !next_block)
+    return SPEC_ERR_INVALID_ARG;
+  if (!aligned(num_accepted, 4) || !aligned(out_tokens, 4) || !aligned(branch_pos, 4) ||
+      !aligned(branch_tok, 4) || !aligned(branch_block, 4) || !aligned(hit, 4) ||
+      !aligned(next_block, 4) || (hits && !aligned(hits, 4)))
+    return SPEC_ERR_INVALID_ARG;
+  if (use_device_of(num_accepted) != cudaSuccess) return SPEC_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch(d3d_select_kernel, dim3((B + kD3dWarps - 1) / kD3dWarps), dim3(kD3dWarps * 32), 0, s,
+             true, num_accepted, out_tokens, branch_pos, branch_tok, branch_block, B, k, NB, blk,
+             hit, next_block) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (hits && launch(d3d_count_kernel, dim3(1), dim3(kD3dCountThreads), 0, s, true,
+                     (const int32_t*)hit, B, hits) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
 }
 
 size_t spec_row_stats_workspace_bytes(int rows, int V) {

@@ -107,3 +107,21 @@ def test_bound_call_checks_buffers_once_at_construction():
                      ("draft_logits", torch.zeros(B, k, V, dtype=torch.bfloat16))):
         with pytest.raises((TypeError, ValueError)):
             sv.Verifier(**{**good, key: bad})
+
+
+def test_d3d_select_host_checks(lib):
+    f = lib.spec_d3d_select
+    ok = dict(n=16, out=16, pos=16, tok=16, blk_=16, B=2, k=3, NB=4, blk=5, hit=16, nxt=16, hits=None)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["n"], a["out"], a["pos"], a["tok"], a["blk_"], a["B"], a["k"], a["NB"], a["blk"],
+                 a["hit"], a["nxt"], a["hits"], None)
+
+    assert call(B=0) == sv.SPEC_ERR_INVALID_ARG
+    assert call(NB=0) == sv.SPEC_ERR_INVALID_ARG
+    assert call(blk=0) == sv.SPEC_ERR_INVALID_ARG
+    assert call(k=40) == sv.SPEC_ERR_UNSUPPORTED
+    assert call(pos=None) == sv.SPEC_ERR_INVALID_ARG
+    assert call(nxt=18) == sv.SPEC_ERR_INVALID_ARG
+    assert call(hits=18) == sv.SPEC_ERR_INVALID_ARG
