@@ -18,7 +18,6 @@ is checked against) on the host cores on the same workload instead.
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import math
@@ -77,10 +76,11 @@ def measured_peaks():
 
 
 def csrc_digest() -> str:
+    """Digest of the sources the sweep kernel is built from (its code, the
+    shared helpers and the plan kernel that lays out its work)."""
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "speculative_decoding_verification_58_gb300",
-                                          "csrc", "*")))
-    files.append(os.path.join(ROOT, "include", "spec_verify.h"))
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_58_gb300", "csrc")
+    files = [os.path.join(csrc, name) for name in ("common.cuh", "plan.cuh", "sweep.cuh")]
     for f in files:
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode())
