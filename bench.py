@@ -66,6 +66,50 @@ def dist_setup():
     return world, rank, local
 
 
+def replica_seed(base: int, rank: int) -> int:
+    """Each replica verifies its own batch: same workload recipe, its own seed."""
+    return base + 1000 * rank
+
+
+def aggregate_value(world: int, ms_max: float) -> float:
+    """Rounds/s of the whole job: every rank completes one round per step, and the
+    step time is the slowest rank's."""
+    return world * 1000.0 / ms_max
+
+
+class Ranks:
+    """Process-group plumbing for N replicas: a barrier and a max over ranks.
+
+    Used for timing only; no data crosses ranks (requests are independent).
+    NCCL with CUDA tensors on GPUs, gloo with CPU tensors in the CPU tests.
+    """
+
+    def __init__(self, world: int, device=None, backend: str = "nccl"):
+        self.world = world
+        self.device = device
+        if world > 1:
+            import torch.distributed as dist
+            if not dist.is_initialized():
+                if backend == "nccl":
+                    dist.init_process_group("nccl", device_id=device)
+                else:
+                    dist.init_process_group(backend)
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max(self, x: float) -> float:
+        if self.world == 1:
+            return x
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -236,14 +280,12 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
+    ranks = Ranks(world, dev, "nccl")
     sv.lib()
 
     name = args.workload or synth.HEADLINE
     cfg = synth.WORKLOADS[name]
-    seed = (args.seed if args.seed is not None else cfg["seed"]) + 1000 * rank
+    seed = replica_seed(args.seed if args.seed is not None else cfg["seed"], rank)
     inp = synth.make_workload(name, seed=seed)
     esize = 2 if inp.dtype == "bf16" else 4
     d = sv.to_device(inp, dev)
@@ -263,18 +305,7 @@ def run_ours(args, world, rank, local):
             sv.spec_verify(**d, workspace=ws, out_tokens=out, num_accepted=nacc, stream=stream,
                            full_sweep=full_sweep, events=events)
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    barrier, max_over_ranks = ranks.barrier, ranks.max
 
     props = torch.cuda.get_device_properties(dev)
     sampler = ClockSampler(f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local))
@@ -464,7 +495,7 @@ def run_ours(args, world, rank, local):
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     sweep_gbs = rep.sweep_bytes / (k_sweep * 1e-3) / 1e9
     round_bytes = rep.sweep_bytes + rep.final_bytes
-    value = world * 1000.0 / ms
+    value = aggregate_value(world, ms)
 
     result = {
         "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world,
