@@ -257,3 +257,31 @@ def test_bound_call_matches_spec_verify_and_sees_new_contents():
         o = oracle.verify(inp.target, inp.draft, inp.tokens, inp.lengths, inp.uniforms,
                           inp.temperature)
         compare(out.cpu().numpy(), n.cpu().numpy(), o, inp.temperature, "bound call")
+
+
+def test_round_captured_in_a_cuda_graph_replays_with_new_contents():
+    """A serving loop captures one round (three kernels, launch overlap kept) and replays it."""
+    a = synth.make_inputs("zipf_mixed_temp", 32, 16, 9000, "bf16", seed=41)
+    b = synth.make_inputs("zipf_mixed_temp", 32, 16, 9000, "bf16", seed=42)
+    s = torch.cuda.Stream()
+    d = sv.to_device(a)
+    ws = sv.alloc_workspace(a.B, a.k, a.V)
+    out = torch.empty((a.B, a.k + 1), dtype=torch.int32, device="cuda")
+    nacc = torch.empty(a.B, dtype=torch.int32, device="cuda")
+    call = sv.Verifier(**d, workspace=ws, out_tokens=out, num_accepted=nacc, stream=s)
+    with torch.cuda.stream(s):
+        call()  # first call on the device sets the kernels up, outside the capture
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    for inp in (a, b, a):
+        for key, t in sv.to_device(inp).items():
+            d[key].copy_(t)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        o = oracle.verify(inp.target, inp.draft, inp.tokens, inp.lengths, inp.uniforms,
+                          inp.temperature)
+        compare(out.cpu().numpy(), nacc.cpu().numpy(), o, inp.temperature, "graph replay")
+        assert sv.spec_verify_report(ws).status == sv.SPEC_OK
