@@ -580,7 +580,7 @@ def run_ours(args, world, rank, local):
         reps, spent = 0, 0.0
         t0 = time.perf_counter()
         o = None
-        while reps < 1 or (spent < 10.0 and reps < 3):
+        while reps < 1 or (spent < 10.0 and reps < 30):
             o = oracle.verify(inp.target, inp.draft, inp.tokens, inp.lengths, inp.uniforms,
                               inp.temperature)
             reps += 1
