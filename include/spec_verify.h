@@ -285,9 +285,11 @@ spec_status_t spec_row_stats(const void* logits, spec_dtype_t dtype, int rows, i
  * NaN; an invalid L_b makes the whole request -1 / NaN (loss NaN); a row
  * without finite mass (NaN, +inf, all -inf) makes its position NaN.
  * delta must be finite and > 0 (the paper uses 0.01), alpha in [0, 1] (0.8).
- * Needs no workspace.  Every logit is used twice (normalisers first, then the
- * sums); the second read is arranged to come from L2.  Asynchronous on
- * `stream`; returns SPEC_OK once enqueued.
+ * Needs no workspace and so records no device status: every position starts
+ * as -1 / NaN and is overwritten when its results are known, so a
+ * device-side wait that runs out (2 s) leaves NaN behind.  Every logit is
+ * used twice (normalisers first, then the sums); the second read is arranged
+ * to come from L2.  Asynchronous on `stream`; returns SPEC_OK once enqueued.
  */
 spec_status_t spec_opd_stats(const void* target_logits, const void* draft_logits,
                              spec_dtype_t dtype, const int32_t* lengths, int B, int k, int V,

@@ -218,18 +218,13 @@ __device__ __forceinline__ void opd_target_vec(SoftAcc& a, ArgAcc& g, const uint
 
 
 // The next position of this cluster, q, q + ncl, ... that has a verified row
-// pair (i < L_b, L_b valid); -1 when there is none.  With `mark` set, the
-// positions passed over get x* = -1 and NaN.
-__device__ __forceinline__ int opd_next_active(const OpdParams& p, int q, int ncl, bool mark) {
+// pair (i < L_b, L_b valid); -1 when there is none.
+__device__ __forceinline__ int opd_next_active(const OpdParams& p, int q, int ncl) {
   const int npos = p.B * p.k;
   for (; q < npos; q += ncl) {
     const int b = q / p.k, i = q - b * p.k;
     const int L = __ldg(&p.lengths[b]);
     if (L >= 1 && L <= p.k && i < L) return q;
-    if (mark) {
-      p.x_star[q] = -1;
-      p.hard[q] = p.rkl[q] = p.rkl_clip[q] = __int_as_float(0x7fc00000);
-    }
   }
   return -1;
 }
@@ -239,15 +234,15 @@ __device__ __forceinline__ int opd_next_active(const OpdParams& p, int q, int nc
 // position comes one position after its pass 1, so the cluster's exchange of
 // normalisers never holds the consumers up.
 template <typename F>
-__device__ __forceinline__ void opd_walk(const OpdParams& p, int cid, int ncl, bool mark, F&& unit) {
+__device__ __forceinline__ void opd_walk(const OpdParams& p, int cid, int ncl, F&& unit) {
   int q_prev = -1;
-  int q = opd_next_active(p, cid, ncl, mark);
+  int q = opd_next_active(p, cid, ncl);
   for (int j = 0;; ++j) {
     if (q >= 0 && !unit(q, j, 1)) return;
     if (j >= 1 && !unit(q_prev, j - 1, 2)) return;
     if (q < 0) return;
     q_prev = q;
-    q = opd_next_active(p, q + ncl, ncl, mark);
+    q = opd_next_active(p, q + ncl, ncl);
   }
 }
 
@@ -265,7 +260,7 @@ __device__ void opd_producer(const OpdParams& p, OpdSmem& sm, int cid, int ncl, 
   const int n = max(0, min(p.slice, p.V - s0));
   const uint64_t pol_keep = l2_policy_evict_last(), pol_drop = l2_policy_evict_first();
   int it = 0;
-  opd_walk(p, cid, ncl, false, [&](int q, int j, int pass) -> bool {
+  opd_walk(p, cid, ncl, [&](int q, int j, int pass) -> bool {
     const int b = q / p.k, i = q - b * p.k;
     const TIn* t = static_cast<const TIn*>(p.target) + ((size_t)b * (p.k + 1) + i) * (size_t)p.V + s0;
     const TIn* d = static_cast<const TIn*>(p.draft) + ((size_t)b * p.k + i) * (size_t)p.V + s0;
@@ -321,7 +316,7 @@ __device__ void opd_consumers(const OpdParams& p, OpdSmem& sm, int cid, int ncl,
   const int ctid = threadIdx.x - kOpdFirstConsumerWarp * 32;
   const float delta = p.delta;
   int it = 0;
-  opd_walk(p, cid, ncl, false, [&](int q, int j, int pass) -> bool {
+  opd_walk(p, cid, ncl, [&](int q, int j, int pass) -> bool {
     const int slot = j & 1;
     const uint32_t par = (j >> 1) & 1;
     float c = 0.0f, nl2d = 0.0f;
@@ -479,7 +474,17 @@ __device__ void opd_bookkeeper(const OpdParams& p, OpdSmem& sm, int cid, int ncl
                                uint32_t rank) {
   const int lane = threadIdx.x & 31;
   float zstar[2] = {0.0f, 0.0f};  // z_d[x*] per slot, loaded when x* becomes known
-  opd_walk(p, cid, ncl, rank == 0 && lane == 0, [&](int q, int j, int pass) -> bool {
+  // Every position of this cluster starts as x* = -1 / NaN: positions past
+  // L_b keep it, verified ones are overwritten with their results, and a
+  // wait that runs out leaves the rest visibly unset.
+  if (rank == 0) {
+    for (int q = cid + ncl * lane; q < p.B * p.k; q += 32 * ncl) {
+      p.x_star[q] = -1;
+      p.hard[q] = p.rkl[q] = p.rkl_clip[q] = __int_as_float(0x7fc00000);
+    }
+    __syncwarp();
+  }
+  opd_walk(p, cid, ncl, [&](int q, int j, int pass) -> bool {
     const int slot = j & 1;
     const uint32_t par = (j >> 1) & 1;
     const int b = q / p.k, i = q - b * p.k;
