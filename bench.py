@@ -345,6 +345,20 @@ def run_ours(args, world, rank, local):
     rep = sv.spec_verify_report(ws, stream)
     gpu_out, gpu_n = out.cpu().numpy(), nacc.cpu().numpy()
 
+    # Round-time distribution: an event pair around each round (the events sit
+    # between rounds, so a round cannot start under the previous one's tail).
+    preps = max(10, min(args.steps, 200))
+    rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(preps)]
+    for a_, b_ in rev:
+        a_.record(stream)
+        step()
+        b_.record(stream)
+    torch.cuda.synchronize(dev)
+    rts = sorted(a_.elapsed_time(b_) for a_, b_ in rev)
+    round_pct = {"p10": rts[int(0.1 * (preps - 1))], "p50": rts[(preps - 1) // 2],
+                 "p90": rts[int(0.9 * (preps - 1))], "rounds": preps, "unit": "ms"}
+
     # Per-kernel durations: the same rounds with events between the kernels.
     kreps = max(10, min(args.steps, 200))
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(kreps)]
@@ -553,6 +567,7 @@ def run_ours(args, world, rank, local):
                      "traffic": ncu_traffic(name),
                      "bytes_per_launch": rep.sweep_bytes},
         "kernels_ms": {"plan": k_plan, "sweep": k_sweep, "final": k_final},
+        "round_ms_percentiles": round_pct,
         "round_bytes": {"sweep": rep.sweep_bytes, "final": rep.final_bytes},
         "e2e": {"value": world / e2e_s, "unit": "rounds/s", "h2d_bytes_per_step": h2d_packed,
                 "d2h_bytes_per_step": d2h, "layout": "packed (rows 0..L_b of each request)",
