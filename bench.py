@@ -272,325 +272,288 @@ def run_reference(args, world, rank):
 # Our arm
 # ---------------------------------------------------------------------------
 
-def run_ours(args, world, rank, local):
+def _event_pair():
     import torch
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
-    import speculative_decoding_verification_58_gb300 as sv
-    from speculative_decoding_verification_58_gb300 import synth
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    ranks = Ranks(world, dev, "nccl")
-    sv.lib()
+class OurArm:
+    """This library's side of the benchmark: one verification round per step,
+    then the extra legs (early exit off, packed batch, OPD statistics, D3D
+    selection, end to end, CPU baseline) on the same inputs."""
 
-    name = args.workload or synth.HEADLINE
-    cfg = synth.WORKLOADS[name]
-    seed = replica_seed(args.seed if args.seed is not None else cfg["seed"], rank)
-    inp = synth.make_workload(name, seed=seed)
-    esize = 2 if inp.dtype == "bf16" else 4
-    d = sv.to_device(inp, dev)
-    ws = sv.alloc_workspace(inp.B, inp.k, inp.V, dev)
-    out = torch.empty((inp.B, inp.k + 1), dtype=torch.int32, device=dev)
-    nacc = torch.empty(inp.B, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    def __init__(self, args, world, rank, local):
+        import torch
 
-    # Bound calls: buffers checked once, one C call per round.
-    bound = {fs: sv.Verifier(**d, workspace=ws, out_tokens=out, num_accepted=nacc, stream=stream,
-                             full_sweep=fs) for fs in (False, True)}
+        import speculative_decoding_verification_58_gb300 as sv
+        from speculative_decoding_verification_58_gb300 import synth
 
-    def step(full_sweep=False, events=None):
+        self.torch, self.sv, self.synth = torch, sv, synth
+        self.args, self.world, self.rank = args, world, rank
+        torch.cuda.set_device(local)
+        self.dev = dev = torch.device("cuda", local)
+        self.ranks = Ranks(world, dev, "nccl")
+        sv.lib()
+
+        self.name = args.workload or synth.HEADLINE
+        cfg = synth.WORKLOADS[self.name]
+        self.seed = replica_seed(args.seed if args.seed is not None else cfg["seed"], rank)
+        self.inp = inp = synth.make_workload(self.name, seed=self.seed)
+        self.esize = 2 if inp.dtype == "bf16" else 4
+        self.d = sv.to_device(inp, dev)
+        self.ws = sv.alloc_workspace(inp.B, inp.k, inp.V, dev)
+        self.out = torch.empty((inp.B, inp.k + 1), dtype=torch.int32, device=dev)
+        self.nacc = torch.empty(inp.B, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        # Bound calls: buffers checked once, one C call per round.
+        self.bound = {fs: sv.Verifier(**self.d, workspace=self.ws, out_tokens=self.out,
+                                      num_accepted=self.nacc, stream=self.stream, full_sweep=fs)
+                      for fs in (False, True)}
+        self.logit_bytes = inp.target.nbytes + inp.draft.nbytes
+        self.reps = max(10, min(args.steps, 200))
+
+    def step(self, full_sweep=False, events=None):
         if events is None:
-            bound[full_sweep]()
+            self.bound[full_sweep]()
         else:
-            sv.spec_verify(**d, workspace=ws, out_tokens=out, num_accepted=nacc, stream=stream,
-                           full_sweep=full_sweep, events=events)
+            self.sv.spec_verify(**self.d, workspace=self.ws, out_tokens=self.out,
+                                num_accepted=self.nacc, stream=self.stream,
+                                full_sweep=full_sweep, events=events)
 
-    barrier, max_over_ranks = ranks.barrier, ranks.max
+    def sync(self):
+        self.torch.cuda.synchronize(self.dev)
 
-    props = torch.cuda.get_device_properties(dev)
-    sampler = ClockSampler(f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local))
+    # -- the timed region ---------------------------------------------------
+    def timed_rounds(self):
+        """K rounds after W warm-up rounds, device-timed with events on the stream."""
+        args, torch = self.args, self.torch
+        for _ in range(max(3, args.warmup)):
+            self.step()
+        self.sync()
+        self.ranks.barrier()
+        self.sync()
+        self.flush = self.logit_bytes < 2 * L2_BYTES
+        if not self.flush:
+            # Inputs larger than L2: back-to-back rounds, one pair of events around all.
+            e0, e1 = _event_pair()
+            e0.record(self.stream)
+            for _ in range(args.steps):
+                self.step()
+            e1.record(self.stream)
+            self.sync()
+            total_ms = e0.elapsed_time(e1)
+        else:
+            # Inputs that fit in L2: overwrite a buffer larger than L2 before every
+            # round and time each round alone.
+            scrub = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=self.dev)
+            pairs = [_event_pair() for _ in range(args.steps)]
+            for a, b in pairs:
+                scrub.fill_(1)
+                a.record(self.stream)
+                self.step()
+                b.record(self.stream)
+            self.sync()
+            total_ms = sum(a.elapsed_time(b) for a, b in pairs)
+        self.ranks.barrier()
+        self.ms = self.ranks.max(total_ms / args.steps)
+        self.rep = self.sv.spec_verify_report(self.ws, self.stream)
+        self.gpu_out, self.gpu_n = self.out.cpu().numpy(), self.nacc.cpu().numpy()
 
-    # Warm-up, then the timed region: K rounds, device-timed with events on the launch stream.
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize(dev)
-    barrier()
-    torch.cuda.synchronize(dev)
-    logit_bytes = inp.target.nbytes + inp.draft.nbytes
-    flush = logit_bytes < 2 * L2_BYTES
-    if not flush:
-        # Inputs larger than L2: back-to-back rounds, one pair of events around all.
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        total_ms = e0.elapsed_time(e1)
-    else:
-        # Inputs that fit in L2: overwrite a buffer larger than L2 before every
-        # round and time each round alone.
-        scrub = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
-        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(args.steps)]
-        for a, b in pairs:
-            scrub.fill_(1)
-            a.record(stream)
-            step()
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        total_ms = sum(a.elapsed_time(b) for a, b in pairs)
-    barrier()
-    ms = max_over_ranks(total_ms / args.steps)
-    rep = sv.spec_verify_report(ws, stream)
-    gpu_out, gpu_n = out.cpu().numpy(), nacc.cpu().numpy()
+    # -- measurements around the timed region --------------------------------
+    def round_percentiles(self):
+        """An event pair around each round (the events sit between rounds, so a
+        round cannot start under the previous one's tail)."""
+        rev = [_event_pair() for _ in range(self.reps)]
+        for a, b in rev:
+            a.record(self.stream)
+            self.step()
+            b.record(self.stream)
+        self.sync()
+        rts = sorted(a.elapsed_time(b) for a, b in rev)
+        n = self.reps
+        return {"p10": rts[int(0.1 * (n - 1))], "p50": rts[(n - 1) // 2],
+                "p90": rts[int(0.9 * (n - 1))], "rounds": n, "unit": "ms"}
 
-    # Round-time distribution: an event pair around each round (the events sit
-    # between rounds, so a round cannot start under the previous one's tail).
-    preps = max(10, min(args.steps, 200))
-    rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(preps)]
-    for a_, b_ in rev:
-        a_.record(stream)
-        step()
-        b_.record(stream)
-    torch.cuda.synchronize(dev)
-    rts = sorted(a_.elapsed_time(b_) for a_, b_ in rev)
-    round_pct = {"p10": rts[int(0.1 * (preps - 1))], "p50": rts[(preps - 1) // 2],
-                 "p90": rts[int(0.9 * (preps - 1))], "rounds": preps, "unit": "ms"}
-
-    # Per-kernel durations: the same rounds with events between the kernels.
-    kreps = max(10, min(args.steps, 200))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(kreps)]
-    for row in evs:
-        for e in row:
-            e.record(stream)  # creates the handles
-    torch.cuda.synchronize(dev)
-    for row in evs:
-        step(events=row)
-    torch.cuda.synchronize(dev)
-    k_plan = statistics.mean(r[0].elapsed_time(r[1]) for r in evs)
-    k_sweep = statistics.mean(r[1].elapsed_time(r[2]) for r in evs)
-    k_final = statistics.mean(r[2].elapsed_time(r[3]) for r in evs)
-
-    # Same workload with early exit switched off (every row i < L_b is swept).
-    full = None
-    if not args.no_full_sweep:
-        for _ in range(3):
-            step(full_sweep=True)
-        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(kreps)]
-        for row in fev:
+    def kernel_times(self, full_sweep=False):
+        """Mean durations of plan, sweep and final: rounds with events between them."""
+        evs = [[self.torch.cuda.Event(enable_timing=True) for _ in range(4)]
+               for _ in range(self.reps)]
+        for row in evs:
             for e in row:
-                e.record(stream)
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        for _ in range(kreps):
-            step(full_sweep=True)
-        f1.record(stream)
-        torch.cuda.synchronize(dev)
-        frep = sv.spec_verify_report(ws, stream)
-        for row in fev:
-            step(full_sweep=True, events=row)
-        torch.cuda.synchronize(dev)
-        fsweep = statistics.mean(r[1].elapsed_time(r[2]) for r in fev)
-        full = {"ms_per_step": f0.elapsed_time(f1) / kreps, "sweep_ms": fsweep,
+                e.record(self.stream)  # creates the handles
+        self.sync()
+        for row in evs:
+            self.step(full_sweep=full_sweep, events=row)
+        self.sync()
+        return tuple(statistics.mean(r[j].elapsed_time(r[j + 1]) for r in evs) for j in range(3))
+
+    def full_sweep_leg(self):
+        """The same workload with early exit switched off (every row i < L_b is swept)."""
+        for _ in range(3):
+            self.step(full_sweep=True)
+        f0, f1 = _event_pair()
+        f0.record(self.stream)
+        for _ in range(self.reps):
+            self.step(full_sweep=True)
+        f1.record(self.stream)
+        self.sync()
+        frep = self.sv.spec_verify_report(self.ws, self.stream)
+        fsweep = self.kernel_times(full_sweep=True)[1]
+        return {"ms_per_step": f0.elapsed_time(f1) / self.reps, "sweep_ms": fsweep,
                 "sweep_bytes": frep.sweep_bytes,
                 "sweep_gbs": frep.sweep_bytes / (fsweep * 1e-3) / 1e9}
 
-    # The same batch packed (AdaFlash Section 3.3: total length sum_b L_b rows
-    # instead of B x k): same outputs, a smaller resident footprint.
-    packed = None
-    if not args.no_packed:
-        pk = synth.pack_rows(inp)
-        rows = sv.to_device_packed(pk, dev)
+    def packed_leg(self):
+        """The same batch packed (AdaFlash Section 3.3: total length sum_b L_b rows
+        instead of B x k): same outputs, a smaller resident footprint."""
+        sv, d = self.sv, self.d
+        pk = self.synth.pack_rows(self.inp)
+        rows = sv.to_device_packed(pk, self.dev)
         pargs = dict(**rows, draft_tokens=d["draft_tokens"], lengths=d["lengths"],
-                     uniforms=d["uniforms"], temperature=d["temperature"], workspace=ws,
-                     out_tokens=out, num_accepted=nacc, stream=stream)
+                     uniforms=d["uniforms"], temperature=d["temperature"], workspace=self.ws,
+                     out_tokens=self.out, num_accepted=self.nacc, stream=self.stream)
         for _ in range(3):
             sv.spec_verify_packed(**pargs)
-        torch.cuda.synchronize(dev)
-        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        p0.record(stream)
-        for _ in range(kreps):
+        self.sync()
+        p0, p1 = _event_pair()
+        p0.record(self.stream)
+        for _ in range(self.reps):
             sv.spec_verify_packed(**pargs)
-        p1.record(stream)
-        torch.cuda.synchronize(dev)
-        same = bool(np.array_equal(out.cpu().numpy(), gpu_out) and
-                    np.array_equal(nacc.cpu().numpy(), gpu_n))
-        pms = p0.elapsed_time(p1) / kreps
-        packed = {"ms_per_step": pms, "value": 1000.0 / pms, "unit": "rounds/s",
-                  "logit_bytes": int(pk.target_rows.nbytes + pk.draft_rows.nbytes),
-                  "padded_logit_bytes": int(logit_bytes), "same_outputs_as_padded": same}
+        p1.record(self.stream)
+        self.sync()
+        same = bool(np.array_equal(self.out.cpu().numpy(), self.gpu_out) and
+                    np.array_equal(self.nacc.cpu().numpy(), self.gpu_n))
+        pms = p0.elapsed_time(p1) / self.reps
         del rows, pargs
-        torch.cuda.empty_cache()
+        self.torch.cuda.empty_cache()
+        return {"ms_per_step": pms, "value": 1000.0 / pms, "unit": "rounds/s",
+                "logit_bytes": int(pk.target_rows.nbytes + pk.draft_rows.nbytes),
+                "padded_logit_bytes": int(self.logit_bytes), "same_outputs_as_padded": same}
 
-    # OPD supervision statistics (AdaFlash Section 3.1) on the same buffers:
-    # both rows of every verified position read once.
-    opd = None
-    if not args.no_opd:
-        st = sv.spec_opd_stats(d["target_logits"], d["draft_logits"], d["lengths"], stream=stream)
+    def opd_leg(self):
+        """OPD supervision statistics (AdaFlash Section 3.1) on the same buffers:
+        both rows of every verified position."""
+        sv, d, inp = self.sv, self.d, self.inp
+        st = sv.spec_opd_stats(d["target_logits"], d["draft_logits"], d["lengths"],
+                               stream=self.stream)
+        call = lambda: sv.spec_opd_stats(d["target_logits"], d["draft_logits"], d["lengths"],
+                                         out=st, stream=self.stream)
         for _ in range(3):
-            sv.spec_opd_stats(d["target_logits"], d["draft_logits"], d["lengths"], out=st,
-                              stream=stream)
-        torch.cuda.synchronize(dev)
-        o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        oreps = max(10, min(args.steps, 100))
-        o0.record(stream)
+            call()
+        self.sync()
+        o0, o1 = _event_pair()
+        oreps = max(10, min(self.args.steps, 100))
+        o0.record(self.stream)
         for _ in range(oreps):
-            sv.spec_opd_stats(d["target_logits"], d["draft_logits"], d["lengths"], out=st,
-                              stream=stream)
-        o1.record(stream)
-        torch.cuda.synchronize(dev)
+            call()
+        o1.record(self.stream)
+        self.sync()
         oms = o0.elapsed_time(o1) / oreps
         positions = int(inp.lengths.sum())
-        obytes = positions * 2 * inp.V * esize
-        opd = {"ms_per_call": oms, "positions": positions, "positions_per_s": positions / (oms * 1e-3),
-               "bytes_per_call": obytes, "gbs": obytes / (oms * 1e-3) / 1e9,
-               "loss_mean": float(st.loss.float().mean().item())}
+        obytes = positions * 2 * inp.V * self.esize
+        return {"ms_per_call": oms, "positions": positions,
+                "positions_per_s": positions / (oms * 1e-3), "bytes_per_call": obytes,
+                "gbs": obytes / (oms * 1e-3) / 1e9,
+                "loss_mean": float(st.loss.float().mean().item())}
 
-    # D3D branch selection on this round's outcome: the paper's main budget
-    # (block 16, coverage C = 12, fan-out F = 2, 24 branches per request).
-    d3d = None
-    if not args.no_d3d:
-        br = synth.make_d3d_branches(inp.lengths, inp.V, C=12, F=2, blk=16, seed=seed + 7)
-        tb = {key: torch.from_numpy(getattr(br, key)).to(dev) for key in ("pos", "tok", "block")}
-        hit, nxt, hits = sv.spec_d3d_select(nacc, out, tb["pos"], tb["tok"], tb["block"],
-                                            stream=stream)
+    def d3d_leg(self):
+        """D3D branch selection on this round's outcome: the paper's main budget
+        (block 16, coverage C = 12, fan-out F = 2, 24 branches per request)."""
+        sv, inp = self.sv, self.inp
+        br = self.synth.make_d3d_branches(inp.lengths, inp.V, C=12, F=2, blk=16,
+                                          seed=self.seed + 7)
+        tb = {key: self.torch.from_numpy(getattr(br, key)).to(self.dev)
+              for key in ("pos", "tok", "block")}
+        hit, nxt, hits = sv.spec_d3d_select(self.nacc, self.out, tb["pos"], tb["tok"],
+                                            tb["block"], stream=self.stream)
+        call = lambda: sv.spec_d3d_select(self.nacc, self.out, tb["pos"], tb["tok"], tb["block"],
+                                          hit=hit, next_block=nxt, hits=hits, stream=self.stream)
         for _ in range(3):
-            sv.spec_d3d_select(nacc, out, tb["pos"], tb["tok"], tb["block"], hit=hit,
-                               next_block=nxt, hits=hits, stream=stream)
-        torch.cuda.synchronize(dev)
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
-        for _ in range(kreps):
-            sv.spec_d3d_select(nacc, out, tb["pos"], tb["tok"], tb["block"], hit=hit,
-                               next_block=nxt, hits=hits, stream=stream)
-        g1.record(stream)
-        torch.cuda.synchronize(dev)
-        d3d = {"us_per_call": g0.elapsed_time(g1) / kreps * 1000, "requests": inp.B,
-               "branches_per_request": int(br.pos.shape[1]), "block": 16,
-               "hit_rate": int(hits.item()) / inp.B,
-               "note": "branch tokens are uniform draws, so hits are rare; latency-bound"}
+            call()
+        self.sync()
+        g0, g1 = _event_pair()
+        g0.record(self.stream)
+        for _ in range(self.reps):
+            call()
+        g1.record(self.stream)
+        self.sync()
+        return {"us_per_call": g0.elapsed_time(g1) / self.reps * 1000, "requests": inp.B,
+                "branches_per_request": int(br.pos.shape[1]), "block": 16,
+                "hit_rate": int(hits.item()) / inp.B,
+                "note": "branch tokens are uniform draws, so hits are rare; latency-bound"}
 
-    # End to end through the public API: pinned host inputs in, results out, every step.
-    import numpy as _np
-    host = {}
-    for key, t in d.items():
-        host[key] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-        host[key].copy_(t.cpu())
-    h_out = torch.empty(out.shape, dtype=torch.int32, pin_memory=True)
-    h_n = torch.empty(nacc.shape, dtype=torch.int32, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = h_out.numel() * 4 + h_n.numel() * 4
-    e2e_steps = args.e2e_steps or max(5, min(50, args.steps))
+    def e2e_legs(self):
+        """End to end through the public API: pinned host inputs in, results out,
+        every step; the padded buffers, then the packed batch (AdaFlash Section
+        3.3: only the rows a round can read, rows 0..L_b of each request)."""
+        torch, sv, d = self.torch, self.sv, self.d
+        host = {}
+        for key, t in d.items():
+            host[key] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            host[key].copy_(t.cpu())
+        h_out = torch.empty(self.out.shape, dtype=torch.int32, pin_memory=True)
+        h_n = torch.empty(self.nacc.shape, dtype=torch.int32, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = h_out.numel() * 4 + h_n.numel() * 4
+        steps = self.args.e2e_steps or max(5, min(50, self.args.steps))
 
-    def e2e_step():
-        for key, t in host.items():
-            d[key].copy_(t, non_blocking=True)
-        step()
-        h_out.copy_(out, non_blocking=True)
-        h_n.copy_(nacc, non_blocking=True)
-        stream.synchronize()
+        def timed(step_fn):
+            for _ in range(2):
+                step_fn()
+            self.ranks.barrier()
+            t0 = time.perf_counter()
+            for _ in range(steps):
+                step_fn()
+            return self.ranks.max((time.perf_counter() - t0) / steps)
 
-    for _ in range(2):
-        e2e_step()
-    barrier()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-    e2e_padded_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps)
+        def padded_step():
+            for key, t in host.items():
+                d[key].copy_(t, non_blocking=True)
+            self.step()
+            h_out.copy_(self.out, non_blocking=True)
+            h_n.copy_(self.nacc, non_blocking=True)
+            self.stream.synchronize()
 
-    # The same, with the batch packed (AdaFlash Section 3.3): the host sends
-    # only the rows a round can read (rows 0..L_b), which is what a serving
-    # engine's packed verification batch holds.
-    pk_host = synth.pack_rows(inp)
-    hp = {key: torch.from_numpy(np.ascontiguousarray(v)).pin_memory()
-          for key, v in (("target_row_start", pk_host.target_row_start),
-                         ("draft_row_start", pk_host.draft_row_start))}
-    for key, v in (("target_rows", pk_host.target_rows), ("draft_rows", pk_host.draft_rows)):
-        t = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16) if v.dtype == np.uint16 \
-            else torch.from_numpy(v)
-        hp[key] = t.pin_memory()
-    for key in ("draft_tokens", "lengths", "uniforms", "temperature"):
-        hp[key] = host[key]
-    dp = {key: torch.empty(t.shape, dtype=t.dtype, device=dev) for key, t in hp.items()}
-    h2d_packed = sum(t.numel() * t.element_size() for t in hp.values())
+        padded_s = timed(padded_step)
 
-    def e2e_packed_step():
-        for key, t in hp.items():
-            dp[key].copy_(t, non_blocking=True)
-        sv.spec_verify_packed(**dp, workspace=ws, out_tokens=out, num_accepted=nacc,
-                              stream=stream)
-        h_out.copy_(out, non_blocking=True)
-        h_n.copy_(nacc, non_blocking=True)
-        stream.synchronize()
+        pk = self.synth.pack_rows(self.inp)
+        hp = {key: torch.from_numpy(np.ascontiguousarray(v)).pin_memory()
+              for key, v in (("target_row_start", pk.target_row_start),
+                             ("draft_row_start", pk.draft_row_start))}
+        for key, v in (("target_rows", pk.target_rows), ("draft_rows", pk.draft_rows)):
+            t = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16) \
+                if v.dtype == np.uint16 else torch.from_numpy(v)
+            hp[key] = t.pin_memory()
+        for key in ("draft_tokens", "lengths", "uniforms", "temperature"):
+            hp[key] = host[key]
+        dp = {key: torch.empty(t.shape, dtype=t.dtype, device=self.dev) for key, t in hp.items()}
+        h2d_packed = sum(t.numel() * t.element_size() for t in hp.values())
 
-    for _ in range(2):
-        e2e_packed_step()
-    e2e_same = bool(np.array_equal(h_out.numpy(), gpu_out) and np.array_equal(h_n.numpy(), gpu_n))
-    barrier()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_packed_step()
-    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps)
-    del dp
-    clocks = sampler.stop()
-    barrier()
+        def packed_step():
+            for key, t in hp.items():
+                dp[key].copy_(t, non_blocking=True)
+            sv.spec_verify_packed(**dp, workspace=self.ws, out_tokens=self.out,
+                                  num_accepted=self.nacc, stream=self.stream)
+            h_out.copy_(self.out, non_blocking=True)
+            h_n.copy_(self.nacc, non_blocking=True)
+            self.stream.synchronize()
 
-    if rank != 0:
-        return
+        packed_step()
+        same = bool(np.array_equal(h_out.numpy(), self.gpu_out) and
+                    np.array_equal(h_n.numpy(), self.gpu_n))
+        packed_s = timed(packed_step)
+        del dp
+        return ({"value": self.world / packed_s, "unit": "rounds/s",
+                 "h2d_bytes_per_step": h2d_packed, "d2h_bytes_per_step": d2h,
+                 "layout": "packed (rows 0..L_b of each request)", "same_outputs": same},
+                {"value": self.world / padded_s, "unit": "rounds/s", "h2d_bytes_per_step": h2d,
+                 "d2h_bytes_per_step": d2h, "layout": "padded [B, k+1, V] / [B, k, V]"})
 
-    peaks, peak_kind = measured_peaks()
-    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    sweep_gbs = rep.sweep_bytes / (k_sweep * 1e-3) / 1e9
-    round_bytes = rep.sweep_bytes + rep.final_bytes
-    value = aggregate_value(world, ms)
-
-    result = {
-        "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic",
-        "config": {"workload": name, "B": inp.B, "k": inp.k, "V": inp.V, "logits": inp.dtype,
-                   "seed": seed, "parallelism": f"replicas x{world}",
-                   "l2": (f"L2 flushed before every round ({logit_bytes / 1e6:.1f} MB of logits)"
-                          if flush else
-                          f"inputs larger than L2: {logit_bytes / 1e9:.2f} GB of logits resident, "
-                          "no flush between steps"),
-                   "early_exit": True},
-        "hbm_gbs": round_bytes / (ms * 1e-3) / 1e9,
-        "hbm_gbs_frac": round_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
-        "roofline": {"bound": "hbm", "kernel": "sweep_kernel", "achieved": sweep_gbs,
-                     "peak": hbm_peak, "unit": "GB/s", "frac": sweep_gbs / hbm_peak,
-                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)" if peak_kind ==
-                     "measured" else "fallback 6.8 TB/s",
-                     "traffic": ncu_traffic(name),
-                     "bytes_per_launch": rep.sweep_bytes},
-        "kernels_ms": {"plan": k_plan, "sweep": k_sweep, "final": k_final},
-        "round_ms_percentiles": round_pct,
-        "round_bytes": {"sweep": rep.sweep_bytes, "final": rep.final_bytes},
-        "e2e": {"value": world / e2e_s, "unit": "rounds/s", "h2d_bytes_per_step": h2d_packed,
-                "d2h_bytes_per_step": d2h, "layout": "packed (rows 0..L_b of each request)",
-                "same_outputs": e2e_same},
-        "e2e_padded": {"value": world / e2e_padded_s, "unit": "rounds/s",
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "layout": "padded [B, k+1, V] / [B, k, V]"},
-        "gpu_launches": 3 * args.steps,
-        "clocks": clocks,
-    }
-    if full is not None:
-        full["sweep_frac"] = full["sweep_gbs"] / hbm_peak
-        result["full_sweep"] = full
-    if packed is not None:
-        result["packed"] = packed
-    if opd is not None:
-        opd["frac"] = opd["gbs"] / hbm_peak
-        result["opd"] = opd
-    if d3d is not None:
-        result["d3d"] = d3d
-
-    if world == 1 and not args.no_cpu_baseline:
+    def cpu_baseline(self, result, round_bytes):
+        """The oracle on one host core for about ten seconds of full rounds, and the
+        parity of the timed run against it."""
         import oracle
+        inp = self.inp
         oracle.build()
         reps, spent = 0, 0.0
         t0 = time.perf_counter()
@@ -603,17 +566,86 @@ def run_ours(args, world, rank, local):
         result["cpu_baseline"] = {
             "value": reps / spent, "unit": "rounds/s", "cores": 1, "kind": "oracle",
             "sample": f"the full {inp.B}-request round, {reps} time(s), single-threaded fp64 oracle"}
-        same = (gpu_n == o.num_accepted) & _np.all(gpu_out == o.out_tokens, axis=1)
+        same = (self.gpu_n == o.num_accepted) & np.all(self.gpu_out == o.out_tokens, axis=1)
         near = o.margin < 1e-6
-        m1, m2 = model_bytes(inp, o, esize)
+        m1, m2 = model_bytes(inp, o, self.esize)
         result["parity"] = {"requests": int(inp.B), "mismatches": int((~same).sum()),
                             "outside_near_tie_band": int((~same & ~near).sum()),
                             "near_ties": int(near.sum())}
         result["byte_models"] = {"M1_all_rows": m1, "M2_rows_to_first_reject": m2,
                                  "moved": round_bytes,
-                                 "M1_gbs": m1 / (ms * 1e-3) / 1e9,
+                                 "M1_gbs": m1 / (self.ms * 1e-3) / 1e9,
                                  "mean_accepted": float(o.num_accepted.mean())}
-    print(json.dumps(result), flush=True)
+
+    def run(self):
+        args, inp = self.args, self.inp
+        props = self.torch.cuda.get_device_properties(self.dev)
+        sampler = ClockSampler(f"GPU-{props.uuid}" if getattr(props, "uuid", None)
+                               else str(self.dev.index))
+        self.timed_rounds()
+        round_pct = self.round_percentiles()
+        k_plan, k_sweep, k_final = self.kernel_times()
+        full = None if args.no_full_sweep else self.full_sweep_leg()
+        packed = None if args.no_packed else self.packed_leg()
+        opd = None if args.no_opd else self.opd_leg()
+        d3d = None if args.no_d3d else self.d3d_leg()
+        e2e, e2e_padded = self.e2e_legs()
+        clocks = sampler.stop()
+        self.ranks.barrier()
+        if self.rank != 0:
+            return
+
+        rep, ms, world = self.rep, self.ms, self.world
+        peaks, peak_kind = measured_peaks()
+        hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+        sweep_gbs = rep.sweep_bytes / (k_sweep * 1e-3) / 1e9
+        round_bytes = rep.sweep_bytes + rep.final_bytes
+        lb = self.logit_bytes
+        result = {
+            "metric": METRIC, "value": aggregate_value(world, ms), "unit": "rounds/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": self.name, "B": inp.B, "k": inp.k, "V": inp.V,
+                       "logits": inp.dtype, "seed": self.seed, "parallelism": f"replicas x{world}",
+                       "l2": (f"L2 flushed before every round ({lb / 1e6:.1f} MB of logits)"
+                              if self.flush else
+                              f"inputs larger than L2: {lb / 1e9:.2f} GB of logits resident, "
+                              "no flush between steps"),
+                       "early_exit": True},
+            "hbm_gbs": round_bytes / (ms * 1e-3) / 1e9,
+            "hbm_gbs_frac": round_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
+            "roofline": {"bound": "hbm", "kernel": "sweep_kernel", "achieved": sweep_gbs,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": sweep_gbs / hbm_peak,
+                         "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"
+                         if peak_kind == "measured" else "fallback 6.8 TB/s",
+                         "traffic": ncu_traffic(self.name),
+                         "bytes_per_launch": rep.sweep_bytes},
+            "kernels_ms": {"plan": k_plan, "sweep": k_sweep, "final": k_final},
+            "round_ms_percentiles": round_pct,
+            "round_bytes": {"sweep": rep.sweep_bytes, "final": rep.final_bytes},
+            "e2e": e2e,
+            "e2e_padded": e2e_padded,
+            "gpu_launches": 3 * args.steps,
+            "clocks": clocks,
+        }
+        if full is not None:
+            full["sweep_frac"] = full["sweep_gbs"] / hbm_peak
+            result["full_sweep"] = full
+        if packed is not None:
+            result["packed"] = packed
+        if opd is not None:
+            opd["frac"] = opd["gbs"] / hbm_peak
+            result["opd"] = opd
+        if d3d is not None:
+            result["d3d"] = d3d
+        if world == 1 and not args.no_cpu_baseline:
+            self.cpu_baseline(result, round_bytes)
+        print(json.dumps(result), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    OurArm(args, world, rank, local).run()
 
 
 def main():
