@@ -34,7 +34,7 @@ struct FinalParams {
   const float* uniforms;
   const float* temperature;
   int B, k, V;
-  int P;           // slice CTAs per request (gridDim.x)
+  int P;           // slice CTAs per request; CTA x is slice x % P of request x / P
   int sweep_grid;  // CTAs of the sweep grid this pass follows
   int32_t* out_tokens;
   int32_t* num_accepted;
@@ -596,7 +596,10 @@ template <typename TIn>
 __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh, float2* rec_sm,
                                            FinalRing& fr) {
   const int nseg = segments_of(p.V);
-  const int part = blockIdx.x, b = blockIdx.y, P = gridDim.x;
+  // A one-dimensional grid of B * P CTAs (a grid's y extent stops at 65535,
+  // below the largest supported batch): slice `part` of request `b`.
+  const int P = p.P;
+  const int b = (int)(blockIdx.x / (unsigned)P), part = (int)(blockIdx.x - (unsigned)b * P);
   WsHeader* h = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
   float2* rec = reinterpret_cast<float2*>(p.ws + p.lay.seg_mass) + (size_t)b * nseg;
   float* slice_ref = reinterpret_cast<float*>(p.ws + p.lay.slice_ref) + (size_t)b * kMaxSlices;
@@ -816,7 +819,7 @@ __global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) 
   if (threadIdx.x == 0) {
     WsHeader* h = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
     __threadfence();
-    const int total = (int)(gridDim.x * gridDim.y);
+    const int total = (int)gridDim.x;
     if (atomicAdd(&h->final_ctas_done, 1) == total - 1) {
       const unsigned long long t0 = global_ns();
       while (*(volatile int32_t*)&h->sweep_exited < p.sweep_grid) {

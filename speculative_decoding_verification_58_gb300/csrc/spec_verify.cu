@@ -288,7 +288,7 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
   // segment records.
   const size_t fsm = std::max((size_t)nseg * sizeof(float2), (size_t)kFinalStages * kFinalStageBytes);
   if (record(ev, 2, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (launch(final_kernel<TIn>, dim3(P, B), dim3(kFinalThreads), fsm, stream, pdl, fp) !=
+  if (launch(final_kernel<TIn>, dim3((unsigned)(P * B)), dim3(kFinalThreads), fsm, stream, pdl, fp) !=
       cudaSuccess)
     return SPEC_ERR_CUDA;
   if (record(ev, 3, stream) != cudaSuccess) return SPEC_ERR_CUDA;

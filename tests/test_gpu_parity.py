@@ -285,3 +285,15 @@ def test_round_captured_in_a_cuda_graph_replays_with_new_contents():
                           inp.temperature)
         compare(out.cpu().numpy(), nacc.cpu().numpy(), o, inp.temperature, "graph replay")
         assert sv.spec_verify_report(ws).status == sv.SPEC_OK
+
+
+@pytest.mark.parametrize("B,k,V,dtype", [
+    (70000, 3, 24, "f32"),      # more requests than a grid's y extent holds
+    (1 << 18, 1, 16, "bf16"),   # SPEC_MAX_B
+])
+def test_largest_batches(B, k, V, dtype):
+    inp = _inputs(B, k, V, dtype, seed=B % 97)
+    inp.lengths = np.random.default_rng(B).integers(1, k + 1, B).astype(np.int32)
+    inp.temperature[::7] = 0.0
+    info, rep, o = check(inp, f"B={B}")
+    assert rep.rows_planned == int(np.sum(np.where(inp.temperature == 0, 1, 2) * inp.lengths))
