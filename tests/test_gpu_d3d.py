@@ -88,3 +88,12 @@ def test_d3d_after_verification_on_the_device():
     np.testing.assert_array_equal(hit.cpu().numpy()[same], want_hit[same])
     np.testing.assert_array_equal(nxt.cpu().numpy()[same], want_nxt[same])
     assert int(hits.item()) == int((hit.cpu().numpy() >= 0).sum())
+
+
+def test_d3d_many_requests():
+    n, out, br = planted(70000, 4, 100, 3, 2, 8, seed=70)
+    want = oracle.d3d_select(n, out, br.pos, br.tok, br.block)
+    got = run(n, out, br)
+    np.testing.assert_array_equal(got[0], want[0])
+    np.testing.assert_array_equal(got[1], want[1])
+    assert got[2] == want[2]

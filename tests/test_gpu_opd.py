@@ -136,3 +136,15 @@ def test_opd_host_checks():
     for kw in (dict(delta=0.0), dict(delta=float("inf")), dict(alpha=1.5), dict(alpha=-0.1)):
         with pytest.raises(sv.SpecVerifyError):
             sv.spec_opd_stats(d["target_logits"], d["draft_logits"], d["lengths"], **kw)
+
+
+def test_opd_many_requests():
+    """More requests than a grid's y extent holds; every position in one launch."""
+    rng = np.random.default_rng(8)
+    B, k, V = 70000, 2, 16
+    t = rng.standard_normal((B, k + 1, V)).astype(np.float32)
+    d = (t[:, :k] + rng.standard_normal((B, k, V))).astype(np.float32)
+    L = rng.integers(1, k + 1, B).astype(np.int32)
+    big = synth.SpecInputs(t, d, np.zeros((B, k), np.int32), L, np.zeros((B, k + 1), np.float32),
+                           np.ones(B, np.float32), "f32")
+    check(big, "B=70000")
