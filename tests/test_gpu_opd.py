@@ -148,3 +148,13 @@ def test_opd_many_requests():
     big = synth.SpecInputs(t, d, np.zeros((B, k), np.int32), L, np.zeros((B, k + 1), np.float32),
                            np.ones(B, np.float32), "f32")
     check(big, "B=70000")
+
+
+def test_opd_largest_vocabulary():
+    V = 1 << 21
+    rng = np.random.default_rng(21)
+    t = (rng.standard_normal((2, 3, V)) * 2).astype(np.float32)
+    d = (t[:, :2] + rng.standard_normal((2, 2, V))).astype(np.float32)
+    inp = synth.SpecInputs(t, d, np.zeros((2, 2), np.int32), np.array([2, 1], np.int32),
+                           np.zeros((2, 3), np.float32), np.ones(2, np.float32), "f32")
+    check(inp, "V=2^21")

@@ -297,3 +297,13 @@ def test_largest_batches(B, k, V, dtype):
     inp.temperature[::7] = 0.0
     info, rep, o = check(inp, f"B={B}")
     assert rep.rows_planned == int(np.sum(np.where(inp.temperature == 0, 1, 2) * inp.lengths))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_largest_vocabulary(dtype):
+    """V = SPEC_MAX_V (2^21): the most segments the final pass holds in shared memory."""
+    V = 1 << 21
+    inp = _inputs(2, 3, V, dtype, seed=21)
+    inp.lengths[:] = [3, 1]
+    inp.temperature[1] = 0.0
+    check(inp, f"V=2^21 {dtype}")
