@@ -85,6 +85,8 @@ SMALL = [
     ("zipf_mixed_temp", 40, 7, 1001, "bf16"),   # rows not 16-byte aligned
     ("zipf_mixed_noise", 17, 3, 333, "f32"),
     ("zipf_adaptive", 5, 1, 9, "bf16"),
+    ("zipf_adaptive", 40, 31, 2000, "bf16"),   # SPEC_MAX_K: 31 positions, 32-bit masks
+    ("zipf_mixed_temp", 24, 31, 1500, "f32"),
 ]
 
 
