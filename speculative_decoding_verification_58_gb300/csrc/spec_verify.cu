@@ -183,20 +183,33 @@ bool sizes_ok(int B, int k, int V) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Make the device that owns `p` current for this library's runtime on this
-// thread (the caller's framework may keep its own notion of the current
-// device).  Host or unregistered pointers leave the current device alone.
-cudaError_t use_device_of(const void* p) {
-  cudaPointerAttributes a;
-  cudaError_t e = cudaPointerGetAttributes(&a, p);
-  if (e != cudaSuccess) return e;
-  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
-    int cur = -1;
-    if ((e = cudaGetDevice(&cur)) != cudaSuccess) return e;
-    if (cur != a.device && a.device >= 0) return cudaSetDevice(a.device);
+// For the duration of one entry point, make the device that owns `p` current
+// on this thread (the caller's framework may keep its own notion of the
+// current device), and give the caller's current device back on return.
+// Host or unregistered pointers leave the current device alone.
+class DeviceOf {
+ public:
+  explicit DeviceOf(const void* p) {
+    cudaPointerAttributes a;
+    err_ = cudaPointerGetAttributes(&a, p);
+    if (err_ != cudaSuccess) return;
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged) return;
+    if ((err_ = cudaGetDevice(&prev_)) != cudaSuccess) return;
+    if (a.device >= 0 && a.device != prev_) {
+      err_ = cudaSetDevice(a.device);
+      switched_ = (err_ == cudaSuccess);
+    }
   }
-  return cudaSuccess;
-}
+  ~DeviceOf() {
+    if (switched_) cudaSetDevice(prev_);
+  }
+  bool ok() const { return err_ == cudaSuccess; }
+
+ private:
+  cudaError_t err_ = cudaSuccess;
+  int prev_ = -1;
+  bool switched_ = false;
+};
 
 template <typename TIn>
 spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
@@ -482,7 +495,8 @@ static spec_status_t verify_entry(const void* target_logits, const void* draft_l
   if (!workspace || !aligned(workspace, 256) ||
       workspace_bytes < spec_verify_workspace_bytes(B, k, V))
     return SPEC_ERR_WORKSPACE;
-  if (use_device_of(target_logits) != cudaSuccess) return SPEC_ERR_CUDA;
+  DeviceOf on_device(target_logits);
+  if (!on_device.ok()) return SPEC_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SPEC_F32)
     return verify_typed<float>(target_logits, draft_logits, draft_tokens, lengths, uniforms,
@@ -544,7 +558,8 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits, s
 spec_status_t spec_verify_report(const void* workspace, void* stream, spec_verify_report_t* report) {
   if (!workspace || !report) return SPEC_ERR_INVALID_ARG;
   WsHeader h;
-  if (use_device_of(workspace) != cudaSuccess) return SPEC_ERR_CUDA;
+  DeviceOf on_device(workspace);
+  if (!on_device.ok()) return SPEC_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(&h, workspace, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return SPEC_ERR_CUDA;
@@ -590,7 +605,8 @@ spec_status_t spec_opd_stats(const void* target_logits, const void* draft_logits
     return SPEC_ERR_INVALID_ARG;
   const bool vec_ok = aligned(target_logits, 16) && aligned(draft_logits, 16) &&
                       ((size_t)V * esize) % 16 == 0;
-  if (use_device_of(target_logits) != cudaSuccess) return SPEC_ERR_CUDA;
+  DeviceOf on_device(target_logits);
+  if (!on_device.ok()) return SPEC_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SPEC_F32)
     return opd_typed<float>(target_logits, draft_logits, lengths, B, k, V, delta, alpha, x_star,
@@ -613,7 +629,8 @@ spec_status_t spec_d3d_select(const int32_t* num_accepted, const int32_t* out_to
       !aligned(branch_tok, 4) || !aligned(branch_block, 4) || !aligned(hit, 4) ||
       !aligned(next_block, 4) || (hits && !aligned(hits, 4)))
     return SPEC_ERR_INVALID_ARG;
-  if (use_device_of(num_accepted) != cudaSuccess) return SPEC_ERR_CUDA;
+  DeviceOf on_device(num_accepted);
+  if (!on_device.ok()) return SPEC_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch(d3d_select_kernel, dim3((B + kD3dWarps - 1) / kD3dWarps), dim3(kD3dWarps * 32), 0, s,
              true, num_accepted, out_tokens, branch_pos, branch_tok, branch_block, B, k, NB, blk,
@@ -646,7 +663,8 @@ spec_status_t spec_row_stats(const void* logits, spec_dtype_t dtype, int rows, i
   if (!workspace || !aligned(workspace, 256) ||
       workspace_bytes < spec_row_stats_workspace_bytes(rows, V))
     return SPEC_ERR_WORKSPACE;
-  if (use_device_of(logits) != cudaSuccess) return SPEC_ERR_CUDA;
+  DeviceOf on_device(logits);
+  if (!on_device.ok()) return SPEC_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SPEC_F32)
     return row_stats_typed<float>(logits, rows, V, temperature, row_max, row_lse, row_arg, workspace,
@@ -716,7 +734,8 @@ extern "C" spec_status_t spec_verify_static(const void* target_logits, const voi
   // The batch must fit the fixed scratch.
   const size_t need = spec_verify_workspace_bytes(B, k, V);
   if (need == 0 || need > SPEC_STATIC_SCRATCH_BYTES) return SPEC_ERR_UNSUPPORTED;
-  if (use_device_of(target_logits) != cudaSuccess) return SPEC_ERR_CUDA;
+  DeviceOf on_device(target_logits);
+  if (!on_device.ok()) return SPEC_ERR_CUDA;
   void* scratch = nullptr;
   if (static_scratch(&scratch) != cudaSuccess) return SPEC_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
