@@ -59,9 +59,9 @@ struct OpdParams {
 struct OpdStageInfo {
   int j;     // index of the position in this cluster's list
   int pass;  // 1 or 2
-  int e0;    // first element of the stage within this CTA's half
+  int e0;    // first element of the stage within this CTA's part of the rows
   int ne;    // elements of each row in the stage
-  int last;  // last stage of the pass over this CTA's half
+  int last;  // last stage of the pass over this CTA's part
 };
 
 // Pass-1 partial of a CTA (or a consumer warp): both rows' softmax partials
@@ -251,7 +251,7 @@ __device__ __forceinline__ void opd_abort(OpdSmem& sm) {
 }
 
 // ---------------------------------------------------------------------------
-// Producer warp: both rows' halves, chunk by chunk, into the ring.
+// Producer warp: this CTA's part of both rows, chunk by chunk, into the ring.
 // ---------------------------------------------------------------------------
 template <typename TIn>
 __device__ void opd_producer(const OpdParams& p, OpdSmem& sm, int cid, int ncl, int s0) {
@@ -429,7 +429,7 @@ __device__ void opd_consumers(const OpdParams& p, OpdSmem& sm, int cid, int ncl,
       }
       if (I.last) break;
     }
-    // End of the pass over this CTA's half: one partial per warp.
+    // End of the pass over this CTA's part: one partial per warp.
     if (pass == 1) {
       soft_warp_reduce(at);
       soft_warp_reduce(ad);
