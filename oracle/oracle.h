@@ -29,7 +29,7 @@
  * or reordering.  Build with -ffp-contract=off so that no fused multiply-add
  * changes the rounding between machines.
  *
- * Readings taken where the pages are silent (each is listed in the design doc too):
+ * Readings taken where the pages are silent:
  *  - decision i uses uniforms[b][i] with the strict test u < min(1, ratio);
  *  - the final (residual or bonus) sample uses uniforms[b][L_b];
  *  - inverse CDF in ascending vocabulary index: the first index j whose
