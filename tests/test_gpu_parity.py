@@ -309,3 +309,27 @@ def test_largest_vocabulary(dtype):
     inp.lengths[:] = [3, 1]
     inp.temperature[1] = 0.0
     check(inp, f"V=2^21 {dtype}")
+
+
+def test_timed_call_and_device_status():
+    """spec_verify_timed gives the same outputs as spec_verify and records its
+    four events in order; spec_verify_device_status reads the recorded status."""
+    inp = synth.make_inputs("zipf_mixed_temp", 24, 16, 5000, "bf16", seed=61)
+    d = sv.to_device(inp)
+    ws = sv.alloc_workspace(inp.B, inp.k, inp.V)
+    want_out, want_n = sv.spec_verify(**d, workspace=ws)
+    want_out, want_n = want_out.cpu().numpy(), want_n.cpu().numpy()
+    assert sv.spec_verify_device_status(ws) == sv.SPEC_OK
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in evs:
+        e.record()
+    torch.cuda.synchronize()
+    out, n = sv.spec_verify(**d, workspace=ws, events=evs)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy(), want_out)
+    np.testing.assert_array_equal(n.cpu().numpy(), want_n)
+    times = [evs[0].elapsed_time(e) for e in evs]
+    assert all(b >= a for a, b in zip(times, times[1:])) and times[-1] > 0
+    d["lengths"][3] = 0  # an invalid length: recorded on the device
+    sv.spec_verify(**d, workspace=ws)
+    assert sv.spec_verify_device_status(ws) == sv.SPEC_ERR_BAD_INPUT
