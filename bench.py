@@ -9,7 +9,9 @@ half with high draft noise (see speculative_decoding_verification_58_gb300/synth
 Prints one JSON line.  ``value`` is verification rounds per second over all
 ranks (each rank verifies its own batch: weak scaling, no collective on the
 data path), with inputs resident in HBM.  The logits (1.28 GB at the default
-workload) are far larger than L2, so no flush is needed between steps.
+workload) are far larger than L2, so no flush is needed between steps; the
+rounds rotate over COPIES resident copies of them, so that no round reads
+rows the round before left in L2 (real rounds get fresh logits).
 
 ``--impl reference`` times the plain CPU oracle (the reference this library
 is checked against) on the host cores on the same workload instead.
@@ -36,6 +38,7 @@ import numpy as np  # noqa: E402
 METRIC = "verify rounds/s & achieved HBM GB/s at B=128,k=16,V=151936 bf16 (1 GB300)"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1000 * 1000  # GB300 L2 (126 MiB)
+COPIES = 3  # resident copies of the batch's logits, used in turn by successive rounds
 
 
 def parse_args():
@@ -301,22 +304,31 @@ class OurArm:
         self.inp = inp = synth.make_workload(self.name, seed=self.seed)
         self.esize = 2 if inp.dtype == "bf16" else 4
         self.d = sv.to_device(inp, dev)
+        # Successive rounds read different copies of the logits (the small
+        # per-request inputs are shared).
+        self.ds = [self.d] + [dict(self.d, target_logits=self.d["target_logits"].clone(),
+                                   draft_logits=self.d["draft_logits"].clone())
+                              for _ in range(COPIES - 1)]
+        self.turn = 0
         self.ws = sv.alloc_workspace(inp.B, inp.k, inp.V, dev)
         self.out = torch.empty((inp.B, inp.k + 1), dtype=torch.int32, device=dev)
         self.nacc = torch.empty(inp.B, dtype=torch.int32, device=dev)
         self.stream = torch.cuda.current_stream(dev)
         # Bound calls: buffers checked once, one C call per round.
-        self.bound = {fs: sv.Verifier(**self.d, workspace=self.ws, out_tokens=self.out,
-                                      num_accepted=self.nacc, stream=self.stream, full_sweep=fs)
+        self.bound = {fs: [sv.Verifier(**dc, workspace=self.ws, out_tokens=self.out,
+                                       num_accepted=self.nacc, stream=self.stream, full_sweep=fs)
+                           for dc in self.ds]
                       for fs in (False, True)}
         self.logit_bytes = inp.target.nbytes + inp.draft.nbytes
         self.reps = max(10, min(args.steps, 200))
 
     def step(self, full_sweep=False, events=None):
+        c = self.turn % COPIES
+        self.turn += 1
         if events is None:
-            self.bound[full_sweep]()
+            self.bound[full_sweep][c]()
         else:
-            self.sv.spec_verify(**self.d, workspace=self.ws, out_tokens=self.out,
+            self.sv.spec_verify(**self.ds[c], workspace=self.ws, out_tokens=self.out,
                                 num_accepted=self.nacc, stream=self.stream,
                                 full_sweep=full_sweep, events=events)
 
@@ -409,16 +421,18 @@ class OurArm:
         sv, d = self.sv, self.d
         pk = self.synth.pack_rows(self.inp)
         rows = sv.to_device_packed(pk, self.dev)
-        pargs = dict(**rows, draft_tokens=d["draft_tokens"], lengths=d["lengths"],
-                     uniforms=d["uniforms"], temperature=d["temperature"], workspace=self.ws,
-                     out_tokens=self.out, num_accepted=self.nacc, stream=self.stream)
-        for _ in range(3):
-            sv.spec_verify_packed(**pargs)
+        pargs = [dict(**{key: (t if c == 0 else t.clone()) for key, t in rows.items()},
+                      draft_tokens=d["draft_tokens"], lengths=d["lengths"],
+                      uniforms=d["uniforms"], temperature=d["temperature"], workspace=self.ws,
+                      out_tokens=self.out, num_accepted=self.nacc, stream=self.stream)
+                 for c in range(COPIES)]
+        for j in range(3):
+            sv.spec_verify_packed(**pargs[j % COPIES])
         self.sync()
         p0, p1 = _event_pair()
         p0.record(self.stream)
-        for _ in range(self.reps):
-            sv.spec_verify_packed(**pargs)
+        for j in range(self.reps):
+            sv.spec_verify_packed(**pargs[j % COPIES])
         p1.record(self.stream)
         self.sync()
         same = bool(np.array_equal(self.out.cpu().numpy(), self.gpu_out) and
@@ -436,16 +450,19 @@ class OurArm:
         sv, d, inp = self.sv, self.d, self.inp
         st = sv.spec_opd_stats(d["target_logits"], d["draft_logits"], d["lengths"],
                                stream=self.stream)
-        call = lambda: sv.spec_opd_stats(d["target_logits"], d["draft_logits"], d["lengths"],
-                                         out=st, stream=self.stream)
-        for _ in range(3):
-            call()
+
+        def call(j):
+            dc = self.ds[j % COPIES]
+            sv.spec_opd_stats(dc["target_logits"], dc["draft_logits"], dc["lengths"], out=st,
+                              stream=self.stream)
+        for j in range(3):
+            call(j)
         self.sync()
         o0, o1 = _event_pair()
         oreps = max(10, min(self.args.steps, 100))
         o0.record(self.stream)
-        for _ in range(oreps):
-            call()
+        for j in range(oreps):
+            call(j)
         o1.record(self.stream)
         self.sync()
         oms = o0.elapsed_time(o1) / oreps
@@ -610,8 +627,8 @@ class OurArm:
                        "logits": inp.dtype, "seed": self.seed, "parallelism": f"replicas x{world}",
                        "l2": (f"L2 flushed before every round ({lb / 1e6:.1f} MB of logits)"
                               if self.flush else
-                              f"inputs larger than L2: {lb / 1e9:.2f} GB of logits resident, "
-                              "no flush between steps"),
+                              f"inputs larger than L2: {lb / 1e9:.2f} GB of logits, "
+                              f"{COPIES} resident copies used in turn, no flush between steps"),
                        "early_exit": True},
             "hbm_gbs": round_bytes / (ms * 1e-3) / 1e9,
             "hbm_gbs_frac": round_bytes / (ms * 1e-3) / 1e9 / hbm_peak,

@@ -319,8 +319,9 @@ __device__ bool slice_records_staged(const TIn* rt, const TIn* rd, int V, const 
     const uint32_t nb = piece_bytes(j);
     unsigned char* dst = ring + slot * kFinalStageBytes;
     mbar_arrive_expect_tx(&fr.full[slot], nb * R);
-    bulk_g2s(dst, rt + (size_t)g0 * kSegElems, nb, &fr.full[slot]);
-    if (has_q) bulk_g2s(dst + S * SB, rd + (size_t)g0 * kSegElems, nb, &fr.full[slot]);
+    const uint64_t pol = l2_policy_evict_first();
+    bulk_g2s_hint(dst, rt + (size_t)g0 * kSegElems, nb, &fr.full[slot], pol);
+    if (has_q) bulk_g2s_hint(dst + S * SB, rd + (size_t)g0 * kSegElems, nb, &fr.full[slot], pol);
   };
   if (threadIdx.x == 0)
     for (int j = 0; j < kFinalStages && j < npieces; ++j) issue(j);

@@ -151,26 +151,6 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
     }
   }
 }
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-// bulk_g2s with an L2 cache policy.
-__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
-                                              uint64_t* bar, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-      : "memory");
-}
-
 // Per-element pass-2 term q log(q/p) = q (dz - c) with dz = z_d - z_t,
 // c = lse_d - lse_t and q = 2^(z_d log2 e + nl2d), nl2d = -lse_d log2 e.
 // Only infinite logits make it non-finite; then 0 log 0 = 0 (z_d = -inf)

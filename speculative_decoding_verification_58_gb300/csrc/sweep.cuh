@@ -233,7 +233,8 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
           I.slot = slot;
           if (nb > 0) {
             mbar_arrive_expect_tx(&sm.full[s], (uint32_t)nb);
-            bulk_g2s(sm.stage[s], src0 + off, (uint32_t)nb, &sm.full[s]);
+            bulk_g2s_hint(sm.stage[s], src0 + off, (uint32_t)nb, &sm.full[s],
+                      l2_policy_evict_first());
           } else {
             mbar_arrive(&sm.full[s]);
           }
@@ -385,7 +386,8 @@ __device__ void sweep_producer_big(const SweepParams& p, SweepSmem& sm, WsHeader
       I.slot = slot;
       if (nb > 0) {
         mbar_arrive_expect_tx(&sm.full[s], (uint32_t)nb);
-        bulk_g2s(sm.stage[s], src0 + off, (uint32_t)nb, &sm.full[s]);
+        bulk_g2s_hint(sm.stage[s], src0 + off, (uint32_t)nb, &sm.full[s],
+                      l2_policy_evict_first());
       } else {
         mbar_arrive(&sm.full[s]);
       }
