@@ -10,8 +10,9 @@ Prints one JSON line.  ``value`` is verification rounds per second over all
 ranks (each rank verifies its own batch: weak scaling, no collective on the
 data path), with inputs resident in HBM.  The logits (1.28 GB at the default
 workload) are far larger than L2, so no flush is needed between steps; the
-rounds rotate over COPIES resident copies of them, so that no round reads
-rows the round before left in L2 (real rounds get fresh logits).
+rounds rotate over ``--copies`` (default 3) resident copies of them, so that
+no round reads rows the round before left in L2 (real rounds get fresh
+logits).
 
 ``--impl reference`` times the plain CPU oracle (the reference this library
 is checked against) on the host cores on the same workload instead.
@@ -38,7 +39,7 @@ import numpy as np  # noqa: E402
 METRIC = "verify rounds/s & achieved HBM GB/s at B=128,k=16,V=151936 bf16 (1 GB300)"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1000 * 1000  # GB300 L2 (126 MiB)
-COPIES = 3  # resident copies of the batch's logits, used in turn by successive rounds
+COPIES = 3  # default resident copies of the batch's logits, used in turn by successive rounds
 
 
 def parse_args():
@@ -55,6 +56,9 @@ def parse_args():
     ap.add_argument("--no-packed", action="store_true")
     ap.add_argument("--no-opd", action="store_true")
     ap.add_argument("--no-d3d", action="store_true")
+    ap.add_argument("--copies", type=int, default=COPIES,
+                    help="resident copies of the logits that successive rounds read in turn "
+                         "(1 for small profiler captures)")
     return ap.parse_args()
 
 
@@ -308,7 +312,7 @@ class OurArm:
         # per-request inputs are shared).
         self.ds = [self.d] + [dict(self.d, target_logits=self.d["target_logits"].clone(),
                                    draft_logits=self.d["draft_logits"].clone())
-                              for _ in range(COPIES - 1)]
+                              for _ in range(max(1, args.copies) - 1)]
         self.turn = 0
         self.ws = sv.alloc_workspace(inp.B, inp.k, inp.V, dev)
         self.out = torch.empty((inp.B, inp.k + 1), dtype=torch.int32, device=dev)
@@ -323,7 +327,7 @@ class OurArm:
         self.reps = max(10, min(args.steps, 200))
 
     def step(self, full_sweep=False, events=None):
-        c = self.turn % COPIES
+        c = self.turn % len(self.ds)
         self.turn += 1
         if events is None:
             self.bound[full_sweep][c]()
@@ -425,14 +429,14 @@ class OurArm:
                       draft_tokens=d["draft_tokens"], lengths=d["lengths"],
                       uniforms=d["uniforms"], temperature=d["temperature"], workspace=self.ws,
                       out_tokens=self.out, num_accepted=self.nacc, stream=self.stream)
-                 for c in range(COPIES)]
+                 for c in range(len(self.ds))]
         for j in range(3):
-            sv.spec_verify_packed(**pargs[j % COPIES])
+            sv.spec_verify_packed(**pargs[j % len(pargs)])
         self.sync()
         p0, p1 = _event_pair()
         p0.record(self.stream)
         for j in range(self.reps):
-            sv.spec_verify_packed(**pargs[j % COPIES])
+            sv.spec_verify_packed(**pargs[j % len(pargs)])
         p1.record(self.stream)
         self.sync()
         same = bool(np.array_equal(self.out.cpu().numpy(), self.gpu_out) and
@@ -452,7 +456,7 @@ class OurArm:
                                stream=self.stream)
 
         def call(j):
-            dc = self.ds[j % COPIES]
+            dc = self.ds[j % len(self.ds)]
             sv.spec_opd_stats(dc["target_logits"], dc["draft_logits"], dc["lengths"], out=st,
                               stream=self.stream)
         for j in range(3):
@@ -628,7 +632,8 @@ class OurArm:
                        "l2": (f"L2 flushed before every round ({lb / 1e6:.1f} MB of logits)"
                               if self.flush else
                               f"inputs larger than L2: {lb / 1e9:.2f} GB of logits, "
-                              f"{COPIES} resident copies used in turn, no flush between steps"),
+                              f"{len(self.ds)} resident copies used in turn, "
+                              "no flush between steps"),
                        "early_exit": True},
             "hbm_gbs": round_bytes / (ms * 1e-3) / 1e9,
             "hbm_gbs_frac": round_bytes / (ms * 1e-3) / 1e9 / hbm_peak,
