@@ -363,6 +363,107 @@ __device__ __forceinline__ void arg_init(ArgAcc& a) {
   a.i = INT32_MAX;
 }
 
+// ---------------------------------------------------------------------------
+// One consumer thread's batch of a stage: N 16-byte vectors of one row held
+// in registers.  Vectors past the stage's end are -inf in every element, so
+// they change neither a max nor a sum of exponentials.
+// ---------------------------------------------------------------------------
+template <typename TIn>
+__device__ __forceinline__ uint4 neg_inf_vec() {
+  const uint32_t w = sizeof(TIn) == 2 ? 0xFF80FF80u : 0xFF800000u;
+  return make_uint4(w, w, w, w);
+}
+
+// Largest element of the batch.
+template <typename TIn, int N>
+__device__ __forceinline__ float batch_max(const uint4 (&v)[N]) {
+  static_assert((N & (N - 1)) == 0, "batch_max reduces a power-of-two batch");
+  if constexpr (sizeof(TIn) == 2) {
+    uint32_t m[N];
+#pragma unroll
+    for (int t = 0; t < N; ++t)
+      m[t] = bf16x2_max(bf16x2_max(v[t].x, v[t].y), bf16x2_max(v[t].z, v[t].w));
+#pragma unroll
+    for (int w = N / 2; w > 0; w >>= 1)
+#pragma unroll
+      for (int t = 0; t < w; ++t) m[t] = bf16x2_max(m[t], m[t + w]);
+    return fmaxf(__uint_as_float(m[0] << 16), __uint_as_float(m[0] & 0xffff0000u));
+  } else {
+    float m[N];
+#pragma unroll
+    for (int t = 0; t < N; ++t)
+      m[t] = fmaxf(fmaxf(__uint_as_float(v[t].x), __uint_as_float(v[t].y)),
+                   fmaxf(__uint_as_float(v[t].z), __uint_as_float(v[t].w)));
+#pragma unroll
+    for (int w = N / 2; w > 0; w >>= 1)
+#pragma unroll
+      for (int t = 0; t < w; ++t) m[t] = fmaxf(m[t], m[t + w]);
+    return m[0];
+  }
+}
+
+// Element e (in index order) of one vector.
+template <typename TIn>
+__device__ __forceinline__ float vec_elem(const uint4& v, int e) {
+  const uint32_t w = e < ElemTraits<TIn>::kPerVec / 2
+                         ? (e < ElemTraits<TIn>::kPerVec / 4 ? v.x : v.y)
+                         : (e < 3 * ElemTraits<TIn>::kPerVec / 4 ? v.z : v.w);
+  if (ElemTraits<TIn>::kPerVec == 4) return __uint_as_float(w);
+  return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+
+// Softmax accumulation of a batch: one max, at most one rescale, then
+// independent packed FMAs, one ex2 per element and four packed accumulators.
+template <typename TIn, int N>
+__device__ __forceinline__ void soft_stage(SoftAcc& a, const uint4 (&v)[N], float sc) {
+  const float gm = batch_max<TIn>(v);
+  if (gm > a.m) {
+    const float nms = __fmul_rn(gm, sc);
+    a.s = __fmul_rn(a.s, ex2(__fsub_rn(a.ms, nms)));
+    a.m = gm;
+    a.ms = nms;
+  }
+  const float2 s2 = make_float2(sc, sc), c2 = make_float2(-a.ms, -a.ms);
+  float2 acc[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int t = 0; t < N; ++t) {
+    const uint32_t w[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
+    if (ElemTraits<TIn>::kPerVec == 8) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 z = make_float2(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u));
+        acc[q] = f32x2_add(acc[q], ex2x2(f32x2_fma(z, s2, c2)));
+      }
+    } else {
+      const int q0 = (t & 1) * 2;
+      acc[q0] = f32x2_add(acc[q0], ex2x2(f32x2_fma(make_float2(__uint_as_float(w[0]), __uint_as_float(w[1])), s2, c2)));
+      acc[q0 + 1] = f32x2_add(acc[q0 + 1], ex2x2(f32x2_fma(make_float2(__uint_as_float(w[2]), __uint_as_float(w[3])), s2, c2)));
+    }
+  }
+  const float2 t2 = f32x2_add(f32x2_add(acc[0], acc[1]), f32x2_add(acc[2], acc[3]));
+  a.s = __fadd_rn(a.s, __fadd_rn(t2.x, t2.y));
+}
+
+// Argmax of a batch: one max; only when it beats the running best, a scan in
+// index order for its first occurrence.  `first` is the element index of
+// vector 0, vectors are `stride` elements apart.
+template <typename TIn, int N>
+__device__ __forceinline__ void arg_stage(ArgAcc& a, const uint4 (&v)[N], int first, int stride) {
+  constexpr int EPV = ElemTraits<TIn>::kPerVec;
+  const float gm = batch_max<TIn>(v);
+  if (!(gm > a.v)) return;
+  int found = INT32_MAX;
+#pragma unroll
+  for (int t = N - 1; t >= 0; --t)
+#pragma unroll
+    for (int e = EPV - 1; e >= 0; --e)
+      if (vec_elem<TIn>(v[t], e) == gm) found = first + t * stride + e;
+  a.v = gm;
+  a.i = found;
+}
+
 // Elements must be offered in increasing index order within one accumulator.
 __device__ __forceinline__ void arg_add(ArgAcc& a, float x, int idx) {
   if (x > a.v) {

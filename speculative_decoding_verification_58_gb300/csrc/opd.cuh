@@ -178,25 +178,6 @@ __device__ __forceinline__ void opd_add(OpdSums& s, float zt, float zd, float c,
   s.kl = __fadd_rn(s.kl, t);
 }
 
-// Pass 1 for one 16-byte vector of target logits: softmax partial and the
-// argmax, which is looked for element by element only when the vector's max
-// beats the best so far (elements come in increasing index order).
-template <typename TIn>
-__device__ __forceinline__ void opd_target_vec(SoftAcc& a, ArgAcc& g, const uint4& v, int idx0) {
-  using Tr = ElemTraits<TIn>;
-  soft_add_vec<TIn>(a, v, kLog2e);
-  // soft_add_vec leaves the running max in a.m; a new best is a larger max.
-  if (a.m > g.v) {
-    float x[Tr::kPerVec];
-    Tr::unpack(v, x);
-#pragma unroll
-    for (int e = Tr::kPerVec - 1; e >= 0; --e)
-      if (x[e] == a.m) g.i = idx0 + e;
-    g.v = a.m;
-  }
-}
-
-
 // The next position of this cluster, q, q + ncl, ... that has a verified row
 // pair (i < L_b, L_b valid); -1 when there is none.
 __device__ __forceinline__ int opd_next_active(const OpdParams& p, int q, int ncl) {
@@ -346,15 +327,20 @@ __device__ void opd_consumers(const OpdParams& p, OpdSmem& sm, int cid, int ncl,
       if (lane == 0) mbar_arrive(&sm.empty[s]);
       ++it;
       if (pass == 1) {
+        // The whole batch at once, as in the row sweep: one max and at most one
+        // rescale per row, then independent exponentials; vectors past the
+        // stage's end are -inf.
         const int base = s0 + I.e0;
 #pragma unroll
         for (int u = 0; u < kOpdVecPerThread; ++u) {
-          const int v = ctid + u * kOpdNC;
-          if (v < nvec) {
-            opd_target_vec<TIn>(at, ag, vt[u], base + v * EPV);
-            soft_add_vec<TIn>(ad, vd[u], kLog2e);
+          if (ctid + u * kOpdNC >= nvec) {
+            vt[u] = neg_inf_vec<TIn>();
+            vd[u] = neg_inf_vec<TIn>();
           }
         }
+        arg_stage<TIn>(ag, vt, base + ctid * EPV, kOpdNC * EPV);
+        soft_stage<TIn>(at, vt, kLog2e);
+        soft_stage<TIn>(ad, vd, kLog2e);
         if (ctid < rem) {
           soft_add1(at, xt, kLog2e);
           soft_add1(ad, xd, kLog2e);
