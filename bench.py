@@ -127,15 +127,18 @@ def measured_peaks():
 
 
 def csrc_digest() -> str:
-    """Digest of the sources the sweep kernel is built from (its code, the
-    shared helpers and the plan kernel that lays out its work)."""
+    """Digest of the code the sweep kernel is built from (its code, the shared
+    helpers and the plan kernel that lays out its work).  Line comments and
+    blank lines are left out, so that editing a comment keeps a recorded
+    capture valid; any change to the code itself does not."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_58_gb300", "csrc")
     files = [os.path.join(csrc, name) for name in ("common.cuh", "plan.cuh", "sweep.cuh")]
     for f in files:
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode())
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            code = [line.split("//", 1)[0].rstrip() for line in fh]
+        h.update(os.path.basename(f).encode())
+        h.update("\n".join(line for line in code if line).encode())
     return h.hexdigest()[:16]
 
 

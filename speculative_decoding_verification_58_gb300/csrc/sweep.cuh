@@ -9,7 +9,8 @@
 //   - lane 0 of the producer warp claims work units (one vocabulary chunk of
 //     one row) from a global counter and streams each chunk into a ring of
 //     shared-memory stages with 1-D bulk async copies (cp.async.bulk,
-//     completion counted on an mbarrier);
+//     completion counted on an mbarrier, L2 evict_first: each byte is read
+//     once);
 //   - eight consumer warps copy their share of a stage into registers, free
 //     the stage, take one packed max over it, rescale at most once, and then
 //     do independent FMA / ex2 / adds (or an argmax) on it;
