@@ -99,6 +99,10 @@ size_t spec_verify_workspace_bytes(int B, int k, int V);
  *                              u_{L_b} for the final sample (unused at T = 0)
  *   temperature   [B]          float: 0 = greedy; otherwise a normal float
  *                              (>= 2^-126) and finite
+ *   B, k, V                    B, k or V below 1 (an empty batch) is
+ *                              SPEC_ERR_INVALID_ARG; B > SPEC_MAX_B,
+ *                              k > SPEC_MAX_K or V > SPEC_MAX_V is
+ *                              SPEC_ERR_UNSUPPORTED
  *   out_tokens    [B, k+1]     int32 out: x_0..x_{n-1}, the final token, then -1
  *   num_accepted  [B]          int32 out: n in [0, L_b], or -1 for a request
  *                              whose inputs were invalid

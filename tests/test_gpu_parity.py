@@ -240,6 +240,15 @@ def test_host_argument_errors_launch_nothing():
     assert L.spec_verify(*bad) == sv.SPEC_ERR_UNSUPPORTED
     bad = list(args); bad[0] += 1
     assert L.spec_verify(*bad) == sv.SPEC_ERR_INVALID_ARG
+    # An empty batch, no draft positions or an empty vocabulary: nothing to do.
+    for idx in (7, 8, 9):
+        bad = list(args); bad[idx] = 0
+        assert L.spec_verify(*bad) == sv.SPEC_ERR_INVALID_ARG
+    assert L.spec_verify_workspace_bytes(0, 3, 64) == 0
+    # Beyond the largest supported sizes: refused, not an argument error.
+    for idx, big in ((7, (1 << 18) + 1), (9, (1 << 21) + 1)):
+        bad = list(args); bad[idx] = big
+        assert L.spec_verify(*bad) == sv.SPEC_ERR_UNSUPPORTED
     torch.cuda.synchronize()
 
 
