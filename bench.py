@@ -131,13 +131,21 @@ def csrc_digest() -> str:
     helpers and the plan kernel that lays out its work).  Line comments and
     blank lines are left out, so that editing a comment keeps a recorded
     capture valid; any change to the code itself does not."""
-    h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_58_gb300", "csrc")
-    files = [os.path.join(csrc, name) for name in ("common.cuh", "plan.cuh", "sweep.cuh")]
-    for f in files:
-        with open(f, encoding="utf-8") as fh:
-            code = [line.split("//", 1)[0].rstrip() for line in fh]
-        h.update(os.path.basename(f).encode())
+    texts = []
+    for name in ("common.cuh", "plan.cuh", "sweep.cuh"):
+        with open(os.path.join(csrc, name), encoding="utf-8") as fh:
+            texts.append((name, fh.read()))
+    return code_digest(texts)
+
+
+def code_digest(texts) -> str:
+    """Digest of (name, source text) pairs with line comments and blank lines
+    left out."""
+    h = hashlib.sha256()
+    for name, text in texts:
+        code = [line.split("//", 1)[0].rstrip() for line in text.splitlines()]
+        h.update(name.encode())
         h.update("\n".join(line for line in code if line).encode())
     return h.hexdigest()[:16]
 
