@@ -106,6 +106,15 @@ def test_verify_full_workloads_match_oracle(name):
     assert rep.chunks_swept <= rep.rows_planned * rep.chunks_per_row
 
 
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+@pytest.mark.parametrize("extra", [1, 2, 3, 4])
+def test_full_workloads_more_seeds_match_oracle(name, extra):
+    """Four more seeded instances of every workload, each compared in full."""
+    seed = synth.WORKLOADS[name]["seed"] + 1000 * extra
+    inp = synth.make_workload(name, seed=seed)
+    check(inp, f"{name} seed={seed}")
+
+
 @pytest.mark.parametrize("name", ["b128_k16_v151936_bf16_zipf_mixed_noise"])
 def test_full_sweep_flag_gives_same_outputs(name):
     inp = synth.make_workload(name, seed=777)
