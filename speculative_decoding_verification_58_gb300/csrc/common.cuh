@@ -81,15 +81,17 @@ struct WsLayout {
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Vocabulary chunks per row: about 2048 units when all rows are active (more
-// for small batches, so that the SMs have work), at least two per row (so
-// that the last units of a round are short and a rejection found while a row
-// streams spares its second half), chunks of at least 2048 elements.  Larger
-// units cost more at the end of a round and in bytes read past a rejection;
-// smaller ones cost per-unit bookkeeping (both measured on GB300: 1 to 256
-// requests of 151936 logits).
+// Vocabulary chunks per row: at least two (so that the last units of a round
+// are short and a rejection found while a row streams spares its second
+// half), more only for the smallest batches (about 256 units when all rows
+// are active: 8 chunks for one request of 16 positions), chunks of at least
+// 2048 elements.  Larger units cost more at the end of a round and in bytes
+// read past a rejection; smaller ones cost per-unit claims and bookkeeping,
+// which is what set the small-batch rounds (measured on GB300 with 1 to 256
+// requests of 151936 logits: 2048 units made the 1-request round 41.5 us,
+// 256 make it 28 us).
 __host__ __device__ inline int chunks_per_row(long long rows_max, int V) {
-  long long want = (2048 + rows_max - 1) / rows_max;
+  long long want = (256 + rows_max - 1) / rows_max;
   if (want < 2) want = 2;
   long long maxc = (V + 2047) / 2048;
   if (maxc < 1) maxc = 1;
