@@ -32,7 +32,7 @@ constexpr int kRedDepth = 8;  // unit-end reduction slots in flight
 constexpr int kFinalThreads = 256;
 constexpr int kSegElems = 256;  // one warp x 8 elements
 constexpr int kMaxSegs = SPEC_MAX_V / kSegElems;
-constexpr int kMaxSlices = 16;  // CTAs that share one request's final row(s)
+constexpr int kMaxSlices = 64;  // CTAs that share one request's final row(s)
 
 // Bounded waits: give up after this many nanoseconds of spinning.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
