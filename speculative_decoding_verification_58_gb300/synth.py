@@ -189,6 +189,66 @@ def make_inputs(recipe: str, B: int, k: int, V: int, dtype: str, seed: int,
     return SpecInputs(target, draft, tokens, lengths, uniforms, temps, dtype)
 
 
+LOW_TV_FORCED_U = np.float32(0.999)
+
+
+def make_low_tv_inputs(B: int, k: int, V: int, dtype: str, sigma: float, seed: int,
+                       threads: int | None = None) -> SpecInputs:
+    """A batch whose draft rows are close to the target rows, with forced rejections.
+
+    Target rows as the ``zipf`` recipe; draft = target + N(0, sigma^2) element
+    by element (in fp32, before any bf16 rounding), so p and q differ by a
+    small total variation and the residual max(0, p - q) carries little mass.
+    Every request verifies all k positions at T = 1.  At one seeded position
+    j_b < k the uniform is ``LOW_TV_FORCED_U`` (0.999), so the request is
+    rejected there whenever p(x)/q(x) < 0.999 (about half the time when the
+    earlier positions were accepted) instead of almost never; every other
+    uniform is a 24-bit draw.  0.999 keeps the forced decision 1e-3 away from
+    the ratio cap 1, so an accepting request is not a near-tie.  Only random
+    numbers are drawn here.
+    """
+    if dtype not in ("f32", "bf16"):
+        raise ValueError("dtype must be 'f32' or 'bf16'")
+    ss = np.random.SeedSequence(seed)
+    batch_seq, *req_seqs = ss.spawn(B + 1)
+    brng = np.random.default_rng(batch_seq)
+    lengths = np.full(B, k, np.int32)
+    temps = np.ones(B, np.float32)
+    uniforms = uniform_24bit(brng, (B, k + 1))
+    forced = brng.integers(0, k, size=B)
+    uniforms[np.arange(B), forced] = LOW_TV_FORCED_U
+    store = np.uint16 if dtype == "bf16" else np.float32
+    target = np.empty((B, k + 1, V), store)
+    draft = np.empty((B, k, V), store)
+    tokens = np.empty((B, k), np.int32)
+    zipf = _zipf_table(V)
+
+    def one_request(b: int) -> None:
+        rng = np.random.default_rng(req_seqs[b])
+        zt = rng.standard_normal((k + 1, V), dtype=np.float32)
+        zt += rng.permutation(zipf)[None, :]
+        zd = zt[:k] + rng.standard_normal((k, V), dtype=np.float32) * np.float32(sigma)
+        if dtype == "bf16":
+            target[b] = bf16_bits(zt)
+            draft[b] = bf16_bits(zd)
+            zd_stored = bf16_to_f32(draft[b])
+        else:
+            target[b] = zt
+            draft[b] = zd
+            zd_stored = zd
+        g = rng.gumbel(size=(k, V))
+        tokens[b] = np.argmax(zd_stored.astype(np.float64) + g, axis=1)
+
+    n_threads = threads or min(16, os.cpu_count() or 1, B)
+    if n_threads <= 1:
+        for b in range(B):
+            one_request(b)
+    else:
+        with ThreadPoolExecutor(n_threads) as pool:
+            list(pool.map(one_request, range(B)))
+    return SpecInputs(target, draft, tokens, lengths, uniforms, temps, dtype)
+
+
 def make_workload(name: str, seed: int | None = None, threads: int | None = None,
                   **overrides) -> SpecInputs:
     """Inputs of one named workload; ``overrides`` may shrink B, k or V for fast checks."""

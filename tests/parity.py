@@ -49,3 +49,25 @@ def compare(gpu_out: np.ndarray, gpu_n: np.ndarray, o: oracle.OracleResult,
             f"out={o.out_tokens[b].tolist()}; {info}")
     assert info["excused"] <= max(1, NEAR_TIE_RATE * rows), (label, info)
     return info
+
+
+def oracle_verify_threads(inp, threads: int = 16) -> oracle.OracleResult:
+    """``oracle.verify`` on a batch split over host threads (requests are
+    independent; the oracle call releases the interpreter lock), concatenated
+    in request order.  Same results as one call."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+    B = inp.B
+    n = max(1, min(threads, os.cpu_count() or 1, B))
+    edges = [B * j // n for j in range(n + 1)]
+
+    def part(j):
+        s = slice(edges[j], edges[j + 1])
+        return oracle.verify(inp.target[s], inp.draft[s], inp.tokens[s], inp.lengths[s],
+                             inp.uniforms[s], inp.temperature[s])
+    with ThreadPoolExecutor(n) as pool:
+        parts = list(pool.map(part, range(n)))
+    cat = lambda f: np.concatenate([getattr(p, f) for p in parts])
+    return oracle.OracleResult(cat("out_tokens"), cat("num_accepted"), cat("margin"),
+                               cat("final_mass"), cat("residual_zero"),
+                               sum(p.bad_requests for p in parts))
