@@ -42,7 +42,9 @@
  *     workspace records SPEC_ERR_BAD_INPUT, readable with
  *     spec_verify_device_status() or spec_verify_report().  No kernel traps.
  *   - Every device-side wait is bounded; a wait that runs out records
- *     SPEC_ERR_TIMEOUT in the workspace and the kernel returns.
+ *     SPEC_ERR_TIMEOUT in the workspace and the kernel returns.  A request
+ *     whose outcome or final token a timed-out wait left unknown reports
+ *     num_accepted = -1 and out_tokens all -1, like an invalid request.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -76,6 +78,15 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
 
 /* Flags for spec_verify_ex. */
 #define SPEC_FLAG_FULL_SWEEP 1u  /* sweep every row i < L_b even past a known rejection */
+/*
+ * Testing aid, never for production: in the final pass, every slice CTA of a
+ * request except the first waits (bounded, 1 ms) for an event that never
+ * happens, as if the request's outcome never arrived.  It exercises the path
+ * a real device-side timeout takes: every request with more than one slice
+ * then reports num_accepted = -1 and out_tokens all -1, and the workspace
+ * records SPEC_ERR_TIMEOUT; nothing faults and the stream stays usable.
+ */
+#define SPEC_FLAG_TEST_LATE_SLICES 2u
 
 /*
  * Bytes of device workspace spec_verify needs for a batch of B requests with
@@ -208,8 +219,10 @@ spec_status_t spec_verify_packed(const void* target_rows, long long rows_t,
  *     contents; each call resets what it needs.  Calls that overlap on the
  *     GPU (other streams, other host threads) race and must be serialised
  *     by the caller.
- *   - Invalid device-side inputs show as num_accepted[b] == -1; the status
- *     word stays in the library's scratch and is not reported separately.
+ *   - Invalid device-side inputs, and a request whose result a device-side
+ *     wait that ran out (2 s) left unknown, show as num_accepted[b] == -1
+ *     and out_tokens all -1; the status word stays in the library's scratch
+ *     and is not reported separately.
  * Arguments are those of spec_verify without the workspace.
  */
 #define SPEC_STATIC_SCRATCH_BYTES (8u << 20)

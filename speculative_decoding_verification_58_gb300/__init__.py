@@ -41,6 +41,7 @@ SPEC_ERR_INTERNAL = 7
 SPEC_F32 = 0
 SPEC_BF16 = 1
 SPEC_FLAG_FULL_SWEEP = 1
+SPEC_FLAG_TEST_LATE_SLICES = 2
 
 # Every entry point include/spec_verify.h declares.
 EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_ex", "spec_verify_timed",
@@ -202,7 +203,7 @@ def alloc_workspace(B: int, k: int, V: int, device=None):
 
 def spec_verify(target_logits, draft_logits, draft_tokens, lengths, uniforms, temperature, *,
                 workspace=None, out_tokens=None, num_accepted=None, stream=None,
-                full_sweep: bool = False, events=None):
+                full_sweep: bool = False, events=None, flags: int = 0):
     """Batched verification on the current (or given) CUDA stream.
 
     Shapes: target [B, k+1, V], draft [B, k, V] (float32 or bfloat16, same),
@@ -213,6 +214,7 @@ def spec_verify(target_logits, draft_logits, draft_tokens, lengths, uniforms, te
     ``events``: optional four recorded ``torch.cuda.Event`` objects (or None
     entries) marking plan / sweep / final / end, for per-kernel timing
     (measurement only: it disables the kernels' launch overlap).
+    ``flags``: further SPEC_FLAG_* bits passed through unchanged.
     """
     torch = _torch()
     B, k1, V = target_logits.shape
@@ -233,7 +235,7 @@ def spec_verify(target_logits, draft_logits, draft_tokens, lengths, uniforms, te
         num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
     _need(out_tokens, "out_tokens", torch.int32, (B, k + 1), dev)
     _need(num_accepted, "num_accepted", torch.int32, (B,), dev)
-    flags = SPEC_FLAG_FULL_SWEEP if full_sweep else 0
+    flags = int(flags) | (SPEC_FLAG_FULL_SWEEP if full_sweep else 0)
     args = (target_logits.data_ptr(), draft_logits.data_ptr(), dt, draft_tokens.data_ptr(),
             lengths.data_ptr(), uniforms.data_ptr(), temperature.data_ptr(), B, k, V,
             out_tokens.data_ptr(), num_accepted.data_ptr(), workspace.data_ptr(),

@@ -76,7 +76,7 @@ constexpr unsigned long long kPartialEmpty = 0x7FC0DEAD7FC0DEADull;
 
 struct WsLayout {
   size_t header, rowdesc, flags, first_reject, state, bad_bits, done, pos_c, pos_arg,
-      partials, seg_mass, slice_ref, slice_arg, final_done, rowbase, warm, total;
+      partials, seg_mass, slice_out, final_done, rowbase, warm, total;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -123,8 +123,7 @@ __host__ __device__ inline WsLayout ws_layout(int B, int k, int C, int V) {
   l.pos_arg = o;      o = align256(o + (size_t)B * k * sizeof(int32_t));
   l.partials = o;     o = align256(o + slots * (size_t)C * sizeof(Partial));
   l.seg_mass = o;     o = align256(o + (size_t)B * segments_of(V) * sizeof(float2));
-  l.slice_ref = o;    o = align256(o + (size_t)B * kMaxSlices * sizeof(float));
-  l.slice_arg = o;    o = align256(o + (size_t)B * kMaxSlices * sizeof(int32_t));
+  l.slice_out = o;    o = align256(o + (size_t)B * kMaxSlices * sizeof(float2));
   l.final_done = o;   o = align256(o + (size_t)B * sizeof(int32_t));
   l.rowbase = o;      o = align256(o + (size_t)B * sizeof(int2));
   l.warm = o;         o = align256(o + 2 * (size_t)C * sizeof(Partial));

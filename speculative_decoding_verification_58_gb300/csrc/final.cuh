@@ -15,8 +15,10 @@
 // sums in float-float, picks the segment holding u_L * total, and re-reads that
 // segment to place the token exactly.
 //
-// Records: a residual segment stores its mass sum max(0, p - q), with p and
-// q normalised by the row normalisers from the sweep.  A bonus segment
+// Records: a residual segment stores sum max(0, p - q) and the q mass where
+// p > q, with p and q normalised by the row normalisers from the sweep; the
+// slices also sum D = sum (p - q) over the pair, from which the combine
+// corrects for the normalisers' residual error (see MassSpec).  A bonus segment
 // stores its own max m and s = sum 2^(z*sc - fl(m*sc)); the last CTA weighs
 // it by 2^(fl(m*sc) - REF), REF the largest segment reference, so the row is
 // read once and the common normaliser cancels in the CDF.
@@ -36,6 +38,7 @@ struct FinalParams {
   int B, k, V;
   int P;           // slice CTAs per request; CTA x is slice x % P of request x / P
   int sweep_grid;  // CTAs of the sweep grid this pass follows
+  int test_late;   // testing aid: slices other than the first give up waiting (see below)
   int32_t* out_tokens;
   int32_t* num_accepted;
   unsigned char* ws;
@@ -54,9 +57,20 @@ struct FinalShared {
   int32_t pos_arg[32];
   int32_t tok[32];                // draft tokens x_0 .. x_{k-1}
   FF cand_excl;
-  float REF;
-  int job, n, cand, token, last;
+  float REF, mu;
+  int job, n, cand, token, last, late, any_late;
 };
+
+// A slice CTA that gave up (its wait for the request's outcome, or for its
+// own copies, ran out) still counts itself in final_done, with this mark
+// added; the last slice to arrive then writes -1 outputs for the request
+// instead of combining records that were never written.
+constexpr int kLateMark = 1 << 16;
+constexpr int kArriveMask = kLateMark - 1;  // slices arrived (P <= kMaxSlices)
+static_assert(kMaxSlices < kLateMark, "the arrival count stays below the late mark");
+// The testing aid's wait: slices other than the first wait this long for an
+// event that never happens, as if their request's outcome never arrived.
+constexpr unsigned long long kTestLateLimitNs = 1000000ull;
 
 // ---------------------------------------------------------------------------
 // Segment loads: lane l holds entries 8l .. 8l+7 of a segment as raw bits
@@ -117,39 +131,112 @@ __device__ __forceinline__ float2 f32x2_sub(float2 a, float2 b) {
   return d;
 }
 
-// How the entries of one request's final row(s) are weighed.  Residual
-// entries: max(0, 2^(zt*sc - a) - 2^(zd*sc - c_d)); target-only entries:
-// 2^(zt*sc - a); a and c_d are row normalisers carried as hi + lo
-// single-precision pairs (float-float) so that they keep their accuracy.
+// How the entries of one request's final row(s) are weighed.
+//
+// Target-only entries (the bonus fallback of a zero residual): p = 2^(zt*sc - a).
+//
+// Residual entries max(0, p - q).  Two things make a plain p - q in single
+// precision too coarse when q is close to p, where the residual's total mass
+// (the total variation of p and q) is small and every error is magnified by
+// its inverse in the normalised CDF:
+//   - the difference of two nearly equal numbers, each rounded relative to
+//     itself: the entries are formed as p - q = (p + q) * (-tanh(delta*ln2/2))
+//     with delta = log2 q - log2 p = (zd - zt)*sc - (c_d - a) taken from the
+//     logits directly, so that the error is relative to |p - q|;
+//   - the row normalisers a and c_d come from the sweep's single-precision
+//     sums and their ratio is off by up to a few 1e-7, which shifts every
+//     entry by the same fraction of q.  The slice pass therefore also sums
+//     D = sum_v (p_v - q_v) over the whole row pair (each slice its share, in
+//     float-float), with p and q normalised by those normalisers; exactly
+//     normalised, the residual is max(0, p - (1 + mu) q) with
+//     mu = D / (1 - D), and each segment's weight is corrected by
+//     -mu * (its q mass where p > q) in the combine.
+// a, c_d and dc = c_d - a are carried as hi + lo single-precision pairs
+// (float-float) so that they keep their accuracy.
 struct MassSpec {
   float sc;
   float a_hi, a_lo;
   float cd_hi, cd_lo;
+  float dc_hi, dc_lo;
   bool has_q;
 };
 
-// The 8 entry masses of a lane's segment piece, in index order.  Packed
-// two-lane arithmetic gives each entry exactly the bits of the scalar
-// formula, so the slice pass and the re-scan agree.
+// -tanh(k * delta) / delta with k = ln(2) / 2, as a polynomial in w = delta^2:
+// the Maclaurin series of tanh, tanh z = z - z^3/3 + 2z^5/15 - 17z^7/315 +
+// 62z^9/2835 - 1382z^11/155925 + ..., truncated after z^11.  For |delta| <= 1
+// (|z| <= 0.347) the first omitted term is below 1.1e-8 of the sum.  The
+// coefficients are the series' own, scaled by powers of k by the compiler.
+constexpr double kTanhK = 0.34657359027997265471;  // ln(2) / 2
+constexpr float kTh0 = (float)(-kTanhK);
+constexpr float kTh1 = (float)(kTanhK * kTanhK * kTanhK / 3.0);
+constexpr float kTh2 = (float)(-2.0 * kTanhK * kTanhK * kTanhK * kTanhK * kTanhK / 15.0);
+constexpr float kTh3 = (float)(17.0 * kTanhK * kTanhK * kTanhK * kTanhK * kTanhK * kTanhK * kTanhK /
+                               315.0);
+constexpr float kTh4 = (float)(-62.0 * kTanhK * kTanhK * kTanhK * kTanhK * kTanhK * kTanhK * kTanhK *
+                               kTanhK * kTanhK / 2835.0);
+constexpr float kTh5 = (float)(1382.0 * kTanhK * kTanhK * kTanhK * kTanhK * kTanhK * kTanhK * kTanhK *
+                               kTanhK * kTanhK * kTanhK * kTanhK / 155925.0);
+// Beyond |delta| = 1 the plain difference p - q loses at most a factor
+// (1 + 2^-1) / (1 - 2^-1) = 3 of relative precision.
+constexpr float kTanhRange = 1.0f;
+
+// Signed residual entries rh = p - q and the draft probabilities qb of a lane's
+// 8 entries (residual job).  Packed two-lane arithmetic gives each entry
+// exactly the bits of the scalar formula, so the slice pass and the re-scan
+// agree.
 template <typename TIn>
-__device__ __forceinline__ void entry_masses(const Seg8<TIn>& t, const Seg8<TIn>& d,
-                                             const MassSpec& ms, float (&r)[8]) {
+__device__ __forceinline__ void residual_entries(const Seg8<TIn>& t, const Seg8<TIn>& d,
+                                                 const MassSpec& ms, float (&rh)[8],
+                                                 float (&qb)[8]) {
   const float2 sc2 = make_float2(ms.sc, ms.sc);
   const float2 na2 = make_float2(-ms.a_hi, -ms.a_hi), al2 = make_float2(ms.a_lo, ms.a_lo);
   const float2 nc2 = make_float2(-ms.cd_hi, -ms.cd_hi), cl2 = make_float2(ms.cd_lo, ms.cd_lo);
+  const float2 nd2 = make_float2(-ms.dc_hi, -ms.dc_hi), dl2 = make_float2(ms.dc_lo, ms.dc_lo);
+  const float2 h1 = make_float2(kTh1, kTh1), h2 = make_float2(kTh2, kTh2);
+  const float2 h3 = make_float2(kTh3, kTh3), h4 = make_float2(kTh4, kTh4);
+  const float2 h5 = make_float2(kTh5, kTh5), h0 = make_float2(kTh0, kTh0);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 zt = seg_pair(t, j), zd = seg_pair(d, j);
+    const float2 a = ex2x2(f32x2_sub(f32x2_fma(zt, sc2, na2), al2));  // p
+    const float2 b = ex2x2(f32x2_sub(f32x2_fma(zd, sc2, nc2), cl2));  // q
+    // zd - zt is exact for bf16 logits (rounded once for fp32); the fused
+    // multiply-add rounds delta once more, relative to delta itself.
+    const float2 dl = f32x2_sub(f32x2_fma(f32x2_sub(zd, zt), sc2, nd2), dl2);
+    const float2 w = f32x2_mul(dl, dl);
+    float2 poly = f32x2_fma(h5, w, h4);
+    poly = f32x2_fma(poly, w, h3);
+    poly = f32x2_fma(poly, w, h2);
+    poly = f32x2_fma(poly, w, h1);
+    poly = f32x2_fma(poly, w, h0);
+    const float2 small = f32x2_mul(f32x2_add(a, b), f32x2_mul(dl, poly));
+    const float2 plain = f32x2_sub(a, b);
+    // A NaN delta (both logits -inf) or an infinite one takes the plain
+    // difference: 0, -q or p.
+    rh[2 * j] = fabsf(dl.x) <= kTanhRange ? small.x : plain.x;
+    rh[2 * j + 1] = fabsf(dl.y) <= kTanhRange ? small.y : plain.y;
+    qb[2 * j] = b.x;
+    qb[2 * j + 1] = b.y;
+  }
+}
+
+// Target-only entries p = 2^(zt*sc - a) of a lane's 8 entries.
+template <typename TIn>
+__device__ __forceinline__ void target_entries(const Seg8<TIn>& t, const MassSpec& ms,
+                                               float (&r)[8]) {
+  const float2 sc2 = make_float2(ms.sc, ms.sc);
+  const float2 na2 = make_float2(-ms.a_hi, -ms.a_hi), al2 = make_float2(ms.a_lo, ms.a_lo);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const float2 pt = ex2x2(f32x2_sub(f32x2_fma(seg_pair(t, j), sc2, na2), al2));
-    if (ms.has_q) {
-      const float2 qd = ex2x2(f32x2_sub(f32x2_fma(seg_pair(d, j), sc2, nc2), cl2));
-      const float2 df = f32x2_sub(pt, qd);
-      r[2 * j] = fmaxf(df.x, 0.0f);
-      r[2 * j + 1] = fmaxf(df.y, 0.0f);
-    } else {
-      r[2 * j] = pt.x;
-      r[2 * j + 1] = pt.y;
-    }
+    r[2 * j] = pt.x;
+    r[2 * j + 1] = pt.y;
   }
+}
+
+// Weight of one residual entry once mu is known: max(0, (p - q) - mu q).
+__device__ __forceinline__ float residual_weight(float rh, float qb, float mu) {
+  return fmaxf(__fmaf_rn(-mu, qb, rh), 0.0f);
 }
 
 // Bonus entries relative to the segment reference msr = fl(m*sc), m the
@@ -202,10 +289,50 @@ __device__ __forceinline__ float warp_max_f32(float x) {
 // wherever the power is not negligible.
 __device__ __forceinline__ float exp2_diff(float a, float b) { return exp2f(__fsub_rn(a, b)); }
 
-// CDF weight of a segment record: its mass, or for the bonus its sum
-// rescaled from its own reference to REF.
-__device__ __forceinline__ float seg_weight(float2 r, bool bonus, float sc, float REF) {
-  if (!bonus) return r.x;
+// One segment's record (warp-cooperative: every lane gets the same value):
+//   residual:    (sum max(0, p - q), sum of q where p > q)
+//   target only: (sum p, 0)
+//   bonus:       (segment max m, sum 2^(z*sc - fl(m*sc)))
+// For a residual, *dlane gets this lane's sum of p - q over its 8 entries
+// (the share of D, see MassSpec).
+template <typename TIn>
+__device__ __forceinline__ float2 seg_record(const Seg8<TIn>& t, const Seg8<TIn>& d,
+                                             const MassSpec& ms, bool bonus, float* dlane) {
+  float r[8];
+  if (bonus) {
+    const float m = warp_max_f32(seg8_max(t));
+    bonus_masses(t, ms.sc, __fmul_rn(m, ms.sc), r);
+    return make_float2(m, warp_sum_f32(sum8(r)));
+  }
+  if (!ms.has_q) {
+    target_entries(t, ms, r);
+    return make_float2(warp_sum_f32(sum8(r)), 0.0f);
+  }
+  float qb[8];
+  residual_entries(t, d, ms, r, qb);
+  float rp = 0.0f, qp = 0.0f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    if (r[e] > 0.0f) {
+      rp = __fadd_rn(rp, r[e]);
+      qp = __fadd_rn(qp, qb[e]);
+    }
+  }
+  *dlane = sum8(r);
+  // Both sums in one butterfly: two shuffles, one packed add per level.
+  float2 v = make_float2(rp, qp);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+    v = f32x2_add(v, make_float2(__shfl_xor_sync(0xffffffffu, v.x, off),
+                                 __shfl_xor_sync(0xffffffffu, v.y, off)));
+  return v;
+}
+
+// CDF weight of a segment record: the residual mass corrected by mu (0 for
+// target-only records), or for the bonus its sum rescaled from its own
+// reference to REF.
+__device__ __forceinline__ float seg_weight(float2 r, bool bonus, float sc, float REF, float mu) {
+  if (!bonus) return fmaxf(__fmaf_rn(-mu, r.y, r.x), 0.0f);
   if (r.y == 0.0f) return 0.0f;
   return __fmul_rn(r.y, exp2_diff(__fmul_rn(r.x, sc), REF));
 }
@@ -221,10 +348,11 @@ __host__ __device__ constexpr int slice_batch() {
   return sizeof(TIn) == 2 ? 2 : 1;
 }
 
-// Records of segments [s_lo, s_hi): (mass, 0), or for the bonus (m, s).
+// Records of segments [s_lo, s_hi) (see seg_record); *dsum accumulates this
+// thread's share of D in float-float.
 template <typename TIn>
 __device__ void slice_records(const TIn* rt, const TIn* rd, int V, const MassSpec& ms, bool bonus,
-                              int s_lo, int s_hi, float2* rec, bool vec_ok) {
+                              int s_lo, int s_hi, float2* rec, bool vec_ok, FF* dsum) {
   constexpr int U = slice_batch<TIn>();
   constexpr int STEP = kFinalWarps * U;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -245,16 +373,9 @@ __device__ void slice_records(const TIn* rt, const TIn* rd, int V, const MassSpe
     for (int q = 0; q < U; ++q) {
       const int seg = s0 + q * kFinalWarps;
       if (seg >= s_hi) break;
-      float r[8];
-      float2 out;
-      if (bonus) {
-        const float m = warp_max_f32(seg8_max(t[q]));
-        bonus_masses(t[q], ms.sc, __fmul_rn(m, ms.sc), r);
-        out = make_float2(m, warp_sum_f32(sum8(r)));
-      } else {
-        entry_masses(t[q], d[q], ms, r);
-        out = make_float2(warp_sum_f32(sum8(r)), 0.0f);
-      }
+      float dl = 0.0f;
+      const float2 out = seg_record(t[q], d[q], ms, bonus, &dl);
+      *dsum = ff_add_f(*dsum, dl);
       if (lane == 0) __stcg(&rec[seg], out);
     }
   };
@@ -276,9 +397,9 @@ __device__ void slice_records(const TIn* rt, const TIn* rd, int V, const MassSpe
 // The same records, with the slice streamed through shared memory by bulk
 // copies (rows 16-byte aligned): a ring of kFinalStages pieces, each S
 // segments of the target row and, for a residual, the same S segments of the
-// draft row after them.  Thread 0 keeps kFinalStages pieces in flight; every
-// warp takes the piece's segments w, w + 8, ... and computes exactly what
-// slice_records computes.  Far more bytes in flight per CTA than register
+// draft row after them.  Every warp takes the piece's segments w, w + 8, ...
+// and computes exactly what slice_records computes; the last warp to be done
+// with a slot refills it, so warps are not held together at every piece.  Far more bytes in flight per CTA than register
 // loads allow, which is what a request finishing alone, at the end of a
 // round, needs.  Returns false if a wait ran out.
 constexpr int kFinalStages = 3;
@@ -286,13 +407,15 @@ constexpr int kFinalStageBytes = 16384;
 
 struct FinalRing {
   uint64_t full[kFinalStages];
+  int freed[kFinalStages];  // warps done with the slot's current piece
+  int issued;               // pieces issued so far (in order)
   int abort_flag;
 };
 
 template <typename TIn>
 __device__ bool slice_records_staged(const TIn* rt, const TIn* rd, int V, const MassSpec& ms,
                                      bool bonus, int s_lo, int s_hi, float2* rec,
-                                     unsigned char* ring, FinalRing& fr) {
+                                     unsigned char* ring, FinalRing& fr, FF* dsum) {
   constexpr int SB = kSegElems * (int)sizeof(TIn);  // bytes of one segment of one row
   constexpr int NV = SB / 512;                      // 16-byte vectors per lane per segment
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -301,7 +424,11 @@ __device__ bool slice_records_staged(const TIn* rt, const TIn* rd, int V, const 
   const int S = kFinalStageBytes / (R * SB);
   const int npieces = (s_hi - s_lo + S - 1) / S;
   if (threadIdx.x == 0) {
-    for (int j = 0; j < kFinalStages; ++j) mbar_init(&fr.full[j], 1);
+    for (int j = 0; j < kFinalStages; ++j) {
+      mbar_init(&fr.full[j], 1);
+      fr.freed[j] = 0;
+    }
+    fr.issued = 0;
     fr.abort_flag = 0;
     fence_mbar_init();
   }
@@ -322,14 +449,17 @@ __device__ bool slice_records_staged(const TIn* rt, const TIn* rd, int V, const 
     const uint64_t pol = l2_policy_evict_first();
     bulk_g2s_hint(dst, rt + (size_t)g0 * kSegElems, nb, &fr.full[slot], pol);
     if (has_q) bulk_g2s_hint(dst + S * SB, rd + (size_t)g0 * kSegElems, nb, &fr.full[slot], pol);
+    atomicMax(&fr.issued, j + 1);
   };
   if (threadIdx.x == 0)
     for (int j = 0; j < kFinalStages && j < npieces; ++j) issue(j);
   bool ok = true;
   for (int j = 0; j < npieces; ++j) {
     const int slot = j % kFinalStages;
-    if (!mbar_wait_bounded(&fr.full[slot], (uint32_t)(j / kFinalStages) & 1u, &fr.abort_flag))
+    if (ok && !mbar_wait_bounded(&fr.full[slot], (uint32_t)(j / kFinalStages) & 1u, &fr.abort_flag)) {
       ok = false;
+      *(volatile int*)&fr.abort_flag = 1;
+    }
     const int g0 = s_lo + j * S, nseg = min(s_hi - g0, S);
     const uint4* buf = reinterpret_cast<const uint4*>(ring + slot * kFinalStageBytes);
     if (ok) {
@@ -361,29 +491,32 @@ __device__ bool slice_records_staged(const TIn* rt, const TIn* rd, int V, const 
             }
           }
         }
-        float r[8];
-        float2 out;
-        if (bonus) {
-          const float m = warp_max_f32(seg8_max(t));
-          bonus_masses(t, ms.sc, __fmul_rn(m, ms.sc), r);
-          out = make_float2(m, warp_sum_f32(sum8(r)));
-        } else {
-          entry_masses(t, d, ms, r);
-          out = make_float2(warp_sum_f32(sum8(r)), 0.0f);
-        }
+        float dl = 0.0f;
+        const float2 out = seg_record(t, d, ms, bonus, &dl);
+        *dsum = ff_add_f(*dsum, dl);
         if (lane == 0) __stcg(&rec[seg], out);
       }
     }
-    // Everyone is done with this piece: the slot can take piece j + stages.
-    __syncthreads();
-    if (threadIdx.x == 0 && ok && j + kFinalStages < npieces) issue(j + kFinalStages);
+    // This warp is done with the slot (its reads are in registers); the last
+    // of the warps to be done refills it with piece j + stages.
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(&fr.freed[slot], 1) == kFinalWarps - 1) {
+        fr.freed[slot] = 0;
+        if (ok && !*(volatile int*)&fr.abort_flag && j + kFinalStages < npieces)
+          issue(j + kFinalStages);
+      }
+    }
   }
   ok = __syncthreads_and(ok);
   if (!ok && threadIdx.x == 0) {
     // A wait ran out: let the copies still in flight land (bounded) before
-    // the shared memory is given back.
+    // the shared memory is given back.  Pieces go out in order, one slot at a
+    // time, so only the last piece issued into each slot can be in flight.
     int dummy = 0;
-    for (int j = 0; j < npieces; ++j)
+    const int issued = fr.issued;
+    for (int j = max(0, issued - kFinalStages); j < issued; ++j)
       mbar_wait_bounded(&fr.full[j % kFinalStages], (uint32_t)(j / kFinalStages) & 1u,
                         (volatile int*)&dummy);
   }
@@ -482,12 +615,14 @@ __device__ __forceinline__ FF block_exclusive_scan_ff(FF x, FinalShared& sh, FF*
 // Inverse CDF over the request's segment records (global, nseg entries):
 // the first entry whose cumulative weight exceeds u * total.  Block-wide;
 // returns the token, or -1 if the total weight is not a finite positive
-// number.  rec_sm: nseg float2 of shared memory.
+// number.  rec_sm: nseg float2 of shared memory.  mu: the residual's
+// normaliser correction (0 otherwise).
 template <typename TIn>
 __device__ int cdf_pick(const TIn* rt, const TIn* rd, int V, const MassSpec& ms, bool bonus,
                         float u, const float2* rec, int nseg, bool vec_ok, FinalShared& sh,
-                        float2* rec_sm) {
+                        float2* rec_sm, float mu) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool residual = !bonus && ms.has_q;
   float refm = -FLT_MAX;
   for (int s = threadIdx.x; s < nseg; s += kFinalThreads) {
     const float2 r = __ldcg(&rec[s]);
@@ -505,11 +640,12 @@ __device__ int cdf_pick(const TIn* rt, const TIn* rd, int V, const MassSpec& ms,
 #pragma unroll
     for (int w = 0; w < kFinalWarps; ++w) REF = fmaxf(REF, sh.warp_f[w]);
   }
-  // Exclusive prefix of the weights, in float-float; thread t owns [sa, sb).
+  // Thread t owns segments [sa, sb).
   const int per = (nseg + kFinalThreads - 1) / kFinalThreads;
   const int sa = min(nseg, (int)threadIdx.x * per), sb = min(nseg, sa + per);
+  // Exclusive prefix of the weights, in float-float.
   FF loc = {0.0f, 0.0f};
-  for (int s = sa; s < sb; ++s) loc = ff_add_f(loc, seg_weight(rec_sm[s], bonus, ms.sc, REF));
+  for (int s = sa; s < sb; ++s) loc = ff_add_f(loc, seg_weight(rec_sm[s], bonus, ms.sc, REF, mu));
   FF total;
   FF run = block_exclusive_scan_ff(loc, sh, &total);
   if (!(total.hi > 0.0f && total.hi <= FLT_MAX)) return -1;  // uniform across the block
@@ -521,7 +657,7 @@ __device__ int cdf_pick(const TIn* rt, const TIn* rd, int V, const MassSpec& ms,
   int cand = -1;
   FF cand_excl = {0.0f, 0.0f};
   for (int s = sa; s < sb; ++s) {
-    const float w = seg_weight(rec_sm[s], bonus, ms.sc, REF);
+    const float w = seg_weight(rec_sm[s], bonus, ms.sc, REF, mu);
     if (w > 0.0f && ff_le(run, target)) {
       cand = s;
       cand_excl = run;
@@ -547,8 +683,13 @@ __device__ int cdf_pick(const TIn* rt, const TIn* rd, int V, const MassSpec& ms,
       const float msr = __fmul_rn(rec_sm[j].x, ms.sc);
       bonus_masses(t, ms.sc, msr, r);
       scale = exp2_diff(msr, REF);
+    } else if (residual) {
+      float qb[8];
+      residual_entries(t, d, ms, r, qb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r[e] = residual_weight(r[e], qb[e], mu);
     } else {
-      entry_masses(t, d, ms, r);
+      target_entries(t, ms, r);
     }
     // Cumulative weight within the segment, in float-float: lane sums, then
     // an exclusive scan over the lanes, then entry by entry.
@@ -603,8 +744,9 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
   const int b = (int)(blockIdx.x / (unsigned)P), part = (int)(blockIdx.x - (unsigned)b * P);
   WsHeader* h = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
   float2* rec = reinterpret_cast<float2*>(p.ws + p.lay.seg_mass) + (size_t)b * nseg;
-  float* slice_ref = reinterpret_cast<float*>(p.ws + p.lay.slice_ref) + (size_t)b * kMaxSlices;
-  int32_t* slice_arg = reinterpret_cast<int32_t*>(p.ws + p.lay.slice_arg) + (size_t)b * kMaxSlices;
+  // Per slice: (max, bits of its lowest index) of a greedy row L, or the
+  // slice's share of D (hi, lo) for a residual.
+  float2* slice_out = reinterpret_cast<float2*>(p.ws + p.lay.slice_out) + (size_t)b * kMaxSlices;
   int32_t* final_done = reinterpret_cast<int32_t*>(p.ws + p.lay.final_done);
   const int L = __ldg(&p.lengths[b]);
   const float T = __ldg(&p.temperature[b]);
@@ -618,6 +760,10 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
     int f = 0;
     uint32_t dec = 0, acc = 0, bad = 0;
     bool late = false;
+    // Testing aid: this slice never sees its outcome and gives up after a
+    // short wait, exercising the path a real timeout takes.
+    const bool never = p.test_late && part != 0;
+    const unsigned long long limit = never ? kTestLateLimitNs : kWaitLimitNs;
     const unsigned long long t0 = global_ns();
     for (;;) {
       f = __ldcg(reinterpret_cast<const int32_t*>(p.ws + p.lay.flags) + b);
@@ -630,8 +776,8 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
       const uint32_t rej = dec & ~acc & lmask;
       const int nn = rej ? (__ffs((int)rej) - 1) : L;
       const uint32_t pre = (nn >= 32) ? 0xffffffffu : ((1u << nn) - 1u);
-      if ((dec & acc & pre) == pre) break;
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if ((dec & acc & pre) == pre && !never) break;
+      if (global_ns() - t0 > limit) {
         late = true;
         break;
       }
@@ -648,7 +794,7 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
       x = __ldg(&p.tokens[bi]);
     }
     if (late) {
-      if (t == 0 && part == 0) record_status(h, SPEC_ERR_TIMEOUT);
+      if (t == 0) record_status(h, SPEC_ERR_TIMEOUT);
       f = 0;  // no outcome: the request reports -1
     }
     sh.pos_c[t] = c4;
@@ -685,12 +831,14 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
       sh.job = job;
       sh.n = n;
       sh.token = token;
+      sh.late = late ? 1 : 0;
     }
   }
   __syncthreads();
   const int job = sh.job;
   const int n = sh.n;
   int token = sh.token;
+  bool gave_up = sh.late != 0;
 
   auto write_outputs = [&](bool invalid, int final_token) {
     for (int j = threadIdx.x; j <= p.k; j += kFinalThreads) {
@@ -703,60 +851,80 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
     }
     if (threadIdx.x == 0) p.num_accepted[b] = invalid ? -1 : n;
   };
-  if (job == kJobNone || job == kJobInvalid) {
-    if (part == 0) write_outputs(job == kJobInvalid, token);
-    return;
-  }
-
-  // ---- this slice's share of the row(s) ----
-  // Row n of the request in either buffer: its first rows come from the
-  // plan kernel (padded or packed layout).
-  const int2 rb = __ldcg(reinterpret_cast<const int2*>(p.ws + p.lay.rowbase) + b);
-  const TIn* trow = static_cast<const TIn*>(p.target) + ((size_t)rb.x + n) * (size_t)p.V;
-  const TIn* drow = job == kJobResidual
-                        ? static_cast<const TIn*>(p.draft) + ((size_t)rb.y + n) * (size_t)p.V
-                        : trow;
-  const bool vec_ok =
-      ((reinterpret_cast<uintptr_t>(trow) | reinterpret_cast<uintptr_t>(drow)) & 15u) == 0;
-  const int s_lo = slice_lo(part, nseg, P), s_hi = slice_lo(part + 1, nseg, P);
+  // ---- this slice's share of the row(s) (none for kJobNone / kJobInvalid) ----
+  const bool rows_job = (job == kJobResidual || job == kJobBonus || job == kJobGreedyRowL);
+  const TIn* trow = nullptr;
+  const TIn* drow = nullptr;
+  bool vec_ok = false;
   MassSpec ms = {};
-  ms.sc = job == kJobGreedyRowL ? 0.0f : softmax_scale(T);
   const bool bonus = (job == kJobBonus);
-  if (job == kJobResidual) {
-    const float4 c4 = sh.pos_c[n];
-    ms.a_hi = c4.x;
-    ms.a_lo = c4.y;
-    ms.cd_hi = c4.z;
-    ms.cd_lo = c4.w;
-    ms.has_q = true;
-  }
-  if (job == kJobGreedyRowL) {
-    const ArgAcc a = slice_argmax(trow, p.V, s_lo, s_hi, vec_ok, sh);
-    if (threadIdx.x == 0) {
-      __stcg(&slice_ref[part], a.v);
-      __stcg(&slice_arg[part], a.i);
+  if (rows_job) {
+    // Row n of the request in either buffer: its first rows come from the
+    // plan kernel (padded or packed layout).
+    const int2 rb = __ldcg(reinterpret_cast<const int2*>(p.ws + p.lay.rowbase) + b);
+    trow = static_cast<const TIn*>(p.target) + ((size_t)rb.x + n) * (size_t)p.V;
+    drow = job == kJobResidual
+               ? static_cast<const TIn*>(p.draft) + ((size_t)rb.y + n) * (size_t)p.V
+               : trow;
+    vec_ok = ((reinterpret_cast<uintptr_t>(trow) | reinterpret_cast<uintptr_t>(drow)) & 15u) == 0;
+    const int s_lo = slice_lo(part, nseg, P), s_hi = slice_lo(part + 1, nseg, P);
+    ms.sc = job == kJobGreedyRowL ? 0.0f : softmax_scale(T);
+    if (job == kJobResidual) {
+      const float4 c4 = sh.pos_c[n];
+      ms.a_hi = c4.x;
+      ms.a_lo = c4.y;
+      ms.cd_hi = c4.z;
+      ms.cd_lo = c4.w;
+      const FF dc = ff_sub(FF{c4.z, c4.w}, FF{c4.x, c4.y});
+      ms.dc_hi = dc.hi;
+      ms.dc_lo = dc.lo;
+      ms.has_q = true;
     }
-  } else {
-    // Aligned rows stream through shared memory; others load directly.
-    if (vec_ok && ((size_t)p.V * sizeof(TIn)) % 16 == 0) {
-      if (!slice_records_staged(trow, drow, p.V, ms, bonus, s_lo, s_hi, rec,
-                                reinterpret_cast<unsigned char*>(rec_sm), fr) &&
-          threadIdx.x == 0)
-        record_status(h, SPEC_ERR_TIMEOUT);
+    if (job == kJobGreedyRowL) {
+      const ArgAcc a = slice_argmax(trow, p.V, s_lo, s_hi, vec_ok, sh);
+      if (threadIdx.x == 0) __stcg(&slice_out[part], make_float2(a.v, __int_as_float(a.i)));
     } else {
-      slice_records(trow, drow, p.V, ms, bonus, s_lo, s_hi, rec, vec_ok);
+      FF dsum = {0.0f, 0.0f};
+      // Aligned rows stream through shared memory; others load directly.
+      if (vec_ok && ((size_t)p.V * sizeof(TIn)) % 16 == 0) {
+        if (!slice_records_staged(trow, drow, p.V, ms, bonus, s_lo, s_hi, rec,
+                                  reinterpret_cast<unsigned char*>(rec_sm), fr, &dsum)) {
+          gave_up = true;  // block-uniform: the staged pass ends in a block-wide vote
+          if (threadIdx.x == 0) record_status(h, SPEC_ERR_TIMEOUT);
+        }
+      } else {
+        slice_records(trow, drow, p.V, ms, bonus, s_lo, s_hi, rec, vec_ok, &dsum);
+      }
+      if (job == kJobResidual) {
+        // The slice's share of D, summed over the block in float-float.
+        FF total;
+        (void)block_exclusive_scan_ff(dsum, sh, &total);
+        if (threadIdx.x == 0) __stcg(&slice_out[part], make_float2(total.hi, total.lo));
+      }
     }
   }
-
-  // ---- the last slice CTA of the request combines ----
+  // ---- the last slice CTA of the request writes the outputs ----
+  // Every slice counts itself in, also one without rows to stream or one
+  // that gave up, so that the count always completes.
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    sh.last = atomicAdd(&final_done[b], 1) == P - 1;
+    const int inc = 1 + (gave_up ? kLateMark : 0);
+    const int old = atomicAdd(&final_done[b], inc);
+    sh.last = (old & kArriveMask) == P - 1;
+    sh.any_late = (old + inc) >= kLateMark;
   }
   __syncthreads();
   if (!sh.last) return;
   __threadfence();
+  if (sh.any_late) {  // some slice has no outcome or no records: no token
+    write_outputs(true, -1);
+    return;
+  }
+  if (!rows_job) {
+    write_outputs(job == kJobInvalid, token);
+    return;
+  }
 
   bool bad = false;
   if (job == kJobGreedyRowL) {
@@ -764,9 +932,10 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
       ArgAcc r;
       arg_init(r);
       for (int q = 0; q < P; ++q) {
+        const float2 so = __ldcg(&slice_out[q]);
         ArgAcc o;
-        o.v = __ldcg(&slice_ref[q]);
-        o.i = __ldcg(&slice_arg[q]);
+        o.v = so.x;
+        o.i = __float_as_int(so.y);
         arg_merge(r, o);
       }
       sh.token = r.i;
@@ -776,16 +945,33 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
     bad = (token == INT32_MAX);
   } else {
     const float u = __ldg(&p.uniforms[(size_t)b * (p.k + 1) + L]);
-    token = cdf_pick(trow, drow, p.V, ms, bonus, u, rec, nseg, vec_ok, sh, rec_sm);
+    // Residual: D = sum (p - q) over the row pair from the slices' shares,
+    // then mu = D / (1 - D), the correction for the normalisers' ratio.
+    float mu = 0.0f;
+    if (job == kJobResidual) {
+      if (threadIdx.x == 0) {
+        FF D = {0.0f, 0.0f};
+        for (int q = 0; q < P; ++q) {
+          const float2 so = __ldcg(&slice_out[q]);
+          D = ff_add(D, FF{so.x, so.y});
+        }
+        const float Df = ff_to_float(D);
+        sh.mu = (Df > -1.0f && Df < 1.0f) ? __fdiv_rn(Df, __fsub_rn(1.0f, Df)) : 0.0f;
+      }
+      __syncthreads();
+      mu = sh.mu;
+    }
+    token = cdf_pick(trow, drow, p.V, ms, bonus, u, rec, nseg, vec_ok, sh, rec_sm, mu);
     if (token < 0 && job == kJobResidual) {
       // Residual mass zero (p_n == q_n up to rounding): draw from p_n.
       if (threadIdx.x == 0) atomicAdd(&h->residual_zero, 1);
       MassSpec pm = ms;
       pm.has_q = false;
-      slice_records(trow, trow, p.V, pm, false, 0, nseg, rec, vec_ok);
+      FF unused = {0.0f, 0.0f};
+      slice_records(trow, trow, p.V, pm, false, 0, nseg, rec, vec_ok, &unused);
       __threadfence_block();
       __syncthreads();
-      token = cdf_pick(trow, trow, p.V, pm, false, u, rec, nseg, vec_ok, sh, rec_sm);
+      token = cdf_pick(trow, trow, p.V, pm, false, u, rec, nseg, vec_ok, sh, rec_sm, 0.0f);
     }
     bad = (token < 0);
   }

@@ -289,6 +289,7 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
   fp.ws = ws;
   fp.lay = lay;
   fp.sweep_grid = (int)grid;
+  fp.test_late = (flags & SPEC_FLAG_TEST_LATE_SLICES) ? 1 : 0;
   const int nseg = segments_of(V);
   // Slices per request: one wave of four CTAs per SM over the batch, each
   // slice at least one segment.
@@ -476,7 +477,8 @@ static spec_status_t verify_entry(const void* target_logits, const void* draft_l
   if (B < 1 || k < 1 || V < 1) return SPEC_ERR_INVALID_ARG;
   if (!sizes_ok(B, k, V)) return SPEC_ERR_UNSUPPORTED;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
-  if ((flags & ~SPEC_FLAG_FULL_SWEEP) != 0) return SPEC_ERR_INVALID_ARG;
+  if ((flags & ~(SPEC_FLAG_FULL_SWEEP | SPEC_FLAG_TEST_LATE_SLICES)) != 0)
+    return SPEC_ERR_INVALID_ARG;
   const bool packed = (t_start != nullptr);
   if (packed) {
     if (!d_start || !aligned(t_start, 4) || !aligned(d_start, 4)) return SPEC_ERR_INVALID_ARG;

@@ -8,13 +8,18 @@ import oracle
 
 # A decision is a near-tie when its uniform lies within this distance of the
 # threshold it is compared with (accept test or an edge of the sampled CDF
-# cell): there the fp32 GPU path and the fp64 oracle may legitimately differ.
-# Near-ties are a property of the inputs (a long-tailed vocabulary has many
-# CDF cells narrower than the band) and are only counted.
+# cell): there the fp32 GPU path and the fp64 oracle may legitimately differ,
+# and such requests are counted and reported instead of compared.  Near-ties
+# are a property of the inputs: a long-tailed vocabulary has many CDF cells
+# narrower than the band, so a few percent of requests are near-ties.
 NEAR_TIE = 1e-6
-# Mismatches excused by a near-tie may be at most this fraction of the logit
-# rows evaluated (at least one per comparison).
-NEAR_TIE_RATE = 1e-5
+# A near-tie may flip only where the GPU's own arithmetic error could flip
+# it: its distance from the threshold must be below the kernels' error bound
+# on a decision (normalised CDF and accept ratio, about 1e-8 typical and
+# below 1e-7 measured, see the design notes), and at most this fraction of
+# the near-ties may flip (at least one per comparison).
+KERNEL_DECISION_ERR = 2e-7
+FLIP_RATE = 0.05
 
 
 def evaluated_rows(o: oracle.OracleResult, temperature: np.ndarray) -> int:
@@ -36,10 +41,12 @@ def compare(gpu_out: np.ndarray, gpu_n: np.ndarray, o: oracle.OracleResult,
     near = (o.margin < NEAR_TIE) & ~greedy & (o.num_accepted >= 0)
     same = (gpu_n == o.num_accepted) & np.all(gpu_out == o.out_tokens, axis=1)
     bad = ~same & ~near
+    flips = ~same & near
     rows = evaluated_rows(o, temperature)
     info = dict(requests=len(gpu_n), mismatches=int((~same).sum()), near_ties=int(near.sum()),
-                excused=int((~same & near).sum()), mismatches_outside_band=int(bad.sum()),
-                rows=rows)
+                excused=int(flips.sum()), mismatches_outside_band=int(bad.sum()),
+                rows=int(rows),
+                max_flip_margin=float(o.margin[flips].max()) if flips.any() else 0.0)
     if bad.any():
         b = int(np.nonzero(bad)[0][0])
         raise AssertionError(
@@ -47,7 +54,8 @@ def compare(gpu_out: np.ndarray, gpu_n: np.ndarray, o: oracle.OracleResult,
             f"(margin {o.margin[b]:.3g}, T {temperature[b]}): gpu n={gpu_n[b]} "
             f"out={gpu_out[b].tolist()} oracle n={o.num_accepted[b]} "
             f"out={o.out_tokens[b].tolist()}; {info}")
-    assert info["excused"] <= max(1, NEAR_TIE_RATE * rows), (label, info)
+    assert info["max_flip_margin"] < KERNEL_DECISION_ERR, (label, info)
+    assert info["excused"] <= max(1, FLIP_RATE * info["near_ties"]), (label, info)
     return info
 
 

@@ -351,3 +351,41 @@ def test_timed_call_and_device_status():
     d["lengths"][3] = 0  # an invalid length: recorded on the device
     sv.spec_verify(**d, workspace=ws)
     assert sv.spec_verify_device_status(ws) == sv.SPEC_ERR_BAD_INPUT
+
+
+def test_timed_out_slices_leave_minus_one_and_the_next_call_works():
+    """A final-pass slice that gives up waiting still counts itself in, and the
+    request then reports -1 (not stale outputs).  The testing flag makes every
+    slice but the first of each request wait, bounded, for an event that never
+    happens; the workspace records SPEC_ERR_TIMEOUT, and a normal call on the
+    same workspace right after matches the oracle."""
+    inp = synth.make_inputs("zipf_mixed_temp", 8, 6, 4096, "bf16", seed=61)
+    d = sv.to_device(inp)
+    ws = sv.alloc_workspace(inp.B, inp.k, inp.V)
+    out = torch.full((inp.B, inp.k + 1), 123, dtype=torch.int32, device="cuda")
+    n = torch.full((inp.B,), 123, dtype=torch.int32, device="cuda")
+    sv.spec_verify(**d, workspace=ws, out_tokens=out, num_accepted=n,
+                   flags=sv.SPEC_FLAG_TEST_LATE_SLICES)
+    assert sv.spec_verify_device_status(ws) == sv.SPEC_ERR_TIMEOUT
+    # 8 requests over 16 segments: every request has several slices.
+    assert np.all(n.cpu().numpy() == -1)
+    assert np.all(out.cpu().numpy() == -1)
+    out2, n2 = sv.spec_verify(**d, workspace=ws, out_tokens=out, num_accepted=n)
+    rep = sv.spec_verify_report(ws)
+    assert rep.status == sv.SPEC_OK, rep
+    o = oracle.verify(inp.target, inp.draft, inp.tokens, inp.lengths, inp.uniforms,
+                      inp.temperature)
+    compare(out2.cpu().numpy(), n2.cpu().numpy(), o, inp.temperature, "after timeouts")
+
+
+def test_one_slice_per_request_is_not_affected_by_the_late_flag():
+    """With a single segment per row every request has exactly one slice (the
+    first), so the testing flag changes nothing."""
+    inp = synth.make_inputs("zipf_mixed_temp", 12, 5, 200, "f32", seed=62)
+    d = sv.to_device(inp)
+    ws = sv.alloc_workspace(inp.B, inp.k, inp.V)
+    out, n = sv.spec_verify(**d, workspace=ws, flags=sv.SPEC_FLAG_TEST_LATE_SLICES)
+    assert sv.spec_verify_device_status(ws) == sv.SPEC_OK
+    o = oracle.verify(inp.target, inp.draft, inp.tokens, inp.lengths, inp.uniforms,
+                      inp.temperature)
+    compare(out.cpu().numpy(), n.cpu().numpy(), o, inp.temperature, "one slice")
