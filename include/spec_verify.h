@@ -124,8 +124,12 @@ size_t spec_verify_workspace_bytes(int B, int k, int V);
  *
  * Logit pointers must be aligned to their element size; 16-byte aligned rows
  * (V * element size a multiple of 16 and 16-byte aligned bases) take the fast
- * path.  Logits may contain -inf; every row that is read must have at least
- * one finite entry, and NaN or +inf make the request invalid.
+ * path.  Logits may contain -inf.  A sampling request (T > 0) needs finite,
+ * positive mass in every row it reads: a NaN or +inf logit in such a row, or
+ * a row of only -inf, makes the request invalid.  A greedy request (T = 0)
+ * only takes argmaxes: a NaN entry is never the maximum, +inf is a maximum
+ * like any other value (the lowest index among equal maxima wins), and a row
+ * with no entry above -inf makes the request invalid.
  *
  * Returns SPEC_OK once the work is enqueued, or an error code (nothing
  * enqueued).

@@ -68,6 +68,7 @@ struct FinalShared {
 constexpr int kLateMark = 1 << 16;
 constexpr int kArriveMask = kLateMark - 1;  // slices arrived (P <= kMaxSlices)
 static_assert(kMaxSlices < kLateMark, "the arrival count stays below the late mark");
+static_assert(kMaxSlices <= 64 && kFinalThreads >= 64, "slice results reduce over two warps");
 // The testing aid's wait: slices other than the first wait this long for an
 // event that never happens, as if their request's outcome never arrived.
 constexpr unsigned long long kTestLateLimitNs = 1000000ull;
@@ -151,12 +152,11 @@ __device__ __forceinline__ float2 f32x2_sub(float2 a, float2 b) {
 //     normalised, the residual is max(0, p - (1 + mu) q) with
 //     mu = D / (1 - D), and each segment's weight is corrected by
 //     -mu * (its q mass where p > q) in the combine.
-// a, c_d and dc = c_d - a are carried as hi + lo single-precision pairs
+// a and dc = c_d - a are carried as hi + lo single-precision pairs
 // (float-float) so that they keep their accuracy.
 struct MassSpec {
   float sc;
   float a_hi, a_lo;
-  float cd_hi, cd_lo;
   float dc_hi, dc_lo;
   bool has_q;
 };
@@ -189,20 +189,24 @@ __device__ __forceinline__ void residual_entries(const Seg8<TIn>& t, const Seg8<
                                                  const MassSpec& ms, float (&rh)[8],
                                                  float (&qb)[8]) {
   const float2 sc2 = make_float2(ms.sc, ms.sc);
-  const float2 na2 = make_float2(-ms.a_hi, -ms.a_hi), al2 = make_float2(ms.a_lo, ms.a_lo);
-  const float2 nc2 = make_float2(-ms.cd_hi, -ms.cd_hi), cl2 = make_float2(ms.cd_lo, ms.cd_lo);
-  const float2 nd2 = make_float2(-ms.dc_hi, -ms.dc_hi), dl2 = make_float2(ms.dc_lo, ms.dc_lo);
+  const float2 na2 = make_float2(-ms.a_hi, -ms.a_hi);
+  const float2 nd2 = make_float2(-ms.dc_hi, -ms.dc_hi), dh2 = make_float2(ms.dc_hi, ms.dc_hi);
   const float2 h1 = make_float2(kTh1, kTh1), h2 = make_float2(kTh2, kTh2);
   const float2 h3 = make_float2(kTh3, kTh3), h4 = make_float2(kTh4, kTh4);
   const float2 h5 = make_float2(kTh5, kTh5), h0 = make_float2(kTh0, kTh0);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const float2 zt = seg_pair(t, j), zd = seg_pair(d, j);
-    const float2 a = ex2x2(f32x2_sub(f32x2_fma(zt, sc2, na2), al2));  // p
-    const float2 b = ex2x2(f32x2_sub(f32x2_fma(zd, sc2, nc2), cl2));  // q
-    // zd - zt is exact for bf16 logits (rounded once for fp32); the fused
-    // multiply-add rounds delta once more, relative to delta itself.
-    const float2 dl = f32x2_sub(f32x2_fma(f32x2_sub(zd, zt), sc2, nd2), dl2);
+    // p and q relative to the high parts of the normalisers only: the low
+    // parts would scale every p, or every q, by the same factor 1 + O(1e-7),
+    // which the mu correction absorbs like any other normaliser error.  q is
+    // formed with the same two high parts that delta subtracts, so that
+    // q / p = 2^delta holds to rounding.  zd - zt is exact for bf16 logits
+    // (rounded once for fp32); the fused multiply-add rounds delta once more,
+    // relative to delta itself.
+    const float2 a = ex2x2(f32x2_fma(zt, sc2, na2));
+    const float2 b = ex2x2(f32x2_sub(f32x2_fma(zd, sc2, na2), dh2));
+    const float2 dl = f32x2_fma(f32x2_sub(zd, zt), sc2, nd2);
     const float2 w = f32x2_mul(dl, dl);
     float2 poly = f32x2_fma(h5, w, h4);
     poly = f32x2_fma(poly, w, h3);
@@ -873,8 +877,6 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
       const float4 c4 = sh.pos_c[n];
       ms.a_hi = c4.x;
       ms.a_lo = c4.y;
-      ms.cd_hi = c4.z;
-      ms.cd_lo = c4.w;
       const FF dc = ff_sub(FF{c4.z, c4.w}, FF{c4.x, c4.y});
       ms.dc_hi = dc.hi;
       ms.dc_lo = dc.lo;
@@ -928,16 +930,26 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
 
   bool bad = false;
   if (job == kJobGreedyRowL) {
-    if (threadIdx.x == 0) {
+    // The P <= 64 slice maxima, one per lane of the first two warps.
+    if (threadIdx.x < 64) {
       ArgAcc r;
       arg_init(r);
-      for (int q = 0; q < P; ++q) {
-        const float2 so = __ldcg(&slice_out[q]);
-        ArgAcc o;
-        o.v = so.x;
-        o.i = __float_as_int(so.y);
-        arg_merge(r, o);
+      if ((int)threadIdx.x < P) {
+        const float2 so = __ldcg(&slice_out[threadIdx.x]);
+        r.v = so.x;
+        r.i = __float_as_int(so.y);
       }
+      arg_warp_reduce(r);
+      if ((threadIdx.x & 31) == 0) {
+        sh.warp_f[threadIdx.x >> 5] = r.v;
+        sh.warp_i[threadIdx.x >> 5] = r.i;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      ArgAcc r = {sh.warp_f[0], sh.warp_i[0]};
+      const ArgAcc o = {sh.warp_f[1], sh.warp_i[1]};
+      arg_merge(r, o);
       sh.token = r.i;
     }
     __syncthreads();
@@ -949,13 +961,19 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
     // then mu = D / (1 - D), the correction for the normalisers' ratio.
     float mu = 0.0f;
     if (job == kJobResidual) {
-      if (threadIdx.x == 0) {
+      // The P <= 64 shares, one per lane of the first two warps.
+      if (threadIdx.x < 64) {
         FF D = {0.0f, 0.0f};
-        for (int q = 0; q < P; ++q) {
-          const float2 so = __ldcg(&slice_out[q]);
-          D = ff_add(D, FF{so.x, so.y});
+        if ((int)threadIdx.x < P) {
+          const float2 so = __ldcg(&slice_out[threadIdx.x]);
+          D = FF{so.x, so.y};
         }
-        const float Df = ff_to_float(D);
+        D = warp_sum_ff(D);
+        if ((threadIdx.x & 31) == 0) sh.warp_ff[threadIdx.x >> 5] = D;
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const float Df = ff_to_float(ff_add(sh.warp_ff[0], sh.warp_ff[1]));
         sh.mu = (Df > -1.0f && Df < 1.0f) ? __fdiv_rn(Df, __fsub_rn(1.0f, Df)) : 0.0f;
       }
       __syncthreads();
@@ -989,7 +1007,7 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
 }
 
 template <typename TIn>
-__global__ void __launch_bounds__(kFinalThreads, 4) final_kernel(FinalParams p) {
+__global__ void __launch_bounds__(kFinalThreads, 3) final_kernel(FinalParams p) {
   extern __shared__ __align__(128) unsigned char fsm_raw[];
   __shared__ FinalShared sh;
   __shared__ FinalRing fr;

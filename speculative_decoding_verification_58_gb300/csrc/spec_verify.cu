@@ -291,9 +291,10 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
   fp.sweep_grid = (int)grid;
   fp.test_late = (flags & SPEC_FLAG_TEST_LATE_SLICES) ? 1 : 0;
   const int nseg = segments_of(V);
-  // Slices per request: one wave of four CTAs per SM over the batch, each
-  // slice at least one segment.
-  int P = (4 * d->sms) / B;
+  // Slices per request: one wave of three CTAs per SM over the batch, but at
+  // least two (a request's residual pair is 1.2 MB in fp32, too much for one
+  // CTA at the end of a round), each slice at least one segment.
+  int P = std::max(2, (3 * d->sms) / B);
   if (P > kMaxSlices) P = kMaxSlices;
   if (P > nseg) P = nseg;
   if (P < 1) P = 1;

@@ -189,6 +189,49 @@ def test_greedy_ties_and_worked_example_structure():
     assert rep.status == sv.SPEC_OK
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_greedy_rows_with_nan_and_inf_match_oracle(dtype):
+    """Greedy rows are only argmaxed: a NaN entry is never the maximum, +inf is
+    a maximum like any other (lowest index wins), and only a row with nothing
+    above -inf makes the request invalid."""
+    B, k, V = 24, 6, 2000
+    rng = np.random.default_rng(71)
+    tl = rng.standard_normal((B, k + 1, V)).astype(np.float32)
+    dl = rng.standard_normal((B, k, V)).astype(np.float32)
+    for b in range(B):
+        for i in range(k + 1):
+            tl[b, i, rng.integers(0, V, 5)] = np.nan       # NaN entries anywhere
+    for b in range(0, B, 3):
+        i = b % (k + 1)
+        tl[b, i, np.argmax(np.nan_to_num(tl[b, i], nan=-np.inf))] = np.nan  # NaN at the max
+    for b in range(1, B, 4):
+        i = (b + 2) % (k + 1)
+        tl[b, i, [700, 300, 1500]] = np.inf               # +inf wins, lowest index (300)
+    tl[5, 2] = -np.inf
+    tl[5, 2, 17] = np.nan                                  # nothing above -inf: invalid
+    # Draft tokens: the argmax where it exists (so rounds run on), with a
+    # seeded wrong token now and then.
+    best = np.nanargmax(np.where(np.isnan(tl[:, :k]), -np.inf, tl[:, :k]), axis=2).astype(np.int32)
+    tok = best.copy()
+    wrong = rng.random((B, k)) < 0.2
+    tok[wrong] = rng.integers(0, V, wrong.sum())
+    tok[5, :2] = best[5, :2]                               # request 5 reaches its bad row 2
+    inp = synth.SpecInputs(tl, dl, tok, rng.integers(1, k + 1, B).astype(np.int32),
+                           synth.uniform_24bit(rng, (B, k + 1)), np.zeros(B, np.float32), "f32")
+    inp.lengths[5] = k
+    if dtype == "bf16":
+        inp.target, inp.draft, inp.dtype = synth.bf16_bits(tl), synth.bf16_bits(dl), "bf16"
+    out, n, rep = run_gpu(inp)
+    o = oracle.verify(inp.target, inp.draft, inp.tokens, inp.lengths, inp.uniforms,
+                      inp.temperature)
+    np.testing.assert_array_equal(n, o.num_accepted)
+    np.testing.assert_array_equal(out, o.out_tokens)
+    assert o.num_accepted[5] == -1 and o.bad_requests == 1
+    assert rep.status == sv.SPEC_ERR_BAD_INPUT and rep.bad_requests == 1
+    # Some request was stopped by, or emitted, a +inf argmax at index 300.
+    assert np.any(out == 300)
+
+
 def test_disjoint_supports_and_masked_logits():
     inp = _inputs(50, 4, 512, "f32", seed=3)
     inp.target[:, :, 256:] = -np.inf
