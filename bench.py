@@ -620,6 +620,39 @@ class OurArm:
                 "gbs": obytes / (oms * 1e-3) / 1e9,
                 "loss_mean": float(st.loss.float().mean().item())}
 
+    def opd_fused_leg(self):
+        """Verification and OPD statistics in one pass (spec_verify_opd): every
+        verified row pair read once for both; compared with the round and the
+        statistics run separately."""
+        sv, inp = self.sv, self.inp
+        st = None
+
+        def call(j):
+            nonlocal st
+            dc = self.w.ds[j % len(self.w.ds)]
+            _, _, st = sv.spec_verify_opd(**dc, workspace=self.ws, out_tokens=self.out,
+                                          num_accepted=self.nacc, out=st, stream=self.stream)
+        for j in range(3):
+            call(j)
+        self.sync()
+        reps = max(10, min(self.args.steps, 100))
+        f0, f1 = _event_pair()
+        f0.record(self.stream)
+        for j in range(reps):
+            call(j)
+        f1.record(self.stream)
+        self.sync()
+        fms = f0.elapsed_time(f1) / reps
+        out, n = self.out.cpu().numpy(), self.nacc.cpu().numpy()
+        positions = int(inp.lengths.sum())
+        obytes = positions * 2 * inp.V * self.esize
+        return {"ms_per_call": fms, "positions": positions, "bytes_per_call": obytes,
+                "gbs": obytes / (fms * 1e-3) / 1e9,
+                "same_verification_outputs": bool(np.array_equal(out, self.gpu_out) and
+                                                  np.array_equal(n, self.gpu_n)),
+                "requests_differing": int(np.sum(np.any(out != self.gpu_out, axis=1) |
+                                                 (n != self.gpu_n)))}
+
     def d3d_leg(self):
         """D3D branch selection on this round's outcome: the paper's main budget
         (block 16, coverage C = 12, fan-out F = 2, 24 branches per request)."""
@@ -798,6 +831,7 @@ class OurArm:
         full = None if args.no_full_sweep else self.full_sweep_leg()
         packed = None if args.no_packed else self.packed_leg()
         opd = None if args.no_opd else self.opd_leg()
+        opd_fused = None if args.no_opd else self.opd_fused_leg()
         d3d = None if args.no_d3d else self.d3d_leg()
         e2e, e2e_padded = self.e2e_legs()
         clocks = sampler.stop()
@@ -840,6 +874,10 @@ class OurArm:
         if opd is not None:
             opd["frac"] = opd["gbs"] / hbm_peak
             result["opd"] = opd
+        if opd_fused is not None:
+            opd_fused["frac"] = opd_fused["gbs"] / hbm_peak
+            opd_fused["separate_ms"] = ms + (opd["ms_per_call"] if opd else 0.0)
+            result["opd_fused"] = opd_fused
         if d3d is not None:
             result["d3d"] = d3d
         if per_workload is not None:

@@ -318,6 +318,33 @@ spec_status_t spec_opd_stats(const void* target_logits, const void* draft_logits
                              float* rkl_clip, float* loss, void* stream);
 
 /*
+ * Verification and OPD statistics in one pass over the batch (AdaFlash
+ * Section 3.1: the supervision comes from the rows verification reads;
+ * Section 2.1 for the rule).  Arguments are spec_verify's (inputs, outputs,
+ * workspace) followed by spec_opd_stats's (delta, alpha and the five
+ * statistics outputs), with the same meaning, layouts and ranges; the
+ * results equal those of the two calls, up to the near-ties of the
+ * verification rule.
+ *
+ * Every verified row pair (i < L_b) is read once from memory for both: the
+ * statistics need all L_b positions, so there is no early exit.  At T_b = 1
+ * the statistics' normalisers decide position i; at T_b = 0 the target
+ * argmax does; any other T_b adds a second pair of softmax sums.  The final
+ * token then comes from the same final pass as spec_verify (residual row
+ * pair, or bonus row L_b).  Device-detected errors and the status word
+ * behave as for spec_verify (read them with spec_verify_device_status on
+ * `workspace`); the statistics of a request whose L_b is valid are computed
+ * even when another of its inputs is invalid.  Padded layout only.
+ */
+spec_status_t spec_verify_opd(const void* target_logits, const void* draft_logits,
+                              spec_dtype_t dtype, const int32_t* draft_tokens,
+                              const int32_t* lengths, const float* uniforms,
+                              const float* temperature, int B, int k, int V, float delta,
+                              float alpha, int32_t* out_tokens, int32_t* num_accepted,
+                              int32_t* x_star, float* hard, float* rkl, float* rkl_clip,
+                              float* loss, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * D3D branch selection after a verification round ("D3D: Decoupled
  * Diffusion Drafting for Asynchronous Speculative Decoding", Methodology,
  * asynchronous inference).  While the target verifies a block, a packed

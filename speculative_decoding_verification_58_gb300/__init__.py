@@ -17,6 +17,7 @@ The functions keep the C names:
 ``spec_verify_device_status(ws)``    just the recorded status
 ``spec_row_stats(...)``              the row sweep alone: max, logsumexp, argmax
 ``spec_opd_stats(...)``              OPD supervision statistics (hard label, reverse KL, clipped)
+``spec_verify_opd(...)``             verification and OPD statistics in one pass over the rows
 ``spec_d3d_select(...)``             D3D branch selection: reuse a prepared successor block
 ``spec_status_string(code)``
 """
@@ -48,7 +49,7 @@ EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_ex", "spec
            "spec_verify_packed", "spec_verify_report",
            "spec_verify_device_status", "spec_row_stats_workspace_bytes", "spec_row_stats",
            "spec_status_string", "spec_abi_version", "spec_verify_static", "spec_opd_stats",
-           "spec_d3d_select")
+           "spec_verify_opd", "spec_d3d_select")
 SPEC_STATIC_SCRATCH_BYTES = 8 << 20
 
 
@@ -121,6 +122,10 @@ def lib() -> ctypes.CDLL:
     L.spec_opd_stats.argtypes = [vp, vp, ci, i32p, ci, ci, ci, ctypes.c_float, ctypes.c_float,
                                  i32p, f32p, f32p, f32p, f32p, vp]
     L.spec_opd_stats.restype = ci
+    L.spec_verify_opd.argtypes = [vp, vp, ci, i32p, i32p, f32p, f32p, ci, ci, ci, ctypes.c_float,
+                                  ctypes.c_float, i32p, i32p, i32p, f32p, f32p, f32p, f32p, vp, csz,
+                                  vp]
+    L.spec_verify_opd.restype = ci
     L.spec_d3d_select.argtypes = [i32p, i32p, i32p, i32p, i32p, ci, ci, ci, ci, i32p, i32p, i32p,
                                   vp]
     L.spec_d3d_select.restype = ci
@@ -475,6 +480,52 @@ def spec_opd_stats(target_logits, draft_logits, lengths, *, delta: float = 0.01,
                                 out.rkl_clip.data_ptr(), out.loss.data_ptr(), _stream_ptr(stream)),
            "spec_opd_stats")
     return out
+
+
+def spec_verify_opd(target_logits, draft_logits, draft_tokens, lengths, uniforms, temperature, *,
+                    delta: float = 0.01, alpha: float = 0.8, workspace=None, out_tokens=None,
+                    num_accepted=None, out=None, stream=None):
+    """Verification and OPD statistics in one pass over the rows.
+
+    Arguments as ``spec_verify`` plus ``delta`` and ``alpha`` as
+    ``spec_opd_stats``; ``out`` may be an ``OpdStats`` of preallocated
+    tensors.  Returns (out_tokens, num_accepted, OpdStats).
+    """
+    torch = _torch()
+    B, k1, V = target_logits.shape
+    k = k1 - 1
+    dev = target_logits.device
+    dt = _dtype_code(target_logits)
+    _need(target_logits, "target_logits", target_logits.dtype, (B, k + 1, V), dev)
+    _need(draft_logits, "draft_logits", target_logits.dtype, (B, k, V), dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, k), dev)
+    _need(lengths, "lengths", torch.int32, (B,), dev)
+    _need(uniforms, "uniforms", torch.float32, (B, k + 1), dev)
+    _need(temperature, "temperature", torch.float32, (B,), dev)
+    if workspace is None:
+        workspace = alloc_workspace(B, k, V, dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, k + 1), dtype=torch.int32, device=dev)
+    if num_accepted is None:
+        num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _need(out_tokens, "out_tokens", torch.int32, (B, k + 1), dev)
+    _need(num_accepted, "num_accepted", torch.int32, (B,), dev)
+    if out is None:
+        f = dict(dtype=torch.float32, device=dev)
+        out = OpdStats(torch.empty((B, k), dtype=torch.int32, device=dev), torch.empty((B, k), **f),
+                       torch.empty((B, k), **f), torch.empty((B, k), **f), torch.empty(B, **f))
+    _need(out.x_star, "x_star", torch.int32, (B, k), dev)
+    for name in ("hard", "rkl", "rkl_clip"):
+        _need(getattr(out, name), name, torch.float32, (B, k), dev)
+    _need(out.loss, "loss", torch.float32, (B,), dev)
+    _check(lib().spec_verify_opd(
+        target_logits.data_ptr(), draft_logits.data_ptr(), dt, draft_tokens.data_ptr(),
+        lengths.data_ptr(), uniforms.data_ptr(), temperature.data_ptr(), B, k, V, float(delta),
+        float(alpha), out_tokens.data_ptr(), num_accepted.data_ptr(), out.x_star.data_ptr(),
+        out.hard.data_ptr(), out.rkl.data_ptr(), out.rkl_clip.data_ptr(), out.loss.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
+        "spec_verify_opd")
+    return out_tokens, num_accepted, out
 
 
 def spec_d3d_select(num_accepted, out_tokens, branch_pos, branch_tok, branch_block, *,

@@ -24,6 +24,15 @@
 // evict-last hint, pass 2 loads evict-first.  Two CTAs per SM.  Clusters
 // that would hold whole rows in shared memory need 8 or 16 CTAs, which leave
 // a fifth of GB300's SMs idle.
+//
+// Verification in the same pass (spec_verify_opd): the statistics read every
+// verified row pair anyway, so the same kernel also decides each position of
+// a valid request at T = 1 (the statistics' own normalisers: accept iff
+// u_i < min(1, p(x_i) / q(x_i)), AdaFlash Section 2.1) or T = 0 (accept iff
+// x_i is the target argmax) and publishes the decision, the row normalisers
+// and the argmax exactly as the row sweep does, so that the final pass
+// samples the residual or bonus token unchanged.  Requests at any other
+// temperature are left to the row sweep, which runs after this kernel.
 #pragma once
 
 #include "common.cuh"
@@ -46,6 +55,14 @@ struct OpdParams {
   const void* target;      // [B, k+1, V]
   const void* draft;       // [B, k, V]
   const int32_t* lengths;  // [B]
+  // Verification in the same pass (verify != 0): inputs, and the workspace the
+  // plan kernel prepared and the final pass reads.
+  int verify;
+  const int32_t* tokens;     // [B, k]
+  const float* uniforms;     // [B, k+1]
+  const float* temperature;  // [B]
+  unsigned char* ws;
+  WsLayout lay;
   int B, k, V;
   int slice;     // elements of each row per CTA of a cluster (multiple of 8)
   int vec_ok;    // rows 16-byte aligned: bulk copies; else ordinary loads
@@ -430,12 +447,79 @@ __device__ __forceinline__ void opd_p1_unpack(const OpdP1& a, bool have, SoftAcc
   }
 }
 
+// Both rows' base-2 log normalisers L2 = ref + log2(S) (float-float) from the
+// parts the lanes hold (lane r: rank r's part; lanes without one hold the
+// identity).  Reference exponents: the largest fl(max * scale) of each row;
+// the parts' sums are brought to it and added in float-float.  Warp-wide;
+// every lane gets the same values.  Returns whether both rows have finite,
+// positive mass.
+__device__ __forceinline__ bool opd_pair_norms(const SoftAcc& t, const SoftAcc& d, bool have,
+                                               FF* l2t, FF* l2d) {
+  const float rt = group_max(t.ms, 5), rd = group_max(d.ms, 5);
+  FF st = {0.0f, 0.0f}, sd = {0.0f, 0.0f};
+  if (have) {
+    if (t.s != 0.0f) st = two_prod(t.s, ex2(__fsub_rn(t.ms, rt)));
+    if (d.s != 0.0f) sd = two_prod(d.s, ex2(__fsub_rn(d.ms, rd)));
+  }
+  st = warp_sum_ff(st);
+  sd = warp_sum_ff(sd);
+  const float St = ff_to_float(st), Sd = ff_to_float(sd);
+  *l2t = ff_add_f(two_sum(rt, log2f(st.hi)), __fdiv_rn(st.lo, st.hi) * kLog2e);
+  *l2d = ff_add_f(two_sum(rd, log2f(sd.hi)), __fdiv_rn(sd.lo, sd.hi) * kLog2e);
+  return St > 0.0f && St <= FLT_MAX && Sd > 0.0f && Sd <= FLT_MAX;
+}
+
+// The accept decision of position i of request b (verification mode; one
+// thread), published as the row sweep publishes it: normalisers or argmax,
+// bad-row bit, first rejection and the decision bits (a rejection releases
+// the writes before it).  T is 0 or 1; l2t / l2d: log2 normalisers at
+// temperature 1.
+template <typename TIn>
+__device__ __noinline__ void opd_decide(const OpdParams& p, int b, int i, int x, float T, float u,
+                                        float zt_x, float zd_x, ArgAcc g, FF l2t, FF l2d,
+                                        bool sums_ok) {
+  const size_t bi = (size_t)b * p.k + i;
+  bool accept, row_ok;
+  if (T == 0.0f) {
+    row_ok = (g.i != INT32_MAX);
+    accept = (g.i == x);
+    __stcg(reinterpret_cast<int32_t*>(p.ws + p.lay.pos_arg) + bi, g.i);
+  } else {
+    row_ok = sums_ok;
+    const float sc = kLog2e;
+    // As in the row sweep's decision: a token the target gives probability
+    // zero is never accepted, one the drafter gives zero always is;
+    // otherwise d = log2 p(x) - log2 q(x) in float-float and 2^d.
+    float ratio;
+    if (zt_x == -INFINITY) {
+      ratio = 0.0f;
+    } else if (zd_x == -INFINITY) {
+      ratio = 1.0f;
+    } else {
+      const FF dd = ff_sub(ff_sub(two_prod(zt_x, sc), l2t), ff_sub(two_prod(zd_x, sc), l2d));
+      const float df = ff_to_float(dd);
+      ratio = df >= 0.0f ? 1.0f : exp2f(df);
+    }
+    accept = u < ratio;
+    __stcg(reinterpret_cast<float4*>(p.ws + p.lay.pos_c) + bi,
+           make_float4(l2t.hi, l2t.lo, l2d.hi, l2d.lo));
+  }
+  if (!row_ok) {
+    accept = false;
+    atomicOr(reinterpret_cast<uint32_t*>(p.ws + p.lay.bad_bits) + b, 1u << i);
+  }
+  unsigned long long* state = reinterpret_cast<unsigned long long*>(p.ws + p.lay.state) + b;
+  if (!accept) atomicMin(reinterpret_cast<int32_t*>(p.ws + p.lay.first_reject) + b, i);
+  if (accept) atomicOr(state, decision_bits(i, true));
+  else atom_or_release_u64(state, decision_bits(i, false));
+}
+
 // ---------------------------------------------------------------------------
 // Bookkeeping warp: merges the consumer warps' partials, exchanges them with
 // the other CTA of the cluster, publishes the normalisers (pass 1) or writes
 // the position's results (pass 2, rank 0).
 // ---------------------------------------------------------------------------
-template <typename TIn>
+template <typename TIn, bool kVerify>
 __device__ void opd_bookkeeper(const OpdParams& p, OpdSmem& sm, int cid, int ncl, uint32_t CS,
                                uint32_t rank) {
   const int lane = threadIdx.x & 31;
@@ -455,6 +539,27 @@ __device__ void opd_bookkeeper(const OpdParams& p, OpdSmem& sm, int cid, int ncl
     const uint32_t par = (j >> 1) & 1;
     const int b = q / p.k, i = q - b * p.k;
     if (pass == 1) {
+      // Verification (rank 0, lane 0) of a valid request at T = 0 or 1: what
+      // the decision needs, loaded before the wait so that the loads overlap
+      // it.  The plan kernel has checked the request's inputs (tokens in
+      // range for a valid request).
+      int vflags = 0, x = 0;
+      float T = 0.0f, u = 0.0f, zt_x = 0.0f, zd_x = 0.0f;
+      if (kVerify && rank == 0 && lane == 0) {
+        vflags = __ldcg(reinterpret_cast<const int32_t*>(p.ws + p.lay.flags) + b);
+        T = __ldg(&p.temperature[b]);
+        if (!(T == 0.0f || T == 1.0f)) vflags = 0;  // left to the row sweep
+        if (vflags & kReqValid) {
+          x = __ldg(&p.tokens[(size_t)b * p.k + i]);
+          if (T != 0.0f) {
+            u = __ldg(&p.uniforms[(size_t)b * (p.k + 1) + i]);
+            zt_x = ElemTraits<TIn>::load(
+                static_cast<const TIn*>(p.target) + ((size_t)b * (p.k + 1) + i) * (size_t)p.V, x);
+            zd_x = ElemTraits<TIn>::load(
+                static_cast<const TIn*>(p.draft) + ((size_t)b * p.k + i) * (size_t)p.V, x);
+          }
+        }
+      }
       if (!mbar_wait_bounded(&sm.p1_done[slot], par, &sm.abort_flag)) {
         opd_abort(sm);
         return false;
@@ -483,24 +588,11 @@ __device__ void opd_bookkeeper(const OpdParams& p, OpdSmem& sm, int cid, int ncl
       }
       // Lane r holds rank r's part; every CTA combines them in rank order.
       opd_p1_unpack(other_rank ? sm.p1_peer[slot][lane] : mine, lane < (int)CS, t, d, g);
-      // Reference exponents: the largest fl(max log2 e) of each row; the
-      // parts' sums are brought to it and added in float-float.
-      const float rt = group_max(t.ms, 5), rd = group_max(d.ms, 5);
-      FF st = {0.0f, 0.0f}, sd = {0.0f, 0.0f};
-      if (lane < (int)CS) {
-        if (t.s != 0.0f) st = two_prod(t.s, ex2(__fsub_rn(t.ms, rt)));
-        if (d.s != 0.0f) sd = two_prod(d.s, ex2(__fsub_rn(d.ms, rd)));
-      }
-      st = warp_sum_ff(st);
-      sd = warp_sum_ff(sd);
       arg_warp_reduce(g);
+      FF l2t, l2d;
+      const bool valid = opd_pair_norms(t, d, lane < (int)CS, &l2t, &l2d);
       if (lane == 0) {
-        const float St = ff_to_float(st), Sd = ff_to_float(sd);
-        const bool valid = St > 0.0f && St <= FLT_MAX && Sd > 0.0f && Sd <= FLT_MAX;
-        // log2-domain normalisers L2 = ref + log2(S) in float-float; then
         // c = (L2_d - L2_t) ln 2, -L2_d and lse_d = L2_d ln 2.
-        const FF l2t = ff_add_f(two_sum(rt, log2f(st.hi)), __fdiv_rn(st.lo, st.hi) * kLog2e);
-        const FF l2d = ff_add_f(two_sum(rd, log2f(sd.hi)), __fdiv_rn(sd.lo, sd.hi) * kLog2e);
         sm.norms[slot] = make_float4(ff_to_float(ff_mul_f(ff_sub(l2d, l2t), kLn2f)),
                                      -ff_to_float(l2d), ff_to_float(ff_mul_f(l2d, kLn2f)),
                                      valid ? 1.0f : 0.0f);
@@ -511,6 +603,8 @@ __device__ void opd_bookkeeper(const OpdParams& p, OpdSmem& sm, int cid, int ncl
           zstar[slot] = ElemTraits<TIn>::load(drow, g.i);
         }
         mbar_arrive(&sm.norm_ready[slot]);
+        if (kVerify && rank == 0 && (vflags & kReqValid) && i < __ldg(&p.lengths[b]))
+          opd_decide<TIn>(p, b, i, x, T, u, zt_x, zd_x, g, l2t, l2d, valid);
       }
       __syncwarp();
       return true;
@@ -567,7 +661,9 @@ __device__ void opd_bookkeeper(const OpdParams& p, OpdSmem& sm, int cid, int ncl
   });
 }
 
-template <typename TIn>
+// kVerify: also decide the verified positions (spec_verify_opd); the
+// statistics-only instance compiles without any of that code.
+template <typename TIn, bool kVerify>
 __global__ void __launch_bounds__(kOpdThreads, kOpdMinBlocks) opd_kernel(OpdParams p) {
   extern __shared__ __align__(128) unsigned char opd_dyn[];
   OpdSmem& sm = *reinterpret_cast<OpdSmem*>(opd_dyn);
@@ -592,12 +688,25 @@ __global__ void __launch_bounds__(kOpdThreads, kOpdMinBlocks) opd_kernel(OpdPara
       "barrier.cluster.arrive.release.aligned;\n\t"
       "barrier.cluster.wait.acquire.aligned;" ::
           : "memory");
+  // Verification mode reads what the plan kernel wrote.
+  if (kVerify) pdl_wait();
   const int cid = blockIdx.x / CS, ncl = gridDim.x / CS;
   const int s0 = (int)rank * p.slice;
   const int warp = threadIdx.x >> 5;
   if (warp >= kOpdFirstConsumerWarp) opd_consumers<TIn>(p, sm, cid, ncl, s0);
   else if (warp == kOpdProducerWarp) opd_producer<TIn>(p, sm, cid, ncl, s0);
-  else opd_bookkeeper<TIn>(p, sm, cid, ncl, CS, rank);
+  else opd_bookkeeper<TIn, kVerify>(p, sm, cid, ncl, CS, rank);
+  // Verification mode: count the CTA out, as the row sweep does, so that the
+  // final pass can hold its completion until every CTA of this grid is done.
+  if constexpr (kVerify) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      WsHeader* h = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
+      if (*(volatile int*)&sm.abort_flag) record_status(h, SPEC_ERR_TIMEOUT);
+      __threadfence();
+      atomicAdd(&h->sweep_exited, 1);
+    }
+  }
 }
 // Per-request mixture loss, one warp per request, after the statistics.
 __global__ void opd_loss_kernel(const int32_t* lengths, const float* hard, const float* rkl_clip,

@@ -28,6 +28,8 @@ struct PlanParams {
   const int32_t* t_start;     // [B] packed layout: first target row of b (null: padded)
   const int32_t* d_start;     // [B] packed layout: first draft row of b
   long long rows_t, rows_d;   // packed layout: rows in the target / draft buffers
+  int skip_t01;               // leave requests at T = 0 or 1 out of the row list
+                              // (another kernel decides them: spec_verify_opd)
   int B, k, V, C, chunk_elems, nch;
   unsigned char* ws;
   WsLayout lay;
@@ -206,7 +208,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   for (int it = lo; it < hi; ++it) {
     const int i = it / p.B, b = it - i * p.B;
     const bool ok = !((bad_mask[b >> 5] >> (b & 31)) & 1u);
-    if (ok && i < __ldg(&p.lengths[b])) cnt += __ldg(&p.temperature[b]) == 0.0f ? 1 : 2;
+    const float T = __ldg(&p.temperature[b]);
+    if (ok && i < __ldg(&p.lengths[b]) && !(p.skip_t01 && (T == 0.0f || T == 1.0f)))
+      cnt += T == 0.0f ? 1 : 2;
   }
   int pos;
   const int total = block_exclusive_scan(cnt, &pos, warp_tot);
@@ -216,6 +220,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     const int L = __ldg(&p.lengths[b]);
     if (!ok || i >= L) continue;
     const float T = __ldg(&p.temperature[b]);
+    if (p.skip_t01 && (T == 0.0f || T == 1.0f)) continue;
     const float sc = T == 0.0f ? 0.0f : softmax_scale(T);
     const int slot = (b * p.k + i) << 1;
     const int trow = (p.t_start != nullptr ? __ldg(&p.t_start[b]) : b * (p.k + 1)) + i;

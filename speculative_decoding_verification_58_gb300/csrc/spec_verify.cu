@@ -211,6 +211,102 @@ class DeviceOf {
   bool switched_ = false;
 };
 
+// Launch the plan kernel (padded layout: t_start == nullptr).
+cudaError_t launch_plan(const int32_t* draft_tokens, const int32_t* lengths, const float* uniforms,
+                        const float* temperature, int B, int k, int V, int C, int ce, int nch,
+                        unsigned char* ws, const WsLayout& lay, cudaStream_t stream, bool pdl,
+                        const int32_t* t_start, const int32_t* d_start, long long rows_t,
+                        long long rows_d, bool skip_t01 = false) {
+  PlanParams pp;
+  pp.skip_t01 = skip_t01 ? 1 : 0;
+  pp.tokens = draft_tokens;
+  pp.lengths = lengths;
+  pp.uniforms = uniforms;
+  pp.temperature = temperature;
+  pp.t_start = t_start;
+  pp.d_start = d_start;
+  pp.rows_t = rows_t;
+  pp.rows_d = rows_d;
+  pp.B = B;
+  pp.k = k;
+  pp.V = V;
+  pp.C = C;
+  pp.chunk_elems = ce;
+  pp.nch = nch;
+  pp.ws = ws;
+  pp.lay = lay;
+  return launch(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, pdl, pp);
+}
+
+// Launch the final pass behind a grid of `decider_grid` CTAs that publish the
+// decisions (the row sweep, or the OPD kernel in verification mode).
+template <typename TIn>
+cudaError_t launch_final(const DeviceInfo* d, const void* target_logits, const void* draft_logits,
+                         const int32_t* draft_tokens, const int32_t* lengths, const float* uniforms,
+                         const float* temperature, int B, int k, int V, int32_t* out_tokens,
+                         int32_t* num_accepted, unsigned char* ws, const WsLayout& lay,
+                         int decider_grid, unsigned flags, cudaStream_t stream, bool pdl) {
+  FinalParams fp;
+  fp.target = target_logits;
+  fp.draft = draft_logits;
+  fp.tokens = draft_tokens;
+  fp.lengths = lengths;
+  fp.uniforms = uniforms;
+  fp.temperature = temperature;
+  fp.B = B;
+  fp.k = k;
+  fp.V = V;
+  fp.out_tokens = out_tokens;
+  fp.num_accepted = num_accepted;
+  fp.ws = ws;
+  fp.lay = lay;
+  fp.sweep_grid = decider_grid;
+  fp.test_late = (flags & SPEC_FLAG_TEST_LATE_SLICES) ? 1 : 0;
+  const int nseg = segments_of(V);
+  // Slices per request: one wave of three CTAs per SM over the batch, but at
+  // least two (a request's residual pair is 1.2 MB in fp32, too much for one
+  // CTA at the end of a round), each slice at least one segment.
+  int P = std::max(2, (3 * d->sms) / B);
+  if (P > kMaxSlices) P = kMaxSlices;
+  if (P > nseg) P = nseg;
+  if (P < 1) P = 1;
+  fp.P = P;
+  // Dynamic shared memory: the slice ring, later reused for the combine's
+  // segment records.
+  const size_t fsm = std::max((size_t)nseg * sizeof(float2), (size_t)kFinalStages * kFinalStageBytes);
+  return launch(final_kernel<TIn>, dim3((unsigned)(P * B)), dim3(kFinalThreads), fsm, stream, pdl,
+                fp);
+}
+
+// Launch the verification sweep (persistent, a multiple of the SM count);
+// *grid_out: its CTAs.
+template <typename TIn>
+cudaError_t launch_sweep(const DeviceInfo* d, const void* target_logits, const void* draft_logits,
+                         const int32_t* draft_tokens, const float* uniforms, int B, int k, int V,
+                         int nch, int ce, unsigned char* ws, const WsLayout& lay, bool early_exit,
+                         int dtype_index, cudaStream_t stream, bool pdl, int* grid_out) {
+  SweepParams sp;
+  sp.target = target_logits;
+  sp.draft = draft_logits;
+  sp.tokens = draft_tokens;
+  sp.uniforms = uniforms;
+  sp.B = B;
+  sp.k = k;
+  sp.V = V;
+  sp.nch = nch;
+  sp.chunk_elems = ce;
+  sp.early_exit = early_exit ? 1 : 0;
+  sp.ws = ws;
+  sp.lay = lay;
+  const long long max_units = 2LL * B * k * nch;
+  long long grid = (long long)d->sms * d->sweep_blocks_per_sm[dtype_index][1];
+  if (grid > max_units) grid = max_units;
+  if (grid < 1) grid = 1;
+  *grid_out = (int)grid;
+  return launch(sweep_kernel<TIn, true>, dim3((unsigned)grid), dim3(kSweepThreads),
+                sizeof(SweepSmem), stream, pdl, sp);
+}
+
 template <typename TIn>
 spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
                            const int32_t* draft_tokens, const int32_t* lengths,
@@ -228,83 +324,24 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
   const int nch = (V + ce - 1) / ce;
   const WsLayout lay = ws_layout(B, k, C, V);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-
-  PlanParams pp;
-  pp.tokens = draft_tokens;
-  pp.lengths = lengths;
-  pp.uniforms = uniforms;
-  pp.temperature = temperature;
-  pp.t_start = t_start;
-  pp.d_start = d_start;
-  pp.rows_t = rows_t;
-  pp.rows_d = rows_d;
-  pp.B = B;
-  pp.k = k;
-  pp.V = V;
-  pp.C = C;
-  pp.chunk_elems = ce;
-  pp.nch = nch;
-  pp.ws = ws;
-  pp.lay = lay;
   // With timing events between the kernels there is nothing to overlap.
   const bool pdl = (ev == nullptr);
   if (record(ev, 0, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (launch(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, pdl, pp) != cudaSuccess)
+  if (launch_plan(draft_tokens, lengths, uniforms, temperature, B, k, V, C, ce, nch, ws, lay,
+                  stream, pdl, t_start, d_start, rows_t, rows_d) != cudaSuccess)
     return SPEC_ERR_CUDA;
 
-  SweepParams sp;
-  sp.target = target_logits;
-  sp.draft = draft_logits;
-  sp.tokens = draft_tokens;
-  sp.uniforms = uniforms;
-  sp.B = B;
-  sp.k = k;
-  sp.V = V;
-  sp.nch = nch;
-  sp.chunk_elems = ce;
-  sp.early_exit = (flags & SPEC_FLAG_FULL_SWEEP) ? 0 : 1;
-  sp.ws = ws;
-  sp.lay = lay;
-  const long long max_units = slots * nch;
-  long long grid = (long long)d->sms * d->sweep_blocks_per_sm[dtype_index][1];
-  if (grid > max_units) grid = max_units;
-  if (grid < 1) grid = 1;
+  int grid = 0;
   if (record(ev, 1, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (launch(sweep_kernel<TIn, true>, dim3((unsigned)grid), dim3(kSweepThreads),
-             sizeof(SweepSmem), stream, pdl, sp) != cudaSuccess)
+  if (launch_sweep<TIn>(d, target_logits, draft_logits, draft_tokens, uniforms, B, k, V, nch, ce,
+                        ws, lay, (flags & SPEC_FLAG_FULL_SWEEP) == 0, dtype_index, stream, pdl,
+                        &grid) != cudaSuccess)
     return SPEC_ERR_CUDA;
 
-  FinalParams fp;
-  fp.target = target_logits;
-  fp.draft = draft_logits;
-  fp.tokens = draft_tokens;
-  fp.lengths = lengths;
-  fp.uniforms = uniforms;
-  fp.temperature = temperature;
-  fp.B = B;
-  fp.k = k;
-  fp.V = V;
-  fp.out_tokens = out_tokens;
-  fp.num_accepted = num_accepted;
-  fp.ws = ws;
-  fp.lay = lay;
-  fp.sweep_grid = (int)grid;
-  fp.test_late = (flags & SPEC_FLAG_TEST_LATE_SLICES) ? 1 : 0;
-  const int nseg = segments_of(V);
-  // Slices per request: one wave of three CTAs per SM over the batch, but at
-  // least two (a request's residual pair is 1.2 MB in fp32, too much for one
-  // CTA at the end of a round), each slice at least one segment.
-  int P = std::max(2, (3 * d->sms) / B);
-  if (P > kMaxSlices) P = kMaxSlices;
-  if (P > nseg) P = nseg;
-  if (P < 1) P = 1;
-  fp.P = P;
-  // Dynamic shared memory: the slice ring, later reused for the combine's
-  // segment records.
-  const size_t fsm = std::max((size_t)nseg * sizeof(float2), (size_t)kFinalStages * kFinalStageBytes);
   if (record(ev, 2, stream) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (launch(final_kernel<TIn>, dim3((unsigned)(P * B)), dim3(kFinalThreads), fsm, stream, pdl, fp) !=
-      cudaSuccess)
+  if (launch_final<TIn>(d, target_logits, draft_logits, draft_tokens, lengths, uniforms,
+                        temperature, B, k, V, out_tokens, num_accepted, ws, lay, grid, flags,
+                        stream, pdl) != cudaSuccess)
     return SPEC_ERR_CUDA;
   if (record(ev, 3, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
@@ -359,7 +396,11 @@ int opd_cluster_size(int V) { return V >= 65536 ? 4 : (V > 16384 ? 2 : 1); }
 
 template <typename TIn>
 cudaError_t opd_prepare() {
-  return cudaFuncSetAttribute(opd_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(opd_kernel<TIn, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sizeof(OpdSmem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(opd_kernel<TIn, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)sizeof(OpdSmem));
 }
 
@@ -376,14 +417,27 @@ cudaError_t opd_max_clusters(int cs, int* out) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(out, opd_kernel<TIn>, &cfg);
+  // Both instances have the same shape and launch bounds; the statistics
+  // instance stands for both.
+  return cudaOccupancyMaxActiveClusters(out, opd_kernel<TIn, false>, &cfg);
 }
+
+// Verification fields of an OPD launch (spec_verify_opd); null tokens means
+// statistics only (spec_opd_stats).
+struct OpdVerify {
+  const int32_t* tokens = nullptr;
+  const float* uniforms = nullptr;
+  const float* temperature = nullptr;
+  int32_t* out_tokens = nullptr;
+  int32_t* num_accepted = nullptr;
+  unsigned char* ws = nullptr;
+};
 
 template <typename TIn>
 spec_status_t opd_typed(const void* target, const void* draft, const int32_t* lengths, int B,
                         int k, int V, float delta, float alpha, int32_t* x_star, float* hard,
                         float* rkl, float* rkl_clip, float* loss, cudaStream_t stream,
-                        int dtype_index, bool vec_ok) {
+                        int dtype_index, bool vec_ok, const OpdVerify& vf = OpdVerify()) {
   DeviceInfo* d = nullptr;
   if (device_info(&d) != cudaSuccess) return SPEC_ERR_CUDA;
   const int cs = opd_cluster_size(V);
@@ -401,8 +455,9 @@ spec_status_t opd_typed(const void* target, const void* draft, const int32_t* le
       *slot = n;
     }
   }
+  const bool verify = vf.tokens != nullptr;
   const long long clusters = std::min<long long>((long long)B * k, *slot);
-  OpdParams op;
+  OpdParams op = {};
   op.target = target;
   op.draft = draft;
   op.lengths = lengths;
@@ -416,19 +471,54 @@ spec_status_t opd_typed(const void* target, const void* draft, const int32_t* le
   op.hard = hard;
   op.rkl = rkl;
   op.rkl_clip = rkl_clip;
+  int C = 0, ce = 0, nch = 0;
+  WsLayout lay = {};
+  if (verify) {
+    // The plan kernel checks the inputs and resets the workspace state the
+    // decisions and the final pass use (its row list is not needed here).
+    C = chunks_per_row(2LL * B * k, V);
+    ce = chunk_elems_for(V, C);
+    nch = (V + ce - 1) / ce;
+    lay = ws_layout(B, k, C, V);
+    if (launch_plan(vf.tokens, lengths, vf.uniforms, vf.temperature, B, k, V, C, ce, nch, vf.ws,
+                    lay, stream, true, nullptr, nullptr, 0, 0, /*skip_t01=*/true) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    op.verify = 1;
+    op.tokens = vf.tokens;
+    op.uniforms = vf.uniforms;
+    op.temperature = vf.temperature;
+    op.ws = vf.ws;
+    op.lay = lay;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(clusters * cs));
   cfg.blockDim = dim3(kOpdThreads);
   cfg.dynamicSmemBytes = sizeof(OpdSmem);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, opd_kernel<TIn>, op) != cudaSuccess) return SPEC_ERR_CUDA;
+  cfg.numAttrs = verify ? 2 : 1;
+  if ((verify ? cudaLaunchKernelEx(&cfg, opd_kernel<TIn, true>, op)
+              : cudaLaunchKernelEx(&cfg, opd_kernel<TIn, false>, op)) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (verify) {
+    // Requests at other temperatures: the row sweep, over the rows the plan
+    // listed (none when every request is at T = 0 or 1).
+    int sweep_grid = 0;
+    if (launch_sweep<TIn>(d, target, draft, vf.tokens, vf.uniforms, B, k, V, nch, ce, vf.ws, lay,
+                          true, dtype_index, stream, true, &sweep_grid) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    if (launch_final<TIn>(d, target, draft, vf.tokens, lengths, vf.uniforms, vf.temperature, B, k,
+                          V, vf.out_tokens, vf.num_accepted, vf.ws, lay,
+                          (int)(clusters * cs) + sweep_grid, 0u, stream, true) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+  }
   const int wpb = 8;
   if (launch(opd_loss_kernel, dim3((B + wpb - 1) / wpb), dim3(wpb * 32), 0, stream, true, lengths,
              (const float*)hard, (const float*)rkl_clip, B, k, alpha, loss) != cudaSuccess)
@@ -616,6 +706,49 @@ spec_status_t spec_opd_stats(const void* target_logits, const void* draft_logits
                             hard, rkl, rkl_clip, loss, s, 0, vec_ok);
   return opd_typed<uint16_t>(target_logits, draft_logits, lengths, B, k, V, delta, alpha, x_star,
                              hard, rkl, rkl_clip, loss, s, 1, vec_ok);
+}
+
+spec_status_t spec_verify_opd(const void* target_logits, const void* draft_logits,
+                              spec_dtype_t dtype, const int32_t* draft_tokens,
+                              const int32_t* lengths, const float* uniforms,
+                              const float* temperature, int B, int k, int V, float delta,
+                              float alpha, int32_t* out_tokens, int32_t* num_accepted,
+                              int32_t* x_star, float* hard, float* rkl, float* rkl_clip,
+                              float* loss, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 1 || k < 1 || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (!sizes_ok(B, k, V)) return SPEC_ERR_UNSUPPORTED;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (!(delta > 0.0f && delta <= FLT_MAX) || !(alpha >= 0.0f && alpha <= 1.0f))
+    return SPEC_ERR_INVALID_ARG;
+  if (!target_logits || !draft_logits || !draft_tokens || !lengths || !uniforms || !temperature ||
+      !out_tokens || !num_accepted || !x_star || !hard || !rkl || !rkl_clip || !loss)
+    return SPEC_ERR_INVALID_ARG;
+  const size_t esize = dtype == SPEC_F32 ? 4 : 2;
+  if (!aligned(target_logits, esize) || !aligned(draft_logits, esize) || !aligned(draft_tokens, 4) ||
+      !aligned(lengths, 4) || !aligned(uniforms, 4) || !aligned(temperature, 4) ||
+      !aligned(out_tokens, 4) || !aligned(num_accepted, 4) || !aligned(x_star, 4) ||
+      !aligned(hard, 4) || !aligned(rkl, 4) || !aligned(rkl_clip, 4) || !aligned(loss, 4))
+    return SPEC_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256) ||
+      workspace_bytes < spec_verify_workspace_bytes(B, k, V))
+    return SPEC_ERR_WORKSPACE;
+  const bool vec_ok = aligned(target_logits, 16) && aligned(draft_logits, 16) &&
+                      ((size_t)V * esize) % 16 == 0;
+  DeviceOf on_device(target_logits);
+  if (!on_device.ok()) return SPEC_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  OpdVerify vf;
+  vf.tokens = draft_tokens;
+  vf.uniforms = uniforms;
+  vf.temperature = temperature;
+  vf.out_tokens = out_tokens;
+  vf.num_accepted = num_accepted;
+  vf.ws = static_cast<unsigned char*>(workspace);
+  if (dtype == SPEC_F32)
+    return opd_typed<float>(target_logits, draft_logits, lengths, B, k, V, delta, alpha, x_star,
+                            hard, rkl, rkl_clip, loss, s, 0, vec_ok, vf);
+  return opd_typed<uint16_t>(target_logits, draft_logits, lengths, B, k, V, delta, alpha, x_star,
+                             hard, rkl, rkl_clip, loss, s, 1, vec_ok, vf);
 }
 
 spec_status_t spec_d3d_select(const int32_t* num_accepted, const int32_t* out_tokens,

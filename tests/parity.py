@@ -79,3 +79,23 @@ def oracle_verify_threads(inp, threads: int = 16) -> oracle.OracleResult:
     return oracle.OracleResult(cat("out_tokens"), cat("num_accepted"), cat("margin"),
                                cat("final_mass"), cat("residual_zero"),
                                sum(p.bad_requests for p in parts))
+
+
+def oracle_opd_threads(inp, delta=0.01, alpha=0.8, threads: int = 16) -> oracle.OpdResult:
+    """``oracle.opd_stats`` on a batch split over host threads, concatenated in
+    request order.  Same results as one call."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+    B = inp.B
+    n = max(1, min(threads, os.cpu_count() or 1, B))
+    edges = [B * j // n for j in range(n + 1)]
+
+    def part(j):
+        s = slice(edges[j], edges[j + 1])
+        return oracle.opd_stats(inp.target[s], inp.draft[s], inp.lengths[s], delta=delta,
+                                alpha=alpha)
+    with ThreadPoolExecutor(n) as pool:
+        parts = list(pool.map(part, range(n)))
+    cat = lambda f: np.concatenate([getattr(p, f) for p in parts])
+    return oracle.OpdResult(cat("x_star"), cat("hard"), cat("rkl"), cat("rkl_clip"), cat("loss"),
+                            sum(p.bad_requests for p in parts))

@@ -24,6 +24,7 @@ torch = pytest.importorskip("torch")
 import oracle
 import speculative_decoding_verification_58_gb300 as sv
 from speculative_decoding_verification_58_gb300 import synth
+from parity import compare, oracle_opd_threads
 
 pytestmark = pytest.mark.gpu
 
@@ -92,22 +93,87 @@ def test_opd_worked_example_of_the_notes():
     assert abs(r["rkl"][0, 0] - g["printed"]["rkl"]) < tol
 
 
-def test_opd_headline_workload_sampled_requests():
-    """B=128, k=16, V=151936 bf16 as the benchmark runs it; the oracle checks 12 requests."""
+def _opd_close(g, o, label, rows=slice(None)):
+    np.testing.assert_array_equal(g["x_star"][rows], o.x_star, err_msg=label)
+    for name in ("hard", "rkl", "rkl_clip"):
+        np.testing.assert_allclose(g[name][rows], getattr(o, name), rtol=RTOL, atol=ATOL,
+                                   equal_nan=True, err_msg=f"{label}: {name}")
+    np.testing.assert_allclose(g["loss"][rows], o.loss, rtol=RTOL, atol=ATOL, equal_nan=True,
+                               err_msg=f"{label}: loss")
+
+
+def test_opd_headline_workload_every_request():
+    """B=128, k=16, V=151936 bf16 as the benchmark runs it; all 128 requests
+    against the oracle (over host threads)."""
     inp = synth.make_workload(synth.HEADLINE)
     g = run(inp)
-    pick = np.random.default_rng(3).choice(inp.B, 12, replace=False)
-    o = oracle.opd_stats(inp.target[pick], inp.draft[pick], inp.lengths[pick])
-    np.testing.assert_array_equal(g["x_star"][pick], o.x_star)
-    for name in ("hard", "rkl", "rkl_clip"):
-        np.testing.assert_allclose(g[name][pick], getattr(o, name), rtol=RTOL, atol=ATOL,
-                                   equal_nan=True, err_msg=name)
-    np.testing.assert_allclose(g["loss"][pick], o.loss, rtol=RTOL, atol=ATOL)
+    _opd_close(g, oracle_opd_threads(inp), "headline")
     # Every position past L_b is -1 / NaN; every verified one is finite.
     for b in range(inp.B):
         L = inp.lengths[b]
         assert np.all(g["x_star"][b, L:] == -1) and np.all(np.isnan(g["rkl"][b, L:]))
         assert np.all(np.isfinite(g["rkl_clip"][b, :L])) and np.all(g["rkl"][b, :L] >= -ATOL)
+
+
+# ---------------------------------------------------------------------------
+# Verification and statistics in one pass (spec_verify_opd)
+# ---------------------------------------------------------------------------
+
+def run_fused(inp, delta=0.01, alpha=0.8):
+    d = sv.to_device(inp)
+    ws = sv.alloc_workspace(inp.B, inp.k, inp.V)
+    out, n, st = sv.spec_verify_opd(**d, delta=delta, alpha=alpha, workspace=ws)
+    rep = sv.spec_verify_report(ws)
+    g = {k: getattr(st, k).cpu().numpy() for k in ("x_star", "hard", "rkl", "rkl_clip", "loss")}
+    return out.cpu().numpy(), n.cpu().numpy(), g, rep
+
+
+def check_fused(inp, label, delta=0.01, alpha=0.8):
+    out, n, g, rep = run_fused(inp, delta, alpha)
+    o = oracle.verify(inp.target, inp.draft, inp.tokens, inp.lengths, inp.uniforms,
+                      inp.temperature)
+    info = compare(out, n, o, inp.temperature, label)
+    _opd_close(g, oracle.opd_stats(inp.target, inp.draft, inp.lengths, delta=delta, alpha=alpha),
+               label)
+    return info, rep
+
+
+@pytest.mark.parametrize("recipe,B,k,V,dtype", [
+    ("gauss", 1, 4, 1024, "f32"),
+    ("zipf_mixed_noise", 24, 16, 5000, "bf16"),     # T = 1: one set of normalisers
+    ("zipf_mixed_temp", 40, 8, 6000, "bf16"),       # greedy and T != 1: second sums
+    ("zipf_adaptive", 16, 16, 70001, "f32"),        # clusters of 4, rows not aligned
+    ("zipf_mixed_temp", 12, 5, 151936, "bf16"),     # the pages' vocabulary
+    ("gauss", 3, 2, 7, "f32"),
+])
+def test_fused_verification_and_statistics_match_oracle(recipe, B, k, V, dtype):
+    inp = synth.make_inputs(recipe, B, k, V, dtype, seed=80 + B + V)
+    info, rep = check_fused(inp, f"fused {recipe} B={B} k={k} V={V} {dtype}")
+    assert rep.status == sv.SPEC_OK, rep
+
+
+def test_fused_headline_workload_every_request():
+    inp = synth.make_workload(synth.HEADLINE)
+    out, n, g, rep = run_fused(inp)
+    o = oracle.verify(inp.target, inp.draft, inp.tokens, inp.lengths, inp.uniforms,
+                      inp.temperature)
+    compare(out, n, o, inp.temperature, "fused headline")
+    _opd_close(g, oracle_opd_threads(inp), "fused headline")
+    assert rep.status == sv.SPEC_OK, rep
+
+
+def test_fused_invalid_request_keeps_its_statistics():
+    """A token out of range invalidates the verification of its request (-1),
+    while its statistics, which do not use tokens, are still computed."""
+    inp = synth.make_inputs("zipf_mixed_noise", 6, 4, 900, "bf16", seed=85)
+    inp.tokens[2, 0] = 900
+    out, n, g, rep = run_fused(inp)
+    o = oracle.verify(inp.target, inp.draft, inp.tokens, inp.lengths, inp.uniforms,
+                      inp.temperature)
+    assert n[2] == -1 and np.all(out[2] == -1) and o.num_accepted[2] == -1
+    compare(out, n, o, inp.temperature, "fused, one invalid request")
+    _opd_close(g, oracle.opd_stats(inp.target, inp.draft, inp.lengths), "fused, invalid request")
+    assert rep.status == sv.SPEC_ERR_BAD_INPUT and rep.bad_requests == 1
 
 
 def test_opd_special_cases():
