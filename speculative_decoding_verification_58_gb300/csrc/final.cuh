@@ -58,7 +58,7 @@ struct FinalShared {
   int32_t tok[32];                // draft tokens x_0 .. x_{k-1}
   FF cand_excl;
   float REF, mu;
-  int job, n, cand, token, last, late, any_late;
+  int job, n, cand, token, last, late, any_late, bad_in;
 };
 
 // A slice CTA that gave up (its wait for the request's outcome, or for its
@@ -761,6 +761,16 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
   if (threadIdx.x < 32) {
     const int t = threadIdx.x;
     const uint32_t lmask = (L >= 32) ? 0xffffffffu : ((1u << L) - 1u);
+    // The per-position inputs the plan does not check (lane t: position t):
+    // tokens x_t in [0, V) for t < L and, when sampling, uniforms u_t in
+    // [0, 1) for t <= L.  Any one out of range makes the request invalid.
+    const int x_t = t < p.k ? __ldg(&p.tokens[(size_t)b * p.k + t]) : 0;
+    const float u_t = (T != 0.0f && t <= L && t <= p.k)
+                          ? __ldg(&p.uniforms[(size_t)b * (p.k + 1) + t])
+                          : 0.0f;
+    const bool in_ok = (t >= L || (x_t >= 0 && x_t < p.V)) &&
+                       (T == 0.0f || t > L || (u_t >= 0.0f && u_t < 1.0f));  // NaN fails
+    const bool inputs_ok = __all_sync(0xffffffffu, in_ok);
     int f = 0;
     uint32_t dec = 0, acc = 0, bad = 0;
     bool late = false;
@@ -771,6 +781,7 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
     const unsigned long long t0 = global_ns();
     for (;;) {
       f = __ldcg(reinterpret_cast<const int32_t*>(p.ws + p.lay.flags) + b);
+      if (!inputs_ok) break;  // invalid: no outcome to wait for
       const unsigned long long st =
           ld_acquire_u64(reinterpret_cast<const unsigned long long*>(p.ws + p.lay.state) + b);
       dec = (uint32_t)st;
@@ -790,13 +801,17 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
     const float4* pos_c = reinterpret_cast<const float4*>(p.ws + p.lay.pos_c);
     const int32_t* pos_arg = reinterpret_cast<const int32_t*>(p.ws + p.lay.pos_arg);
     float4 c4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    int g = -1, x = -1;
+    int g = -1;
     if (t < p.k) {
       const size_t bi = (size_t)b * p.k + t;
       c4 = __ldcg(&pos_c[bi]);
       g = __ldcg(&pos_arg[bi]);
-      x = __ldg(&p.tokens[bi]);
     }
+    const int x = t < p.k ? x_t : -1;
+    // A request the plan admitted whose tokens or uniforms are out of range:
+    // recorded once, by the slice that writes its outputs.
+    const bool bad_in = (f & kReqValid) && !inputs_ok;
+    if (bad_in) f = 0;
     if (late) {
       if (t == 0) record_status(h, SPEC_ERR_TIMEOUT);
       f = 0;  // no outcome: the request reports -1
@@ -836,6 +851,7 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
       sh.n = n;
       sh.token = token;
       sh.late = late ? 1 : 0;
+      sh.bad_in = bad_in ? 1 : 0;
     }
   }
   __syncthreads();
@@ -924,6 +940,11 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
     return;
   }
   if (!rows_job) {
+    if (sh.bad_in && threadIdx.x == 0) {
+      atomicAdd(&h->bad_requests, 1);
+      atomicMin(&h->first_bad, b);
+      record_status(h, SPEC_ERR_BAD_INPUT);
+    }
     write_outputs(job == kJobInvalid, token);
     return;
   }

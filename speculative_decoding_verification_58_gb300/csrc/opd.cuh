@@ -551,6 +551,9 @@ __device__ void opd_bookkeeper(const OpdParams& p, OpdSmem& sm, int cid, int ncl
         if (!(T == 0.0f || T == 1.0f)) vflags = 0;  // left to the row sweep
         if (vflags & kReqValid) {
           x = __ldg(&p.tokens[(size_t)b * p.k + i]);
+          // A token out of range (the final pass turns its request into -1)
+          // reads element 0 instead.
+          if ((unsigned)x >= (unsigned)p.V) x = 0;
           if (T != 0.0f) {
             u = __ldg(&p.uniforms[(size_t)b * (p.k + 1) + i]);
             zt_x = ElemTraits<TIn>::load(

@@ -3,10 +3,10 @@
 // reads, position-major (all requests' position 0, then position 1, ...), so
 // that a rejection found at an early position can spare the rows behind it.
 //
-// One CTA, two flat-parallel passes: (1) every (request, position) item is
-// checked with independent loads, invalid requests land in a shared bitmask;
-// (2) every (position, request) item is counted, its request's state reset,
-// and one block-wide scan places the row descriptors.
+// One CTA, two flat-parallel passes: (1) every request's scalars are
+// checked (invalid requests land in a shared bitmask) and its state reset;
+// (2) every (position, request) item is counted and one block-wide scan
+// places the row descriptors.
 //
 // Row addressing: request b's target rows are rows t0_b + 0..L_b of the
 // target buffer and its draft rows d0_b + 0..L_b-1 of the draft buffer.  The
@@ -132,72 +132,33 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
            ((unsigned long long)__float_as_uint(1.0f) << 32) | __float_as_uint(0.0f));
   __syncthreads();
 
-  // Pass 1, item j = b*(k+1) + i: the request's scalars (at i = 0: 1 <= L <= k
-  // from the length head's clamp, T is 0 or a finite normal float, packed
-  // rows inside their buffers), token x_i in [0, V) for i < L, uniform u_i
-  // in [0, 1) for i <= L when T > 0.  Four items per thread per round, all
-  // loads issued before any is used.
-  const int k1 = p.k + 1;
-  const int items1 = p.B * k1;
-  constexpr int kR = 4;
-  for (int base = 0; base < items1; base += kR * kPlanThreads) {
-    int L[kR], x[kR], t0[kR], d0[kR];
-    float T[kR], u[kR];
-#pragma unroll
-    for (int q = 0; q < kR; ++q) {
-      const int j = base + q * kPlanThreads + tid;
-      L[q] = 0;
-      x[q] = 0;
-      T[q] = 0.0f;
-      u[q] = 0.0f;
-      t0[q] = 0;
-      d0[q] = 0;
-      if (j < items1) {
-        const int b = j / k1;
-        const int i = j - b * k1;
-        L[q] = __ldg(&p.lengths[b]);
-        T[q] = __ldg(&p.temperature[b]);
-        if (i < p.k) x[q] = __ldg(&p.tokens[(size_t)b * p.k + i]);
-        u[q] = __ldg(&p.uniforms[j]);
-        if (i == 0 && p.t_start != nullptr) {
-          t0[q] = __ldg(&p.t_start[b]);
-          d0[q] = __ldg(&p.d_start[b]);
-        }
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < kR; ++q) {
-      const int j = base + q * kPlanThreads + tid;
-      if (j >= items1) break;
-      const int b = j / k1;
-      const int i = j - b * k1;
-      bool bad = (i == 0) && !(L[q] >= 1 && L[q] <= p.k && temperature_ok(T[q]));
-      // Packed rows: target rows t0 .. t0+L exist, and draft rows d0 .. d0+L-1
-      // unless the request is greedy (its draft rows are never read).
-      bad = bad || (i == 0 && p.t_start != nullptr &&
-                    !(t0[q] >= 0 && (long long)t0[q] + L[q] + 1 <= p.rows_t &&
-                      (T[q] == 0.0f || (d0[q] >= 0 && (long long)d0[q] + L[q] <= p.rows_d))));
-      bad = bad || (i < L[q] && i < p.k && (x[q] < 0 || x[q] >= p.V));
-      bad = bad || (T[q] > 0.0f && i <= L[q] && !(u[q] >= 0.0f && u[q] < 1.0f));  // NaN fails
-      if (bad) atomicOr(&bad_mask[b >> 5], 1u << (b & 31));
-    }
-  }
-  __syncthreads();
-
-  // Request-level state.
+  // Requests: the scalars the row list depends on (1 <= L <= k from the
+  // length head's clamp, T is 0 or a finite normal float, packed rows inside
+  // their buffers), request state, first rows.  The per-position inputs
+  // (tokens in [0, V), uniforms in [0, 1)) are checked by the final pass,
+  // which loads them anyway; until then every use guards its index.
   for (int b = tid; b < p.B; b += kPlanThreads) {
-    const bool ok = !((bad_mask[b >> 5] >> (b & 31)) & 1u);
-    const bool greedy = __ldg(&p.temperature[b]) == 0.0f;
-    flags[b] = ok ? (kReqValid | (greedy ? kReqGreedy : 0)) : 0;
+    const int L = __ldg(&p.lengths[b]);
+    const float T = __ldg(&p.temperature[b]);
+    const int2 rb = p.t_start != nullptr ? make_int2(__ldg(&p.t_start[b]), __ldg(&p.d_start[b]))
+                                         : make_int2(b * (p.k + 1), b * p.k);
+    bool bad = !(L >= 1 && L <= p.k && temperature_ok(T));
+    // Packed rows: target rows t0 .. t0+L exist, and draft rows d0 .. d0+L-1
+    // unless the request is greedy (its draft rows are never read).
+    bad = bad || (p.t_start != nullptr &&
+                  !(rb.x >= 0 && (long long)rb.x + L + 1 <= p.rows_t &&
+                    (T == 0.0f || (rb.y >= 0 && (long long)rb.y + L <= p.rows_d))));
+    if (bad) atomicOr(&bad_mask[b >> 5], 1u << (b & 31));
+    flags[b] = bad ? 0 : (kReqValid | (T == 0.0f ? kReqGreedy : 0));
     first_reject[b] = p.k;
-    rowbase[b] = p.t_start != nullptr ? make_int2(__ldg(&p.t_start[b]), __ldg(&p.d_start[b]))
-                                      : make_int2(b * (p.k + 1), b * p.k);
-    if (!ok) {
+    rowbase[b] = rb;
+    if (bad) {
       atomicAdd(&h->bad_requests, 1);
       atomicMin(&h->first_bad, b);
       atomicCAS(&h->status, SPEC_OK, SPEC_ERR_BAD_INPUT);
     }
   }
+  __syncthreads();
 
   // Pass 2, item it = i*B + b: the rows of (b, i) in position-major order;
   // one block-wide scan places their descriptors.

@@ -5,6 +5,7 @@
 // predecessor's results with griddepcontrol.wait before reading them.
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <mutex>
@@ -17,6 +18,17 @@
 #include "sweep.cuh"
 
 namespace specv {
+
+// A named NVTX range for the lifetime of the object (host side: what an
+// entry point enqueues, and each launch within it, shows as a labelled range
+// in a timeline profiler; without one attached it costs a pointer check).
+class NvtxRange {
+ public:
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // ---------------------------------------------------------------------------
 // Row-statistics kernels (spec_row_stats).
@@ -217,6 +229,7 @@ cudaError_t launch_plan(const int32_t* draft_tokens, const int32_t* lengths, con
                         unsigned char* ws, const WsLayout& lay, cudaStream_t stream, bool pdl,
                         const int32_t* t_start, const int32_t* d_start, long long rows_t,
                         long long rows_d, bool skip_t01 = false) {
+  NvtxRange r("plan_kernel");
   PlanParams pp;
   pp.skip_t01 = skip_t01 ? 1 : 0;
   pp.tokens = draft_tokens;
@@ -246,6 +259,7 @@ cudaError_t launch_final(const DeviceInfo* d, const void* target_logits, const v
                          const float* temperature, int B, int k, int V, int32_t* out_tokens,
                          int32_t* num_accepted, unsigned char* ws, const WsLayout& lay,
                          int decider_grid, unsigned flags, cudaStream_t stream, bool pdl) {
+  NvtxRange r("final_kernel");
   FinalParams fp;
   fp.target = target_logits;
   fp.draft = draft_logits;
@@ -285,6 +299,7 @@ cudaError_t launch_sweep(const DeviceInfo* d, const void* target_logits, const v
                          const int32_t* draft_tokens, const float* uniforms, int B, int k, int V,
                          int nch, int ce, unsigned char* ws, const WsLayout& lay, bool early_exit,
                          int dtype_index, cudaStream_t stream, bool pdl, int* grid_out) {
+  NvtxRange r("sweep_kernel");
   SweepParams sp;
   sp.target = target_logits;
   sp.draft = draft_logits;
@@ -316,6 +331,7 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
                            void* const* ev, const int32_t* t_start = nullptr,
                            const int32_t* d_start = nullptr, long long rows_t = 0,
                            long long rows_d = 0) {
+  NvtxRange r(t_start != nullptr ? "spec_verify_packed" : "spec_verify");
   DeviceInfo* d = nullptr;
   if (device_info(&d) != cudaSuccess) return SPEC_ERR_CUDA;
   const long long slots = 2LL * B * k;
@@ -438,6 +454,7 @@ spec_status_t opd_typed(const void* target, const void* draft, const int32_t* le
                         int k, int V, float delta, float alpha, int32_t* x_star, float* hard,
                         float* rkl, float* rkl_clip, float* loss, cudaStream_t stream,
                         int dtype_index, bool vec_ok, const OpdVerify& vf = OpdVerify()) {
+  NvtxRange r(vf.tokens != nullptr ? "spec_verify_opd" : "spec_opd_stats");
   DeviceInfo* d = nullptr;
   if (device_info(&d) != cudaSuccess) return SPEC_ERR_CUDA;
   const int cs = opd_cluster_size(V);
@@ -504,9 +521,12 @@ spec_status_t opd_typed(const void* target, const void* draft, const int32_t* le
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = verify ? 2 : 1;
-  if ((verify ? cudaLaunchKernelEx(&cfg, opd_kernel<TIn, true>, op)
-              : cudaLaunchKernelEx(&cfg, opd_kernel<TIn, false>, op)) != cudaSuccess)
-    return SPEC_ERR_CUDA;
+  {
+    NvtxRange ro("opd_kernel");
+    if ((verify ? cudaLaunchKernelEx(&cfg, opd_kernel<TIn, true>, op)
+                : cudaLaunchKernelEx(&cfg, opd_kernel<TIn, false>, op)) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+  }
   if (verify) {
     // Requests at other temperatures: the row sweep, over the rows the plan
     // listed (none when every request is at T = 0 or 1).

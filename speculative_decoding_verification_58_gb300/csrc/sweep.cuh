@@ -468,12 +468,15 @@ __device__ __noinline__ void decide_position(const SweepParams& p, int bi, bool 
                           : static_cast<const TIn*>(p.target) + ((size_t)rb.x + i) * (size_t)p.V;
     const TIn* drow = dry ? reinterpret_cast<const TIn*>(p.ws + p.lay.warm)
                           : static_cast<const TIn*>(p.draft) + ((size_t)rb.y + i) * (size_t)p.V;
-    const float zt = ElemTraits<TIn>::load(trow, x);
-    const float zd = ElemTraits<TIn>::load(drow, x);
+    // A token out of range (the final pass turns its request into -1) reads
+    // element 0 instead and counts as a row without mass.
+    const bool x_ok = (unsigned)x < (unsigned)p.V;
+    const float zt = ElemTraits<TIn>::load(trow, x_ok ? x : 0);
+    const float zd = ElemTraits<TIn>::load(drow, x_ok ? x : 0);
     FF ct, cd;
     bool okt, okd;
     pair_log2_normalisers(pt, p.nch, sc, &ct, &cd, &okt, &okd, &late);
-    row_ok = okt && okd;
+    row_ok = okt && okd && x_ok;
     // A token the target gives probability zero is never accepted; a token
     // the drafter gives probability zero (and the target not) always is.
     // Otherwise d = log2 p(x) - log2 q(x) = (zt*sc - ct) - (zd*sc - cd) in

@@ -42,7 +42,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc(), "-gencode", GENCODE, "-O3", "-lineinfo", "-std=c++17",
            "-Xcompiler", "-fPIC", "-shared", "-I", INCLUDE,
-           *SOURCES, "-o", tmp]
+           *SOURCES, "-o", tmp, "-ldl"]
     if verbose_ptxas:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.run(cmd, check=True)
