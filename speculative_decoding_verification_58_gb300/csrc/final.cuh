@@ -50,16 +50,32 @@ constexpr int kJobNone = 0, kJobResidual = 1, kJobBonus = 2, kJobGreedyRowL = 3,
               kJobTargetOnly = 5;
 
 struct FinalShared {
-  FF warp_ff[kFinalWarps + 1];
+  long long dwarp[kFinalWarps];   // a slice's share of D, per warp (fixed point)
   float warp_f[kFinalWarps];
   int warp_i[kFinalWarps];
   float4 pos_c[32];               // float-float log2 normalisers (target, draft) per position (k <= 31)
   int32_t pos_arg[32];
   int32_t tok[32];                // draft tokens x_0 .. x_{k-1}
-  FF cand_excl;
-  float REF, mu;
-  int job, n, cand, token, last, late, any_late, bad_in;
+  long long dsx[2];               // combine: D shares summed per warp (fixed point)
+  long long wsum[kFinalWarps];    // combine: per warp, its sum of weights (fixed point),
+  long long wexcl[kFinalWarps];   //          its last candidate segment's prefix
+  int wcand[kFinalWarps];         //          and that segment (-1: none)
+  float warp_w[kFinalWarps];      //          and its largest weight bound
+  float uL;
+  int job, n, token, last, late, any_late, bad_in, warm;
 };
+
+// Is a request's outcome known from its decision word?  n = the first
+// rejected position among the L verified ones (or L); known when every
+// position before n is decided (and so accepted).
+__device__ __forceinline__ bool outcome_known_word(unsigned long long st, int L) {
+  const uint32_t dec = (uint32_t)st, acc = (uint32_t)(st >> 32);
+  const uint32_t lmask = (L >= 32) ? 0xffffffffu : ((1u << L) - 1u);
+  const uint32_t rej = dec & ~acc & lmask;
+  const int n = rej ? (__ffs((int)rej) - 1) : L;
+  const uint32_t pre = (n >= 32) ? 0xffffffffu : ((1u << n) - 1u);
+  return (dec & acc & pre) == pre;
+}
 
 // A slice CTA that gave up (its wait for the request's outcome, or for its
 // own copies, ran out) still counts itself in final_done, with this mark
@@ -341,6 +357,36 @@ __device__ __forceinline__ float seg_weight(float2 r, bool bonus, float sc, floa
   return __fmul_rn(r.y, exp2_diff(__fmul_rn(r.x, sc), REF));
 }
 
+// Fixed-point sums.  The combine adds weights as 64-bit integers, each
+// weight scaled by a power of two chosen from the largest one: integer sums
+// are exact and independent of their order, so a prefix sum costs one
+// integer add per step instead of a float-float addition, and the chain of
+// dependent steps after the last slice arrives stays short.  Quantising a
+// weight to 2^-50 of the largest changes the CDF by less than 2^-37 of its
+// total even over 2^13 segments.  The slices' shares of D are summed the
+// same way, on a fixed scale of 2^58 (|D| <= 2).
+constexpr float kDScale = 288230376151711744.0f;       // 2^58
+constexpr float kDUnscale = 3.4694469519536142e-18f;   // 2^-58
+
+// 2^e as a float (e in [-126, 127]).
+__device__ __forceinline__ float exp2_int(int e) { return __int_as_float((e + 127) << 23); }
+
+__device__ __forceinline__ long long warp_sum_i64(long long x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+__device__ __forceinline__ long long warp_incl_scan_i64(long long x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  return x;
+}
+
 // ---------------------------------------------------------------------------
 // Slice passes.  Warp w takes segments s_lo + w, s_lo + w + 8, ... in
 // batches of U; the next batch is loaded before the current one is
@@ -356,7 +402,8 @@ __host__ __device__ constexpr int slice_batch() {
 // thread's share of D in float-float.
 template <typename TIn>
 __device__ void slice_records(const TIn* rt, const TIn* rd, int V, const MassSpec& ms, bool bonus,
-                              int s_lo, int s_hi, float2* rec, bool vec_ok, FF* dsum) {
+                              int s_lo, int s_hi, float2* rec, bool vec_ok,
+                              long long* dsum) {
   constexpr int U = slice_batch<TIn>();
   constexpr int STEP = kFinalWarps * U;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -379,7 +426,7 @@ __device__ void slice_records(const TIn* rt, const TIn* rd, int V, const MassSpe
       if (seg >= s_hi) break;
       float dl = 0.0f;
       const float2 out = seg_record(t[q], d[q], ms, bonus, &dl);
-      *dsum = ff_add_f(*dsum, dl);
+      *dsum += __float2ll_rn(__fmul_rn(dl, kDScale));
       if (lane == 0) __stcg(&rec[seg], out);
     }
   };
@@ -419,7 +466,7 @@ struct FinalRing {
 template <typename TIn>
 __device__ bool slice_records_staged(const TIn* rt, const TIn* rd, int V, const MassSpec& ms,
                                      bool bonus, int s_lo, int s_hi, float2* rec,
-                                     unsigned char* ring, FinalRing& fr, FF* dsum) {
+                                     unsigned char* ring, FinalRing& fr, long long* dsum) {
   constexpr int SB = kSegElems * (int)sizeof(TIn);  // bytes of one segment of one row
   constexpr int NV = SB / 512;                      // 16-byte vectors per lane per segment
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -497,7 +544,7 @@ __device__ bool slice_records_staged(const TIn* rt, const TIn* rd, int V, const 
         }
         float dl = 0.0f;
         const float2 out = seg_record(t, d, ms, bonus, &dl);
-        *dsum = ff_add_f(*dsum, dl);
+        *dsum += __float2ll_rn(__fmul_rn(dl, kDScale));
         if (lane == 0) __stcg(&rec[seg], out);
       }
     }
@@ -575,158 +622,200 @@ __device__ ArgAcc slice_argmax(const TIn* row, int V, int s_lo, int s_hi, bool v
   return r;
 }
 
-__device__ __forceinline__ FF ff_shfl_up(FF a, int off) {
-  return {__shfl_up_sync(0xffffffffu, a.hi, off), __shfl_up_sync(0xffffffffu, a.lo, off)};
-}
-
-// Inclusive warp scan in float-float (lane order).
-__device__ __forceinline__ FF warp_incl_scan_ff(FF x) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const FF y = ff_shfl_up(x, off);
-    if (lane >= off) x = ff_add(y, x);
-  }
-  return x;
-}
-
-// Block-wide exclusive scan of one float-float per thread; all threads get
-// the total.
-__device__ __forceinline__ FF block_exclusive_scan_ff(FF x, FinalShared& sh, FF* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const FF incl = warp_incl_scan_ff(x);
-  if (lane == 31) sh.warp_ff[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const FF w = lane < kFinalWarps ? sh.warp_ff[lane] : FF{0.0f, 0.0f};
-    const FF wi = warp_incl_scan_ff(w);
-    FF wx = ff_shfl_up(wi, 1);
-    if (lane == 0) wx = FF{0.0f, 0.0f};
-    __syncwarp();
-    if (lane < kFinalWarps) sh.warp_ff[lane] = wx;
-    if (lane == kFinalWarps - 1) sh.warp_ff[kFinalWarps] = wi;
-  }
-  __syncthreads();
-  // Exclusive prefix within the warp, then the warp's offset.
-  FF ex = ff_shfl_up(incl, 1);
-  if (lane == 0) ex = FF{0.0f, 0.0f};
-  ex = ff_add(sh.warp_ff[warp], ex);
-  *total = sh.warp_ff[kFinalWarps];
-  __syncthreads();
-  return ex;
-}
-
 // Inverse CDF over the request's segment records (global, nseg entries):
-// the first entry whose cumulative weight exceeds u * total.  Block-wide;
-// returns the token, or -1 if the total weight is not a finite positive
-// number.  rec_sm: nseg float2 of shared memory.  mu: the residual's
-// normaliser correction (0 otherwise).
+// the first entry whose cumulative weight exceeds u * total.  Block-wide.
+// Returns -1 on every thread if the weights have no mass or one of them is
+// not a finite number; otherwise warp 0 gets the token and the other warps
+// kPicked.  dshares: the P slices' shares of D (fixed point, 2^-58) for a
+// residual, from which mu = D / (1 - D) is formed here (their loads go out
+// with the record loads), or null (mu = 0).  rec_sm: nseg float2 of shared
+// memory.  dry: made-up records and shares instead of rec and dshares (see
+// final_body); nothing global is read from them or written either way.
+constexpr int kPicked = INT32_MAX - 1;
+
 template <typename TIn>
-__device__ int cdf_pick(const TIn* rt, const TIn* rd, int V, const MassSpec& ms, bool bonus,
-                        float u, const float2* rec, int nseg, bool vec_ok, FinalShared& sh,
-                        float2* rec_sm, float mu) {
+__device__ __noinline__ int cdf_pick(const TIn* rt, const TIn* rd, int V, MassSpec ms, bool bonus,
+                                     float u, const float2* rec, int nseg, bool vec_ok,
+                                     FinalShared& sh, float2* rec_sm, const long long* dshares,
+                                     int P, bool dry) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool residual = !bonus && ms.has_q;
-  float refm = -FLT_MAX;
-  for (int s = threadIdx.x; s < nseg; s += kFinalThreads) {
-    const float2 r = __ldcg(&rec[s]);
+  // One round of loads: the D shares (threads < P) and the records, with
+  // the largest weight bound (record.x, or a bonus record's sum) and the
+  // bonus reference.
+  long long dfx = 0;
+  if (dshares != nullptr && (int)threadIdx.x < P) dfx = dry ? 0ll : __ldcg(&dshares[threadIdx.x]);
+  float refm = -FLT_MAX, wmx = 0.0f;
+  auto take = [&](int s, float2 r) {
     rec_sm[s] = r;
-    if (bonus && r.y > 0.0f) refm = fmaxf(refm, __fmul_rn(r.x, ms.sc));
+    if (bonus) {
+      if (r.y > 0.0f) refm = fmaxf(refm, __fmul_rn(r.x, ms.sc));
+      wmx = fmaxf(wmx, r.y);
+    } else {
+      wmx = fmaxf(wmx, r.x);
+    }
+  };
+  // The first kRecRound records of each thread are all loaded before any is
+  // stored, so that their loads overlap (the shared-memory stores would
+  // otherwise hold each load behind the previous one).
+  constexpr int kRecRound = 4;
+  float2 rr[kRecRound];
+#pragma unroll
+  for (int q = 0; q < kRecRound; ++q) {
+    const int s = threadIdx.x + q * kFinalThreads;
+    rr[q] = s < nseg ? (dry ? make_float2(1.0f, 0.5f) : __ldcg(&rec[s])) : make_float2(0.0f, 0.0f);
   }
-  float REF = 0.0f;
-  if (bonus) {
-    refm = warp_max_f32(refm);
-    if (lane == 0) sh.warp_f[warp] = refm;
+#pragma unroll
+  for (int q = 0; q < kRecRound; ++q) {
+    const int s = threadIdx.x + q * kFinalThreads;
+    if (s < nseg) take(s, rr[q]);
+  }
+  for (int s = threadIdx.x + kRecRound * kFinalThreads; s < nseg; s += kFinalThreads)
+    take(s, dry ? make_float2(1.0f, 0.5f) : __ldcg(&rec[s]));
+  if (dshares != nullptr && warp < 2) {  // P <= 64 shares over two warps
+    dfx = warp_sum_i64(dfx);
+    if (lane == 0) sh.dsx[warp] = dfx;
+  }
+  refm = warp_max_f32(refm);
+  wmx = warp_max_f32(wmx);
+  if (lane == 0) {
+    sh.warp_f[warp] = refm;
+    sh.warp_w[warp] = wmx;
   }
   __syncthreads();
-  if (bonus) {
-    REF = -FLT_MAX;
-#pragma unroll
-    for (int w = 0; w < kFinalWarps; ++w) REF = fmaxf(REF, sh.warp_f[w]);
+  // mu, REF and the weight bound: every thread forms them from the same
+  // values in the same order.
+  float mu = 0.0f;
+  if (dshares != nullptr) {
+    const float Df = __fmul_rn(__ll2float_rn(sh.dsx[0] + sh.dsx[1]), kDUnscale);
+    mu = (Df > -1.0f && Df < 1.0f) ? __fdiv_rn(Df, __fsub_rn(1.0f, Df)) : 0.0f;
   }
+  float REF = -FLT_MAX, WMX = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kFinalWarps; ++w) {
+    REF = fmaxf(REF, sh.warp_f[w]);
+    WMX = fmaxf(WMX, sh.warp_w[w]);
+  }
+  if (!bonus) REF = 0.0f;
+  // A residual weight R - mu Q+ exceeds R by at most about |mu| (Q+ is at
+  // most the q mass, about 1); a bonus weight s * 2^(m*sc - REF) is at most
+  // s.  Weights are clamped to the bound, which only ever trims rounding.
+  const float bound = residual ? __fadd_ru(WMX, __fmul_ru(2.0f, fabsf(mu))) : WMX;
+  if (!(bound > 0.0f && bound <= FLT_MAX)) return -1;  // uniform across the block
+  // bound < 2^(eb+1); weights scaled by 2^S stay below 2^50, their sum below 2^63.
+  const int eb = ((__float_as_int(bound) >> 23) & 0xff) - 127;
+  const float fsc = exp2_int(min(126, 49 - eb));
+  auto fixed = [&](float w) { return __float2ll_rn(__fmul_rn(fminf(w, bound), fsc)); };
+
   // Thread t owns segments [sa, sb).
   const int per = (nseg + kFinalThreads - 1) / kFinalThreads;
   const int sa = min(nseg, (int)threadIdx.x * per), sb = min(nseg, sa + per);
-  // Exclusive prefix of the weights, in float-float.
-  FF loc = {0.0f, 0.0f};
-  for (int s = sa; s < sb; ++s) loc = ff_add_f(loc, seg_weight(rec_sm[s], bonus, ms.sc, REF, mu));
-  FF total;
-  FF run = block_exclusive_scan_ff(loc, sh, &total);
-  if (!(total.hi > 0.0f && total.hi <= FLT_MAX)) return -1;  // uniform across the block
-  const FF target = ff_mul_f(total, u);
-
-  // The last segment with positive weight that starts at or before target.
-  if (threadIdx.x == 0) sh.cand = -1;
-  __syncthreads();
-  int cand = -1;
-  FF cand_excl = {0.0f, 0.0f};
+  long long loc = 0;
+  bool finite = true;
   for (int s = sa; s < sb; ++s) {
     const float w = seg_weight(rec_sm[s], bonus, ms.sc, REF, mu);
-    if (w > 0.0f && ff_le(run, target)) {
+    finite = finite && (w >= 0.0f && w <= FLT_MAX);
+    loc += fixed(w);
+  }
+  const long long incl = warp_incl_scan_i64(loc);
+  if (lane == 31) sh.wsum[warp] = incl;
+  if (__syncthreads_or(!finite)) return -1;
+  long long wv[kFinalWarps];
+#pragma unroll
+  for (int w = 0; w < kFinalWarps; ++w) wv[w] = sh.wsum[w];
+  long long total = 0, run = 0;
+#pragma unroll
+  for (int w = 0; w < kFinalWarps; ++w) {
+    if (w == warp) run = total;
+    total += wv[w];
+  }
+  if (total <= 0) return -1;
+  run += incl - loc;  // exclusive prefix of this thread's first segment
+  // target = floor(total * u), u in [0, 1) scaled exactly to 64 bits.
+  const long long target = (long long)__umul64hi((unsigned long long)total,
+                                                 __float2ull_rz(__fmul_rn(u, 18446744073709551616.0f)));
+
+  // The last segment with weight that starts at or before target: within a
+  // thread the last one found, within a warp the highest lane that has one,
+  // within the block the highest warp.
+  int cand = -1;
+  long long cand_excl = 0;
+  for (int s = sa; s < sb; ++s) {
+    const long long w = fixed(seg_weight(rec_sm[s], bonus, ms.sc, REF, mu));
+    if (w > 0 && run <= target) {
       cand = s;
       cand_excl = run;
     }
-    run = ff_add_f(run, w);
+    run += w;
   }
-  if (cand >= 0) atomicMax(&sh.cand, cand);
+  const unsigned has = __ballot_sync(0xffffffffu, cand >= 0);
+  if (has == 0u) {
+    if (lane == 0) sh.wcand[warp] = -1;
+  } else if (lane == 31 - __clz(has)) {
+    sh.wcand[warp] = cand;
+    sh.wexcl[warp] = cand_excl;
+  }
   __syncthreads();
-  const int j = sh.cand;
-  if (cand >= 0 && cand == j) sh.cand_excl = cand_excl;
-  __syncthreads();
+  if (warp != 0) return kPicked;
+  // A positive total always has a candidate (the first segment with weight
+  // starts at 0); j stays inside the row regardless.
+  int j = 0;
+  long long jexcl = 0;
+#pragma unroll
+  for (int w = kFinalWarps - 1; w >= 0; --w) {
+    const int c = sh.wcand[w];
+    if (c >= 0) {
+      j = c;
+      jexcl = sh.wexcl[w];
+      break;
+    }
+  }
 
   // Re-read segment j: the first entry whose cumulative weight exceeds the
-  // target, or the segment's last entry with mass when rounding left the
-  // target just past the segment's own sum.
-  if (warp == 0) {
-    Seg8<TIn> t, d;
-    seg_load(t, rt, j * kSegElems + lane * 8, V, vec_ok);
-    if (ms.has_q && !bonus) seg_load(d, rd, j * kSegElems + lane * 8, V, vec_ok);
-    float r[8];
-    float scale = 1.0f;
-    if (bonus) {
-      const float msr = __fmul_rn(rec_sm[j].x, ms.sc);
-      bonus_masses(t, ms.sc, msr, r);
-      scale = exp2_diff(msr, REF);
-    } else if (residual) {
-      float qb[8];
-      residual_entries(t, d, ms, r, qb);
+  // target, or the segment's last entry with weight when the target lies
+  // past the segment's own sum of entries (its record is that sum up to
+  // rounding).
+  Seg8<TIn> t, d;
+  seg_load(t, rt, j * kSegElems + lane * 8, V, vec_ok);
+  if (ms.has_q && !bonus) seg_load(d, rd, j * kSegElems + lane * 8, V, vec_ok);
+  float r[8];
+  if (bonus) {
+    const float msr = __fmul_rn(rec_sm[j].x, ms.sc);
+    bonus_masses(t, ms.sc, msr, r);
+    const float scale = exp2_diff(msr, REF);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) r[e] = residual_weight(r[e], qb[e], mu);
-    } else {
-      target_entries(t, ms, r);
-    }
-    // Cumulative weight within the segment, in float-float: lane sums, then
-    // an exclusive scan over the lanes, then entry by entry.
-    FF lsum = {0.0f, 0.0f};
+    for (int e = 0; e < 8; ++e) r[e] = __fmul_rn(r[e], scale);
+  } else if (residual) {
+    float qb[8];
+    residual_entries(t, d, ms, r, qb);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) lsum = ff_add_f(lsum, r[e]);
-    const FF lincl = warp_incl_scan_ff(lsum);
-    FF cum = ff_shfl_up(lincl, 1);
-    if (lane == 0) cum = FF{0.0f, 0.0f};
-    const FF tseg = ff_sub(target, sh.cand_excl);
-    int first_e = 8, last_pos = -1;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      cum = ff_add_f(cum, r[e]);
-      if (first_e == 8 && r[e] > 0.0f && !ff_le(ff_mul_f(cum, scale), tseg)) first_e = e;
-      if (r[e] > 0.0f) last_pos = e;
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, first_e < 8);
-    int token;
-    if (hit) {
-      const int l = __ffs(hit) - 1;
-      token = j * kSegElems + l * 8 + __shfl_sync(0xffffffffu, first_e, l);
-    } else {
-      const unsigned has = __ballot_sync(0xffffffffu, last_pos >= 0);
-      const int l = has ? 31 - __clz(has) : 0;
-      token = j * kSegElems + l * 8 + max(0, __shfl_sync(0xffffffffu, last_pos, l));
-    }
-    if (lane == 0) sh.token = token;
+    for (int e = 0; e < 8; ++e) r[e] = residual_weight(r[e], qb[e], mu);
+  } else {
+    target_entries(t, ms, r);
   }
-  __syncthreads();
-  const int tk = sh.token;
-  __syncthreads();
-  return tk;
+  long long fe[8], lsum = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    fe[e] = fixed(fmaxf(r[e], 0.0f));  // a NaN entry counts as no weight
+    lsum += fe[e];
+  }
+  long long cum = warp_incl_scan_i64(lsum) - lsum;
+  const long long tseg = target - jexcl;
+  int first_e = 8, last_pos = -1;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    cum += fe[e];
+    if (first_e == 8 && fe[e] > 0 && cum > tseg) first_e = e;
+    if (fe[e] > 0) last_pos = e;
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, first_e < 8);
+  if (hit) {
+    const int l = __ffs(hit) - 1;
+    return j * kSegElems + l * 8 + __shfl_sync(0xffffffffu, first_e, l);
+  }
+  const unsigned hasm = __ballot_sync(0xffffffffu, last_pos >= 0);
+  const int l = hasm ? 31 - __clz(hasm) : 0;
+  return j * kSegElems + l * 8 + max(0, __shfl_sync(0xffffffffu, last_pos, l));
 }
 
 // Slice bounds in segments.
@@ -748,12 +837,38 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
   const int b = (int)(blockIdx.x / (unsigned)P), part = (int)(blockIdx.x - (unsigned)b * P);
   WsHeader* h = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
   float2* rec = reinterpret_cast<float2*>(p.ws + p.lay.seg_mass) + (size_t)b * nseg;
-  // Per slice: (max, bits of its lowest index) of a greedy row L, or the
-  // slice's share of D (hi, lo) for a residual.
+  // Per slice: (max, bits of its lowest index) of a greedy row L, or for a
+  // residual the slice's share of D as a 64-bit fixed-point integer (2^-58).
   float2* slice_out = reinterpret_cast<float2*>(p.ws + p.lay.slice_out) + (size_t)b * kMaxSlices;
   int32_t* final_done = reinterpret_cast<int32_t*>(p.ws + p.lay.final_done);
   const int L = __ldg(&p.lengths[b]);
   const float T = __ldg(&p.temperature[b]);
+  // The request's first rows, written by the plan kernel: loaded now, off
+  // the path that follows the outcome.
+  const int2 rb = __ldcg(reinterpret_cast<const int2*>(p.ws + p.lay.rowbase) + b);
+
+  // A slice that starts before its request's outcome is known (small
+  // batches: the pass launches behind the sweep and waits) first runs the
+  // combine once on made-up records, writing nothing global, so that its
+  // code is in the caches when the real combine runs: otherwise the one CTA
+  // per request that combines fetches that code from memory, on the round's
+  // critical path, and after an L2 flush that took 17 of a single request's
+  // 44 us.
+  if (threadIdx.x == 0) {
+    const unsigned long long st0 =
+        ld_acquire_u64(reinterpret_cast<const unsigned long long*>(p.ws + p.lay.state) + b);
+    const int f0 = __ldcg(reinterpret_cast<const int32_t*>(p.ws + p.lay.flags) + b);
+    sh.warm = (f0 & kReqValid) && part == 0 && !outcome_known_word(st0, L);
+  }
+  __syncthreads();
+  if (sh.warm) {
+    MassSpec wm = {};
+    wm.sc = 1.0f;
+    wm.has_q = true;
+    const TIn* wr = reinterpret_cast<const TIn*>(p.ws);  // any 1 KB the call owns
+    (void)cdf_pick<TIn>(wr, wr, kSegElems, wm, false, 0.5f, nullptr, 1, true, sh, rec_sm,
+                        reinterpret_cast<const long long*>(slice_out), P, true);
+  }
 
   // Warp 0: wait for the outcome (flags and masks, every lane the same),
   // then one round of loads of every position's normalisers, argmax and
@@ -768,6 +883,7 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
     const float u_t = (T != 0.0f && t <= L && t <= p.k)
                           ? __ldg(&p.uniforms[(size_t)b * (p.k + 1) + t])
                           : 0.0f;
+    if (t == L) sh.uL = u_t;  // the final token's uniform (0 at T = 0)
     const bool in_ok = (t >= L || (x_t >= 0 && x_t < p.V)) &&
                        (T == 0.0f || t > L || (u_t >= 0.0f && u_t < 1.0f));  // NaN fails
     const bool inputs_ok = __all_sync(0xffffffffu, in_ok);
@@ -778,26 +894,25 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
     // short wait, exercising the path a real timeout takes.
     const bool never = p.test_late && part != 0;
     const unsigned long long limit = never ? kTestLateLimitNs : kWaitLimitNs;
+    // The request's flags are the plan's (fixed for the round); the wait
+    // polls the decision word alone.  A row without mass is recorded in
+    // bad_bits before the decision that releases it, so bad_bits is read
+    // once, after the acquire that ends the wait.
+    f = __ldcg(reinterpret_cast<const int32_t*>(p.ws + p.lay.flags) + b);
     const unsigned long long t0 = global_ns();
-    for (;;) {
-      f = __ldcg(reinterpret_cast<const int32_t*>(p.ws + p.lay.flags) + b);
-      if (!inputs_ok) break;  // invalid: no outcome to wait for
+    while (inputs_ok && (f & kReqValid)) {  // otherwise no outcome to wait for
       const unsigned long long st =
           ld_acquire_u64(reinterpret_cast<const unsigned long long*>(p.ws + p.lay.state) + b);
       dec = (uint32_t)st;
       acc = (uint32_t)(st >> 32);
-      bad = __ldcg(reinterpret_cast<const uint32_t*>(p.ws + p.lay.bad_bits) + b);
-      if (!(f & kReqValid)) break;
-      const uint32_t rej = dec & ~acc & lmask;
-      const int nn = rej ? (__ffs((int)rej) - 1) : L;
-      const uint32_t pre = (nn >= 32) ? 0xffffffffu : ((1u << nn) - 1u);
-      if ((dec & acc & pre) == pre && !never) break;
+      if (outcome_known_word(st, L) && !never) break;
       if (global_ns() - t0 > limit) {
         late = true;
         break;
       }
-      __nanosleep(256);
+      __nanosleep(128);
     }
+    bad = __ldcg(reinterpret_cast<const uint32_t*>(p.ws + p.lay.bad_bits) + b);
     const float4* pos_c = reinterpret_cast<const float4*>(p.ws + p.lay.pos_c);
     const int32_t* pos_arg = reinterpret_cast<const int32_t*>(p.ws + p.lay.pos_arg);
     float4 c4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -860,6 +975,9 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
   int token = sh.token;
   bool gave_up = sh.late != 0;
 
+  // At most 32 outputs per request: warp 0 writes them all (after cdf_pick,
+  // only warp 0 holds the token).
+  static_assert(SPEC_MAX_K + 1 <= 32, "one warp writes a request's outputs");
   auto write_outputs = [&](bool invalid, int final_token) {
     for (int j = threadIdx.x; j <= p.k; j += kFinalThreads) {
       int v = -1;
@@ -879,9 +997,8 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
   MassSpec ms = {};
   const bool bonus = (job == kJobBonus);
   if (rows_job) {
-    // Row n of the request in either buffer: its first rows come from the
-    // plan kernel (padded or packed layout).
-    const int2 rb = __ldcg(reinterpret_cast<const int2*>(p.ws + p.lay.rowbase) + b);
+    // Row n of the request in either buffer: its first rows (rb) come from
+    // the plan kernel (padded or packed layout).
     trow = static_cast<const TIn*>(p.target) + ((size_t)rb.x + n) * (size_t)p.V;
     drow = job == kJobResidual
                ? static_cast<const TIn*>(p.draft) + ((size_t)rb.y + n) * (size_t)p.V
@@ -902,7 +1019,7 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
       const ArgAcc a = slice_argmax(trow, p.V, s_lo, s_hi, vec_ok, sh);
       if (threadIdx.x == 0) __stcg(&slice_out[part], make_float2(a.v, __int_as_float(a.i)));
     } else {
-      FF dsum = {0.0f, 0.0f};
+      long long dsum = 0;
       // Aligned rows stream through shared memory; others load directly.
       if (vec_ok && ((size_t)p.V * sizeof(TIn)) % 16 == 0) {
         if (!slice_records_staged(trow, drow, p.V, ms, bonus, s_lo, s_hi, rec,
@@ -914,10 +1031,16 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
         slice_records(trow, drow, p.V, ms, bonus, s_lo, s_hi, rec, vec_ok, &dsum);
       }
       if (job == kJobResidual) {
-        // The slice's share of D, summed over the block in float-float.
-        FF total;
-        (void)block_exclusive_scan_ff(dsum, sh, &total);
-        if (threadIdx.x == 0) __stcg(&slice_out[part], make_float2(total.hi, total.lo));
+        // The slice's share of D (fixed point, 2^-58), summed over the block.
+        const long long wsum = warp_sum_i64(dsum);
+        if ((threadIdx.x & 31) == 0) sh.dwarp[threadIdx.x >> 5] = wsum;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          long long total = 0;
+#pragma unroll
+          for (int w = 0; w < kFinalWarps; ++w) total += sh.dwarp[w];
+          __stcg(reinterpret_cast<long long*>(slice_out) + part, total);
+        }
       }
     }
   }
@@ -977,40 +1100,24 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
     token = sh.token;
     bad = (token == INT32_MAX);
   } else {
-    const float u = __ldg(&p.uniforms[(size_t)b * (p.k + 1) + L]);
-    // Residual: D = sum (p - q) over the row pair from the slices' shares,
-    // then mu = D / (1 - D), the correction for the normalisers' ratio.
-    float mu = 0.0f;
-    if (job == kJobResidual) {
-      // The P <= 64 shares, one per lane of the first two warps.
-      if (threadIdx.x < 64) {
-        FF D = {0.0f, 0.0f};
-        if ((int)threadIdx.x < P) {
-          const float2 so = __ldcg(&slice_out[threadIdx.x]);
-          D = FF{so.x, so.y};
-        }
-        D = warp_sum_ff(D);
-        if ((threadIdx.x & 31) == 0) sh.warp_ff[threadIdx.x >> 5] = D;
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        const float Df = ff_to_float(ff_add(sh.warp_ff[0], sh.warp_ff[1]));
-        sh.mu = (Df > -1.0f && Df < 1.0f) ? __fdiv_rn(Df, __fsub_rn(1.0f, Df)) : 0.0f;
-      }
-      __syncthreads();
-      mu = sh.mu;
-    }
-    token = cdf_pick(trow, drow, p.V, ms, bonus, u, rec, nseg, vec_ok, sh, rec_sm, mu);
+    const float u = sh.uL;
+    // A residual's D = sum (p - q) over the row pair comes from the slices'
+    // shares; cdf_pick turns it into mu = D / (1 - D), the correction for
+    // the normalisers' ratio.
+    token = cdf_pick(trow, drow, p.V, ms, bonus, u, rec, nseg, vec_ok, sh, rec_sm,
+                     job == kJobResidual ? reinterpret_cast<const long long*>(slice_out) : nullptr,
+                     P, false);
     if (token < 0 && job == kJobResidual) {
       // Residual mass zero (p_n == q_n up to rounding): draw from p_n.
       if (threadIdx.x == 0) atomicAdd(&h->residual_zero, 1);
       MassSpec pm = ms;
       pm.has_q = false;
-      FF unused = {0.0f, 0.0f};
+      long long unused = 0;
       slice_records(trow, trow, p.V, pm, false, 0, nseg, rec, vec_ok, &unused);
       __threadfence_block();
       __syncthreads();
-      token = cdf_pick(trow, trow, p.V, pm, false, u, rec, nseg, vec_ok, sh, rec_sm, 0.0f);
+      token = cdf_pick(trow, trow, p.V, pm, false, u, rec, nseg, vec_ok, sh, rec_sm, nullptr, P,
+                       false);
     }
     bad = (token < 0);
   }

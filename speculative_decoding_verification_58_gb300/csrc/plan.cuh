@@ -4,9 +4,10 @@
 // that a rejection found at an early position can spare the rows behind it.
 //
 // One CTA, two flat-parallel passes: (1) every request's scalars are
-// checked (invalid requests land in a shared bitmask) and its state reset;
-// (2) every (position, request) item is counted and one block-wide scan
-// places the row descriptors.
+// checked and its state reset (invalid requests land in a shared bitmask, or,
+// for a batch of at most one request per thread, every request's row facts
+// in a shared table); (2) every (position, request) item is counted and one
+// block-wide scan places the row descriptors.
 //
 // Row addressing: request b's target rows are rows t0_b + 0..L_b of the
 // target buffer and its draft rows d0_b + 0..L_b-1 of the draft buffer.  The
@@ -81,6 +82,17 @@ __device__ __forceinline__ void fill_u32(uint32_t* dst, size_t n, uint32_t v) {
   for (size_t j = (n & ~size_t(3)) + threadIdx.x; j < n; j += kPlanThreads) dst[j] = v;
 }
 
+// One request's row facts, kept in shared memory for the row pass when the
+// batch has at most one request per thread.
+struct PlanReq {
+  int L;       // positions to verify
+  int rows;    // rows per position in the row list: 0 (none), 1 (greedy) or 2
+  float sc;    // log2(e) / T, 0 at T = 0
+  int t0, d0;  // first target and draft rows
+};
+static_assert(kPlanThreads * sizeof(PlanReq) <= (SPEC_MAX_B / 32) * sizeof(uint32_t),
+              "the request table fits in the bad-mask words it shares");
+
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   // This kernel may itself be launched early, behind the previous kernel on
   // the stream: nothing is read or written before that kernel has finished.
@@ -88,14 +100,32 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   // Dependents may launch now; they wait for this grid's completion before
   // reading anything it writes.
   pdl_launch_dependents();
-  __shared__ uint32_t bad_mask[SPEC_MAX_B / 32];
+  // Either the bad-request bitmask (large batches) or the request table
+  // (at most one request per thread).
+  __shared__ __align__(16) uint32_t words[SPEC_MAX_B / 32];
   __shared__ int warp_tot[33];
   const int tid = threadIdx.x;
+  const bool small = p.B <= kPlanThreads;
+  uint32_t* bad_mask = words;
+  PlanReq* req = reinterpret_cast<PlanReq*>(words);
   WsHeader* h = reinterpret_cast<WsHeader*>(p.ws + p.lay.header);
   int4* rowdesc = reinterpret_cast<int4*>(p.ws + p.lay.rowdesc);
   int2* rowbase = reinterpret_cast<int2*>(p.ws + p.lay.rowbase);
   int32_t* flags = reinterpret_cast<int32_t*>(p.ws + p.lay.flags);
   int32_t* first_reject = reinterpret_cast<int32_t*>(p.ws + p.lay.first_reject);
+
+  // A small batch's request scalars are loaded first, so that their round
+  // trip overlaps the workspace fills below.
+  auto load_req = [&](int b, int& L, float& T, int2& rb) {
+    L = __ldg(&p.lengths[b]);
+    T = __ldg(&p.temperature[b]);
+    rb = p.t_start != nullptr ? make_int2(__ldg(&p.t_start[b]), __ldg(&p.d_start[b]))
+                              : make_int2(b * (p.k + 1), b * p.k);
+  };
+  int L0 = 0;
+  float T0 = 0.0f;
+  int2 rb0 = make_int2(0, 0);
+  if (small && tid < p.B) load_req(tid, L0, T0, rb0);
 
   if (tid == 0) {
     h->status = SPEC_OK;
@@ -112,8 +142,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     h->sweep_exited = 0;
     h->final_ctas_done = 0;
   }
-  const int words = (p.B + 31) >> 5;
-  for (int w = tid; w < words; w += kPlanThreads) bad_mask[w] = 0u;
+  if (!small)
+    for (int w = tid; w < ((p.B + 31) >> 5); w += kPlanThreads) bad_mask[w] = 0u;
 
   // Per-call state that does not depend on the inputs, with coalesced
   // stores: decision masks, chunk and final-pass counters to zero, every
@@ -138,17 +168,16 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   // (tokens in [0, V), uniforms in [0, 1)) are checked by the final pass,
   // which loads them anyway; until then every use guards its index.
   for (int b = tid; b < p.B; b += kPlanThreads) {
-    const int L = __ldg(&p.lengths[b]);
-    const float T = __ldg(&p.temperature[b]);
-    const int2 rb = p.t_start != nullptr ? make_int2(__ldg(&p.t_start[b]), __ldg(&p.d_start[b]))
-                                         : make_int2(b * (p.k + 1), b * p.k);
+    int L = L0;
+    float T = T0;
+    int2 rb = rb0;
+    if (!small) load_req(b, L, T, rb);
     bool bad = !(L >= 1 && L <= p.k && temperature_ok(T));
     // Packed rows: target rows t0 .. t0+L exist, and draft rows d0 .. d0+L-1
     // unless the request is greedy (its draft rows are never read).
     bad = bad || (p.t_start != nullptr &&
                   !(rb.x >= 0 && (long long)rb.x + L + 1 <= p.rows_t &&
                     (T == 0.0f || (rb.y >= 0 && (long long)rb.y + L <= p.rows_d))));
-    if (bad) atomicOr(&bad_mask[b >> 5], 1u << (b & 31));
     flags[b] = bad ? 0 : (kReqValid | (T == 0.0f ? kReqGreedy : 0));
     first_reject[b] = p.k;
     rowbase[b] = rb;
@@ -157,39 +186,58 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       atomicMin(&h->first_bad, b);
       atomicCAS(&h->status, SPEC_OK, SPEC_ERR_BAD_INPUT);
     }
+    if (small) {
+      const bool listed = !bad && !(p.skip_t01 && (T == 0.0f || T == 1.0f));
+      req[b] = PlanReq{L, listed ? (T == 0.0f ? 1 : 2) : 0, T == 0.0f ? 0.0f : softmax_scale(T),
+                       rb.x, rb.y};
+    } else if (bad) {
+      atomicOr(&bad_mask[b >> 5], 1u << (b & 31));
+    }
   }
   __syncthreads();
 
-  // Pass 2, item it = i*B + b: the rows of (b, i) in position-major order;
+  // Row pass, item it = i*B + b: the rows of (b, i) in position-major order;
   // one block-wide scan places their descriptors.
+  auto item = [&](int b, int i, int& rows, float& sc, int& trow, int& drow) {
+    if (small) {
+      const PlanReq r = req[b];
+      rows = i < r.L ? r.rows : 0;
+      sc = r.sc;
+      trow = r.t0 + i;
+      drow = r.d0 + i;
+      return;
+    }
+    const bool ok = !((bad_mask[b >> 5] >> (b & 31)) & 1u);
+    const float T = __ldg(&p.temperature[b]);
+    rows = (ok && i < __ldg(&p.lengths[b]) && !(p.skip_t01 && (T == 0.0f || T == 1.0f)))
+               ? (T == 0.0f ? 1 : 2)
+               : 0;
+    sc = T == 0.0f ? 0.0f : softmax_scale(T);
+    trow = (p.t_start != nullptr ? __ldg(&p.t_start[b]) : b * (p.k + 1)) + i;
+    drow = (p.t_start != nullptr ? __ldg(&p.d_start[b]) : b * p.k) + i;
+  };
   const int items = p.k * p.B;
   const int per = (items + kPlanThreads - 1) / kPlanThreads;
   const int lo = min(items, tid * per), hi = min(items, lo + per);
   int cnt = 0;
   for (int it = lo; it < hi; ++it) {
     const int i = it / p.B, b = it - i * p.B;
-    const bool ok = !((bad_mask[b >> 5] >> (b & 31)) & 1u);
-    const float T = __ldg(&p.temperature[b]);
-    if (ok && i < __ldg(&p.lengths[b]) && !(p.skip_t01 && (T == 0.0f || T == 1.0f)))
-      cnt += T == 0.0f ? 1 : 2;
+    int rows, trow, drow;
+    float sc;
+    item(b, i, rows, sc, trow, drow);
+    cnt += rows;
   }
   int pos;
   const int total = block_exclusive_scan(cnt, &pos, warp_tot);
   for (int it = lo; it < hi; ++it) {
     const int i = it / p.B, b = it - i * p.B;
-    const bool ok = !((bad_mask[b >> 5] >> (b & 31)) & 1u);
-    const int L = __ldg(&p.lengths[b]);
-    if (!ok || i >= L) continue;
-    const float T = __ldg(&p.temperature[b]);
-    if (p.skip_t01 && (T == 0.0f || T == 1.0f)) continue;
-    const float sc = T == 0.0f ? 0.0f : softmax_scale(T);
+    int rows, trow, drow;
+    float sc;
+    item(b, i, rows, sc, trow, drow);
+    if (rows == 0) continue;
     const int slot = (b * p.k + i) << 1;
-    const int trow = (p.t_start != nullptr ? __ldg(&p.t_start[b]) : b * (p.k + 1)) + i;
     rowdesc[pos++] = make_int4(slot, __float_as_int(sc), trow, 0);
-    if (T != 0.0f) {
-      const int drow = (p.t_start != nullptr ? __ldg(&p.d_start[b]) : b * p.k) + i;
-      rowdesc[pos++] = make_int4(slot | 1, __float_as_int(sc), drow, 0);
-    }
+    if (rows == 2) rowdesc[pos++] = make_int4(slot | 1, __float_as_int(sc), drow, 0);
   }
   if (tid == 0) {
     h->rows_planned = total;

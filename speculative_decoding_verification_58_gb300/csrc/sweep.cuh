@@ -133,10 +133,13 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
   // described (row descriptors loaded, one lane per unit), checked (skip
   // flag loaded), then issued.  Each step consumes values loaded one loop
   // iteration earlier, so no global round trip stands in front of a copy.
+  // Units 0 .. gridDim.x-1 are the CTAs' first units, one each, taken
+  // without a claim so that the first copy waits for no round trip; the
+  // counter hands out the units after them.
   auto want_at = [&](int base) { return base < small_after ? kClaim : 1; };
   auto claim = [&](int want) {
     int v = 0;
-    if (lane == 0) v = atomicAdd(&h->work_next, want);
+    if (lane == 0) v = (int)gridDim.x + atomicAdd(&h->work_next, want);
     return v;  // lane 0 only; broadcast when needed
   };
   auto describe = [&](int base, int want) {
@@ -153,10 +156,12 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
     return fr;
   };
 
-  int wantC = want_at(0);
-  int baseC = __shfl_sync(0xffffffffu, claim(wantC), 0);
+  int wantC = 1;
+  int baseC = (int)blockIdx.x;
   int4 rdC = describe(baseC, wantC);
-  int frC = check(rdC);
+  // No decision can precede a CTA's first unit by much; the check before
+  // each stage still applies to it.
+  int frC = INT32_MAX;
   int wantB = want_at(baseC + wantC);
   int baseB = __shfl_sync(0xffffffffu, claim(wantB), 0);
   int4 rdB = describe(baseB, wantB);
@@ -325,8 +330,12 @@ __device__ void sweep_producer_big(const SweepParams& p, SweepSmem& sm, WsHeader
     return u < units_total ? __ldcg(&rowdesc[u / p.nch]) : make_int4(-1, 0, 0, 0);
   };
 
-  int nxt = atomicAdd(&h->work_next, 1);
+  // The CTA's first unit is unit blockIdx.x, taken without a claim so that
+  // the first copy waits for no round trip; the counter hands out the units
+  // after the grid's first ones.
+  int nxt = (int)blockIdx.x;
   int4 nrd = describe(nxt);
+  bool first_unit = true;
   while (nxt < units_total) {
     const int uu = nxt;
     const int4 rd = nrd;
@@ -357,8 +366,12 @@ __device__ void sweep_producer_big(const SweepParams& p, SweepSmem& sm, WsHeader
     const char* src0 = reinterpret_cast<const char*>(rowp + a0);
     const int look = nstage > kLookStages ? nstage - kLookStages : 0;
     for (int j = 0; j < nstage; ++j) {
-      const int frj = recheck ? *(volatile const int32_t*)&first_reject[ub] : INT32_MAX;
-      if (j == look) nxt = atomicAdd(&h->work_next, 1);
+      // The CTA's first stage goes out without the look: no decision can
+      // precede it by much, and its load would stand before the first copy.
+      const int frj = (recheck && !(first_unit && j == 0))
+                          ? *(volatile const int32_t*)&first_reject[ub]
+                          : INT32_MAX;
+      if (j == look) nxt = (int)gridDim.x + atomicAdd(&h->work_next, 1);
       if (j == look + 1) {
         nrd = describe(nxt);
         described = true;
@@ -402,8 +415,9 @@ __device__ void sweep_producer_big(const SweepParams& p, SweepSmem& sm, WsHeader
       if (drop) break;
     }
     if (!ok) break;
+    first_unit = false;
     // A unit that ended before its look-ahead point claims its successor now.
-    if (nxt < 0) nxt = atomicAdd(&h->work_next, 1);
+    if (nxt < 0) nxt = (int)gridDim.x + atomicAdd(&h->work_next, 1);
     if (!described) nrd = describe(nxt);
   }
 
