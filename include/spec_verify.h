@@ -382,6 +382,37 @@ const char* spec_status_string(spec_status_t status);
 /* SPEC_VERIFY_ABI_VERSION of the loaded library. */
 int spec_abi_version(void);
 
+/*
+ * Range-checking builds.  The library built with -DSPEC_DEBUG
+ * (libspecverify_debug.so, same entry points and results) checks, on the
+ * device, every index its kernels form into a buffer whose extent is known:
+ * row descriptors, logit rows of both buffers, partial slots, completion
+ * counters, segments, sampled tokens, OPD outputs and D3D branch slots.  An
+ * index outside its range is counted, the site of the first failing check
+ * kept, and the access redirected to element 0 of the same buffer, so that a
+ * fault of the library's own indexing shows as a count instead of a stray
+ * access.  Site codes:
+ *    1 plan: descriptor slot        7 final pass: residual / bonus row
+ *    2 sweep: descriptor index      8 final pass: chosen segment
+ *    3 sweep: logit row             9 final pass: sampled token < V
+ *    4 sweep: partial slot         10 OPD: logit row, argmax element
+ *    5 sweep: completion counter   11 OPD: output element
+ *    6 sweep: decided position     12 D3D: branch slot
+ */
+
+/* 1 if the loaded library is the range-checking build, else 0. */
+int spec_debug_build(void);
+
+/*
+ * Wait for `stream`, then copy the range checks that failed on the current
+ * device since the last reset into *failures and the site of the first of
+ * them into *first_site (0 when none; both host pointers, either may be
+ * null), and reset both when `reset` is non-zero.  The counters are
+ * device-wide (every call on the device adds to them).  A release build
+ * reports 0 and SPEC_OK.  Returns SPEC_OK or SPEC_ERR_CUDA.
+ */
+spec_status_t spec_debug_checks(int32_t* failures, int32_t* first_site, int reset, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

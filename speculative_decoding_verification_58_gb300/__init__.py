@@ -20,6 +20,7 @@ The functions keep the C names:
 ``spec_verify_opd(...)``             verification and OPD statistics in one pass over the rows
 ``spec_d3d_select(...)``             D3D branch selection: reuse a prepared successor block
 ``spec_status_string(code)``
+``spec_debug_build()``, ``spec_debug_checks()``  the range-checking build (SPEC_VERIFY_DEBUG=1)
 """
 
 from __future__ import annotations
@@ -29,7 +30,10 @@ import os
 from dataclasses import dataclass
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+# SPEC_VERIFY_DEBUG=1 in the environment loads the range-checking build
+# (same entry points; see spec_debug_checks) instead of the release one.
+DEBUG_BUILD = os.environ.get("SPEC_VERIFY_DEBUG", "") not in ("", "0")
+LIB_PATH = os.path.join(_HERE, "libspecverify_debug.so" if DEBUG_BUILD else "libspecverify.so")
 
 SPEC_OK = 0
 SPEC_ERR_INVALID_ARG = 1
@@ -49,7 +53,7 @@ EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_ex", "spec
            "spec_verify_packed", "spec_verify_report",
            "spec_verify_device_status", "spec_row_stats_workspace_bytes", "spec_row_stats",
            "spec_status_string", "spec_abi_version", "spec_verify_static", "spec_opd_stats",
-           "spec_verify_opd", "spec_d3d_select")
+           "spec_verify_opd", "spec_d3d_select", "spec_debug_build", "spec_debug_checks")
 SPEC_STATIC_SCRATCH_BYTES = 8 << 20
 
 
@@ -133,17 +137,40 @@ def lib() -> ctypes.CDLL:
     L.spec_status_string.restype = ctypes.c_char_p
     L.spec_abi_version.argtypes = []
     L.spec_abi_version.restype = ci
+    L.spec_debug_build.argtypes = []
+    L.spec_debug_build.restype = ci
+    L.spec_debug_checks.argtypes = [vp, vp, ci, vp]
+    L.spec_debug_checks.restype = ci
     _lib = L
     return L
 
 
 def build(force: bool = False) -> str:
-    """Compile the library in-tree with nvcc for sm_103a."""
+    """Compile the library and its range-checking build in-tree with nvcc
+    for sm_103a; return the path of the one this process loads."""
     global _lib
     from . import make_lib
-    path = make_lib.build(force=force)
+    make_lib.build_all(force=force)
     _lib = None
-    return path
+    return LIB_PATH
+
+
+def spec_debug_build() -> bool:
+    """Whether the loaded library is the range-checking build."""
+    return bool(lib().spec_debug_build())
+
+
+def spec_debug_checks(reset: bool = False, stream=None) -> tuple[int, int]:
+    """(failed range checks on the current device since the last reset, site
+    of the first); both 0 in a release build."""
+    import torch
+    f, site = ctypes.c_int32(0), ctypes.c_int32(0)
+    st = torch.cuda.current_stream() if stream is None else stream
+    code = lib().spec_debug_checks(ctypes.addressof(f), ctypes.addressof(site), int(reset),
+                                   ctypes.c_void_p(st.cuda_stream))
+    if code != SPEC_OK:
+        raise SpecVerifyError(code, "spec_debug_checks")
+    return f.value, site.value
 
 
 def status_string(code: int) -> str:

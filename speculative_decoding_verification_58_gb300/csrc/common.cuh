@@ -706,6 +706,45 @@ __device__ __forceinline__ void record_status(WsHeader* h, int code) {
 }
 
 // ---------------------------------------------------------------------------
+// Range checks of a SPEC_DEBUG build.  Each checked index into a buffer (a
+// row, a descriptor, a partial slot, a segment, an output element) is
+// compared with the buffer's extent; one that falls outside is counted in a
+// device-wide counter, with the site of the first such check (read and reset
+// through spec_debug_checks), and replaced by 0, a valid index at every
+// site, so that the access stays inside the buffer.  Release builds compile
+// the checks away.
+// ---------------------------------------------------------------------------
+enum SpecDebugSite {
+  kSitePlanRowdesc = 1,   // plan: descriptor slot < 2 B k
+  kSiteSweepRowdesc = 2,  // sweep: descriptor index < rows planned
+  kSiteSweepRow = 3,      // sweep: logit row < rows of its buffer
+  kSiteSweepPartial = 4,  // sweep: partial slot < rows x chunks
+  kSiteSweepCount = 5,    // sweep: (request, position) counter < B k
+  kSiteDecide = 6,        // sweep: decided (request, position) < B k
+  kSiteFinalRow = 7,      // final pass: residual / bonus row < rows of its buffer
+  kSiteFinalSegment = 8,  // final pass: chosen segment < segments of the row
+  kSiteFinalToken = 9,    // final pass: sampled token < V
+  kSiteOpdRow = 10,       // OPD statistics: logit row < rows of its buffer
+  kSiteOpdOut = 11,       // OPD statistics: output element < B k
+  kSiteD3d = 12,          // D3D selection: branch slot < branches
+};
+
+__device__ int g_debug_failures;  // checks that failed since the last reset
+__device__ int g_debug_site;      // site of the first of them
+
+__device__ __forceinline__ long long spec_debug_index(long long i, long long n, int site) {
+  if (i >= 0 && i < n) return i;
+  if (atomicAdd(&g_debug_failures, 1) == 0) atomicExch(&g_debug_site, site);
+  return 0;
+}
+
+#ifdef SPEC_DEBUG
+#define SPEC_CHECKED(i, n, site) spec_debug_index((long long)(i), (long long)(n), (site))
+#else
+#define SPEC_CHECKED(i, n, site) (i)
+#endif
+
+// ---------------------------------------------------------------------------
 // Partials: single 8-byte atomic exchanges and relaxed loads.
 // ---------------------------------------------------------------------------
 

@@ -54,7 +54,8 @@ __global__ void __launch_bounds__(kD3dWarps * 32) d3d_select_kernel(
     }
   }
   if (lane == 0) hit[b] = found;
-  const int32_t* src = branch_block + ((size_t)b * NB + (found >= 0 ? found : 0)) * blk;
+  const int32_t* src =
+      branch_block + ((size_t)b * NB + SPEC_CHECKED(found >= 0 ? found : 0, NB, kSiteD3d)) * blk;
   for (int t = lane; t < blk; t += 32)
     next_block[(size_t)b * blk + t] = found >= 0 ? __ldg(&src[t]) : -1;
 }

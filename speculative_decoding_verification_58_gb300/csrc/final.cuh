@@ -39,6 +39,7 @@ struct FinalParams {
   int P;           // slice CTAs per request; CTA x is slice x % P of request x / P
   int sweep_grid;  // CTAs of the sweep grid this pass follows
   int test_late;   // testing aid: slices other than the first give up waiting (see below)
+  long long rows_t, rows_d;  // rows of the target and draft buffers (range checks)
   int32_t* out_tokens;
   int32_t* num_accepted;
   unsigned char* ws;
@@ -770,6 +771,7 @@ __device__ __noinline__ int cdf_pick(const TIn* rt, const TIn* rd, int V, MassSp
       break;
     }
   }
+  if (!dry) j = (int)SPEC_CHECKED(j, nseg, kSiteFinalSegment);
 
   // Re-read segment j: the first entry whose cumulative weight exceeds the
   // target, or the segment's last entry with weight when the target lies
@@ -999,9 +1001,12 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
   if (rows_job) {
     // Row n of the request in either buffer: its first rows (rb) come from
     // the plan kernel (padded or packed layout).
-    trow = static_cast<const TIn*>(p.target) + ((size_t)rb.x + n) * (size_t)p.V;
+    trow = static_cast<const TIn*>(p.target) +
+           (size_t)SPEC_CHECKED((long long)rb.x + n, p.rows_t, kSiteFinalRow) * (size_t)p.V;
     drow = job == kJobResidual
-               ? static_cast<const TIn*>(p.draft) + ((size_t)rb.y + n) * (size_t)p.V
+               ? static_cast<const TIn*>(p.draft) +
+                     (size_t)SPEC_CHECKED((long long)rb.y + n, p.rows_d, kSiteFinalRow) *
+                         (size_t)p.V
                : trow;
     vec_ok = ((reinterpret_cast<uintptr_t>(trow) | reinterpret_cast<uintptr_t>(drow)) & 15u) == 0;
     const int s_lo = slice_lo(part, nseg, P), s_hi = slice_lo(part + 1, nseg, P);
@@ -1121,6 +1126,7 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
     }
     bad = (token < 0);
   }
+  if (!bad && threadIdx.x < 32) token = (int)SPEC_CHECKED(token, p.V, kSiteFinalToken);
   if (threadIdx.x == 0) {
     const unsigned long long rows = job == kJobResidual ? 2ull : 1ull;
     atomicAdd(&h->final_rows, rows);

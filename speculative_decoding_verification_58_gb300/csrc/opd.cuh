@@ -239,6 +239,7 @@ __device__ void opd_producer(const OpdParams& p, OpdSmem& sm, int cid, int ncl, 
   const uint64_t pol_keep = l2_policy_evict_last(), pol_drop = l2_policy_evict_first();
   int it = 0;
   opd_walk(p, cid, ncl, [&](int q, int j, int pass) -> bool {
+    q = (int)SPEC_CHECKED(q, (long long)p.B * p.k, kSiteOpdRow);
     const int b = q / p.k, i = q - b * p.k;
     const TIn* t = static_cast<const TIn*>(p.target) + ((size_t)b * (p.k + 1) + i) * (size_t)p.V + s0;
     const TIn* d = static_cast<const TIn*>(p.draft) + ((size_t)b * p.k + i) * (size_t)p.V + s0;
@@ -603,7 +604,7 @@ __device__ void opd_bookkeeper(const OpdParams& p, OpdSmem& sm, int cid, int ncl
         // Rank 0 will need z_d[x*] for the hard-label term: load it now.
         if (rank == 0 && valid) {
           const TIn* drow = static_cast<const TIn*>(p.draft) + ((size_t)b * p.k + i) * (size_t)p.V;
-          zstar[slot] = ElemTraits<TIn>::load(drow, g.i);
+          zstar[slot] = ElemTraits<TIn>::load(drow, SPEC_CHECKED(g.i, p.V, kSiteOpdRow));
         }
         mbar_arrive(&sm.norm_ready[slot]);
         if (kVerify && rank == 0 && (vflags & kReqValid) && i < __ldg(&p.lengths[b]))
@@ -650,10 +651,11 @@ __device__ void opd_bookkeeper(const OpdParams& p, OpdSmem& sm, int cid, int ncl
     if (rank == 0 && lane == 0) {
       const float4 nr = sm.norms[slot];
       if (nr.w != 0.0f) {
-        p.x_star[q] = sm.nx[slot];
-        p.hard[q] = __fsub_rn(nr.z, zstar[slot]);
-        p.rkl[q] = inf ? INFINITY : ff_to_float(kl);
-        p.rkl_clip[q] = ff_to_float(kc);
+        const long long qo = SPEC_CHECKED(q, (long long)p.B * p.k, kSiteOpdOut);
+        p.x_star[qo] = sm.nx[slot];
+        p.hard[qo] = __fsub_rn(nr.z, zstar[slot]);
+        p.rkl[qo] = inf ? INFINITY : ff_to_float(kl);
+        p.rkl_clip[qo] = ff_to_float(kc);
       } else {
         p.x_star[q] = -1;
         p.hard[q] = p.rkl[q] = p.rkl_clip[q] = __int_as_float(0x7fc00000);

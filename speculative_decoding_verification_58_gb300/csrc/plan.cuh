@@ -236,8 +236,14 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     item(b, i, rows, sc, trow, drow);
     if (rows == 0) continue;
     const int slot = (b * p.k + i) << 1;
-    rowdesc[pos++] = make_int4(slot, __float_as_int(sc), trow, 0);
-    if (rows == 2) rowdesc[pos++] = make_int4(slot | 1, __float_as_int(sc), drow, 0);
+    const long long slots = 2LL * p.B * p.k;
+    rowdesc[SPEC_CHECKED(pos, slots, kSitePlanRowdesc)] = make_int4(slot, __float_as_int(sc), trow, 0);
+    ++pos;
+    if (rows == 2) {
+      rowdesc[SPEC_CHECKED(pos, slots, kSitePlanRowdesc)] =
+          make_int4(slot | 1, __float_as_int(sc), drow, 0);
+      ++pos;
+    }
   }
   if (tid == 0) {
     h->rows_planned = total;

@@ -258,7 +258,8 @@ cudaError_t launch_final(const DeviceInfo* d, const void* target_logits, const v
                          const int32_t* draft_tokens, const int32_t* lengths, const float* uniforms,
                          const float* temperature, int B, int k, int V, int32_t* out_tokens,
                          int32_t* num_accepted, unsigned char* ws, const WsLayout& lay,
-                         int decider_grid, unsigned flags, cudaStream_t stream, bool pdl) {
+                         int decider_grid, unsigned flags, cudaStream_t stream, bool pdl,
+                         long long rows_t, long long rows_d) {
   NvtxRange r("final_kernel");
   FinalParams fp;
   fp.target = target_logits;
@@ -276,6 +277,8 @@ cudaError_t launch_final(const DeviceInfo* d, const void* target_logits, const v
   fp.lay = lay;
   fp.sweep_grid = decider_grid;
   fp.test_late = (flags & SPEC_FLAG_TEST_LATE_SLICES) ? 1 : 0;
+  fp.rows_t = rows_t;
+  fp.rows_d = rows_d;
   const int nseg = segments_of(V);
   // Slices per request: one wave of three CTAs per SM over the batch, but at
   // least two (a request's residual pair is 1.2 MB in fp32, too much for one
@@ -298,7 +301,8 @@ template <typename TIn>
 cudaError_t launch_sweep(const DeviceInfo* d, const void* target_logits, const void* draft_logits,
                          const int32_t* draft_tokens, const float* uniforms, int B, int k, int V,
                          int nch, int ce, unsigned char* ws, const WsLayout& lay, bool early_exit,
-                         int dtype_index, cudaStream_t stream, bool pdl, int* grid_out) {
+                         int dtype_index, cudaStream_t stream, bool pdl, int* grid_out,
+                         long long rows_t, long long rows_d) {
   NvtxRange r("sweep_kernel");
   SweepParams sp;
   sp.target = target_logits;
@@ -313,6 +317,9 @@ cudaError_t launch_sweep(const DeviceInfo* d, const void* target_logits, const v
   sp.early_exit = early_exit ? 1 : 0;
   sp.ws = ws;
   sp.lay = lay;
+  sp.rows_t = rows_t;
+  sp.rows_d = rows_d;
+  sp.parts_total = 2LL * B * k * nch;
   const long long max_units = 2LL * B * k * nch;
   long long grid = (long long)d->sms * d->sweep_blocks_per_sm[dtype_index][1];
   if (grid > max_units) grid = max_units;
@@ -349,15 +356,18 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
 
   int grid = 0;
   if (record(ev, 1, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+  // Rows of the two buffers: the padded layout's, or the caller's for packed rows.
+  const long long nrt = t_start != nullptr ? rows_t : (long long)B * (k + 1);
+  const long long nrd = t_start != nullptr ? rows_d : (long long)B * k;
   if (launch_sweep<TIn>(d, target_logits, draft_logits, draft_tokens, uniforms, B, k, V, nch, ce,
                         ws, lay, (flags & SPEC_FLAG_FULL_SWEEP) == 0, dtype_index, stream, pdl,
-                        &grid) != cudaSuccess)
+                        &grid, nrt, nrd) != cudaSuccess)
     return SPEC_ERR_CUDA;
 
   if (record(ev, 2, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   if (launch_final<TIn>(d, target_logits, draft_logits, draft_tokens, lengths, uniforms,
                         temperature, B, k, V, out_tokens, num_accepted, ws, lay, grid, flags,
-                        stream, pdl) != cudaSuccess)
+                        stream, pdl, nrt, nrd) != cudaSuccess)
     return SPEC_ERR_CUDA;
   if (record(ev, 3, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
@@ -388,6 +398,9 @@ spec_status_t row_stats_typed(const void* logits, int rows, int V, const float* 
   sp.early_exit = 0;
   sp.ws = ws;
   sp.lay = lay;
+  sp.rows_t = rows;
+  sp.rows_d = rows;
+  sp.parts_total = (long long)rows * nch;
   long long grid = (long long)d->sms * d->sweep_blocks_per_sm[dtype_index][0];
   if (grid > (long long)rows * nch) grid = (long long)rows * nch;
   if (launch(sweep_kernel<TIn, false>, dim3((unsigned)grid), dim3(kSweepThreads),
@@ -532,11 +545,13 @@ spec_status_t opd_typed(const void* target, const void* draft, const int32_t* le
     // listed (none when every request is at T = 0 or 1).
     int sweep_grid = 0;
     if (launch_sweep<TIn>(d, target, draft, vf.tokens, vf.uniforms, B, k, V, nch, ce, vf.ws, lay,
-                          true, dtype_index, stream, true, &sweep_grid) != cudaSuccess)
+                          true, dtype_index, stream, true, &sweep_grid, (long long)B * (k + 1),
+                          (long long)B * k) != cudaSuccess)
       return SPEC_ERR_CUDA;
     if (launch_final<TIn>(d, target, draft, vf.tokens, lengths, vf.uniforms, vf.temperature, B, k,
                           V, vf.out_tokens, vf.num_accepted, vf.ws, lay,
-                          (int)(clusters * cs) + sweep_grid, 0u, stream, true) != cudaSuccess)
+                          (int)(clusters * cs) + sweep_grid, 0u, stream, true,
+                          (long long)B * (k + 1), (long long)B * k) != cudaSuccess)
       return SPEC_ERR_CUDA;
   }
   const int wpb = 8;
@@ -553,6 +568,42 @@ using namespace specv;
 extern "C" {
 
 int spec_abi_version(void) { return SPEC_VERIFY_ABI_VERSION; }
+
+int spec_debug_build(void) {
+#ifdef SPEC_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+spec_status_t spec_debug_checks(int32_t* failures, int32_t* first_site, int reset, void* stream) {
+  int32_t f = 0, site = 0;
+#ifdef SPEC_DEBUG
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyFromSymbolAsync(&f, g_debug_failures, sizeof f, 0, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaMemcpyFromSymbolAsync(&site, g_debug_site, sizeof site, 0, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (reset) {
+    const int32_t zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_debug_failures, &zero, sizeof zero, 0, cudaMemcpyHostToDevice,
+                                s) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_debug_site, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+  }
+#else
+  (void)reset;
+  (void)stream;
+#endif
+  if (failures) *failures = f;
+  if (first_site) *first_site = site;
+  return SPEC_OK;
+}
 
 const char* spec_status_string(spec_status_t s) {
   switch (s) {

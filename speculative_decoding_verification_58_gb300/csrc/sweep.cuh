@@ -38,6 +38,8 @@ struct SweepParams {
   const float* uniforms;     // [B, k+1]
   int B, k, V, nch, chunk_elems;
   int early_exit;
+  long long rows_t, rows_d;  // rows of the target and draft buffers (range checks)
+  long long parts_total;     // partial slots in the workspace (range checks)
   unsigned char* ws;
   WsLayout lay;
 };
@@ -144,7 +146,9 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
   };
   auto describe = [&](int base, int want) {
     int4 rd = make_int4(-1, 0, 0, 0);
-    if (lane < want && base + lane < units_total) rd = __ldcg(&rowdesc[(base + lane) / p.nch]);
+    if (lane < want && base + lane < units_total)
+      rd = __ldcg(&rowdesc[SPEC_CHECKED((base + lane) / p.nch, units_total / p.nch,
+                                        kSiteSweepRowdesc)]);
     return rd;
   };
   auto check = [&](int4 rd) {  // first known rejection of the unit's request, or k
@@ -193,8 +197,10 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
       if (lane == 0) {
         const int chunk = uu - (uu / p.nch) * p.nch;
         // The descriptor's row is absolute within its buffer (target or draft).
-        const TIn* rowp = static_cast<const TIn*>((kVerify && (slot & 1)) ? p.draft : p.target) +
-                          (size_t)lrow * (size_t)p.V;
+        const bool drow = kVerify && (slot & 1);
+        const TIn* rowp =
+            static_cast<const TIn*>(drow ? p.draft : p.target) +
+            (size_t)SPEC_CHECKED(lrow, drow ? p.rows_d : p.rows_t, kSiteSweepRow) * (size_t)p.V;
         const bool greedy = (sc == 0.0f);
         // Element range of the chunk and its 16-byte aligned core.
         const int e0 = chunk * p.chunk_elems;
@@ -327,7 +333,9 @@ __device__ void sweep_producer_big(const SweepParams& p, SweepSmem& sm, WsHeader
     return true;
   };
   auto describe = [&](int u) {
-    return u < units_total ? __ldcg(&rowdesc[u / p.nch]) : make_int4(-1, 0, 0, 0);
+    return u < units_total
+               ? __ldcg(&rowdesc[SPEC_CHECKED(u / p.nch, units_total / p.nch, kSiteSweepRowdesc)])
+               : make_int4(-1, 0, 0, 0);
   };
 
   // The CTA's first unit is unit blockIdx.x, taken without a claim so that
@@ -351,8 +359,10 @@ __device__ void sweep_producer_big(const SweepParams& p, SweepSmem& sm, WsHeader
       ui = bi - ub * p.k;
     }
     // The descriptor's row is absolute within its buffer (target or draft).
-    const TIn* rowp = static_cast<const TIn*>((kVerify && (slot & 1)) ? p.draft : p.target) +
-                      (size_t)rd.z * (size_t)p.V;
+    const bool drow = kVerify && (slot & 1);
+    const TIn* rowp =
+        static_cast<const TIn*>(drow ? p.draft : p.target) +
+        (size_t)SPEC_CHECKED(rd.z, drow ? p.rows_d : p.rows_t, kSiteSweepRow) * (size_t)p.V;
     const bool greedy = (sc == 0.0f);
     // Element range of the chunk and its 16-byte aligned core.
     const int e0 = chunk * p.chunk_elems;
@@ -455,6 +465,7 @@ template <typename TIn>
 __device__ __noinline__ void decide_position(const SweepParams& p, int bi, bool greedy, float sc,
                                              int x, float u_i, int2 rb, bool dry) {
   const int lane = threadIdx.x & 31;
+  if (!dry) bi = (int)SPEC_CHECKED(bi, (long long)p.B * p.k, kSiteDecide);
   const int b = bi / p.k;
   const int i = bi - b * p.k;
   const Partial* parts = reinterpret_cast<const Partial*>(p.ws + p.lay.partials);
@@ -478,10 +489,14 @@ __device__ __noinline__ void decide_position(const SweepParams& p, int bi, bool 
     // The gathers of z_t[x] and z_d[x] go out first and overlap the partial
     // loads.  Target chunks then draft chunks: the two slots are adjacent.
     // The dry run gathers from the workspace instead, which always exists.
-    const TIn* trow = dry ? reinterpret_cast<const TIn*>(p.ws + p.lay.warm)
-                          : static_cast<const TIn*>(p.target) + ((size_t)rb.x + i) * (size_t)p.V;
-    const TIn* drow = dry ? reinterpret_cast<const TIn*>(p.ws + p.lay.warm)
-                          : static_cast<const TIn*>(p.draft) + ((size_t)rb.y + i) * (size_t)p.V;
+    const TIn* trow =
+        dry ? reinterpret_cast<const TIn*>(p.ws + p.lay.warm)
+            : static_cast<const TIn*>(p.target) +
+                  (size_t)SPEC_CHECKED((long long)rb.x + i, p.rows_t, kSiteSweepRow) * (size_t)p.V;
+    const TIn* drow =
+        dry ? reinterpret_cast<const TIn*>(p.ws + p.lay.warm)
+            : static_cast<const TIn*>(p.draft) +
+                  (size_t)SPEC_CHECKED((long long)rb.y + i, p.rows_d, kSiteSweepRow) * (size_t)p.V;
     // A token out of range (the final pass turns its request into -1) reads
     // element 0 instead and counts as a row without mass.
     const bool x_ok = (unsigned)x < (unsigned)p.V;
@@ -700,13 +715,17 @@ __device__ void sweep_bookkeeper(const SweepParams& p, SweepSmem& sm, WsHeader* 
       out_m = a.m;
       out_aux = __float_as_uint(a.s);
     }
-    if (lane == 0) store_partial(&parts[meta.part], out_m, out_aux);
+    if (lane == 0)
+      store_partial(&parts[SPEC_CHECKED(meta.part, p.parts_total, kSiteSweepPartial)], out_m,
+                    out_aux);
 
     if (kVerify) {
       // Count this chunk of (b, i); the CTA that brings the count to its
       // total decides.
       int old = 0;
-      if (lane == 0) old = atomicAdd(&done[meta.slot >> 1], 1);
+      if (lane == 0)
+        old = atomicAdd(&done[SPEC_CHECKED(meta.slot >> 1, (long long)p.B * p.k, kSiteSweepCount)],
+                        1);
       resolve_pending();
       pend_bi = meta.slot >> 1;
       pend_old = old;

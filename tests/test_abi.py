@@ -125,3 +125,18 @@ def test_d3d_select_host_checks(lib):
     assert call(pos=None) == sv.SPEC_ERR_INVALID_ARG
     assert call(nxt=18) == sv.SPEC_ERR_INVALID_ARG
     assert call(hits=18) == sv.SPEC_ERR_INVALID_ARG
+
+
+def test_range_checking_build_exports_the_same_symbols(lib):
+    # The -DSPEC_DEBUG build sits beside the release library: same entry
+    # points, and it says which one it is.
+    from speculative_decoding_verification_58_gb300 import make_lib
+    dbg = ctypes.CDLL(make_lib.LIB_DEBUG)
+    for name in declared_functions():
+        assert hasattr(dbg, name), name
+    assert dbg.spec_debug_build() == 1
+    assert lib.spec_debug_build() == 0
+    # A release build has no checks to report and touches no device for it.
+    f, site = ctypes.c_int32(7), ctypes.c_int32(7)
+    assert lib.spec_debug_checks(ctypes.addressof(f), ctypes.addressof(site), 1, None) == sv.SPEC_OK
+    assert (f.value, site.value) == (0, 0)
