@@ -885,26 +885,27 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
     const float u_t = (T != 0.0f && t <= L && t <= p.k)
                           ? __ldg(&p.uniforms[(size_t)b * (p.k + 1) + t])
                           : 0.0f;
+    // The request's flags are the plan's (fixed for the round).  The first
+    // look at the decision word goes out with the input loads above (its
+    // acquire holds back only the loads after it); the wait then polls the
+    // word alone.  A row without mass is recorded in bad_bits before the
+    // decision that releases it, so bad_bits is read once, after the acquire
+    // that ends the wait.
+    int f = __ldcg(reinterpret_cast<const int32_t*>(p.ws + p.lay.flags) + b);
+    unsigned long long st =
+        ld_acquire_u64(reinterpret_cast<const unsigned long long*>(p.ws + p.lay.state) + b);
     if (t == L) sh.uL = u_t;  // the final token's uniform (0 at T = 0)
     const bool in_ok = (t >= L || (x_t >= 0 && x_t < p.V)) &&
                        (T == 0.0f || t > L || (u_t >= 0.0f && u_t < 1.0f));  // NaN fails
     const bool inputs_ok = __all_sync(0xffffffffu, in_ok);
-    int f = 0;
     uint32_t dec = 0, acc = 0, bad = 0;
     bool late = false;
     // Testing aid: this slice never sees its outcome and gives up after a
     // short wait, exercising the path a real timeout takes.
     const bool never = p.test_late && part != 0;
     const unsigned long long limit = never ? kTestLateLimitNs : kWaitLimitNs;
-    // The request's flags are the plan's (fixed for the round); the wait
-    // polls the decision word alone.  A row without mass is recorded in
-    // bad_bits before the decision that releases it, so bad_bits is read
-    // once, after the acquire that ends the wait.
-    f = __ldcg(reinterpret_cast<const int32_t*>(p.ws + p.lay.flags) + b);
     const unsigned long long t0 = global_ns();
     while (inputs_ok && (f & kReqValid)) {  // otherwise no outcome to wait for
-      const unsigned long long st =
-          ld_acquire_u64(reinterpret_cast<const unsigned long long*>(p.ws + p.lay.state) + b);
       dec = (uint32_t)st;
       acc = (uint32_t)(st >> 32);
       if (outcome_known_word(st, L) && !never) break;
@@ -913,6 +914,7 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
         break;
       }
       __nanosleep(128);
+      st = ld_acquire_u64(reinterpret_cast<const unsigned long long*>(p.ws + p.lay.state) + b);
     }
     bad = __ldcg(reinterpret_cast<const uint32_t*>(p.ws + p.lay.bad_bits) + b);
     const float4* pos_c = reinterpret_cast<const float4*>(p.ws + p.lay.pos_c);
