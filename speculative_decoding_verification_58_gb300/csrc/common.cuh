@@ -416,8 +416,8 @@ __device__ __forceinline__ float vec_elem(const uint4& v, int e) {
 // Softmax accumulation of a batch: one max, at most one rescale, then
 // independent packed FMAs, one ex2 per element and four packed accumulators.
 template <typename TIn, int N>
-__device__ __forceinline__ void soft_stage(SoftAcc& a, const uint4 (&v)[N], float sc) {
-  const float gm = batch_max<TIn>(v);
+__device__ __forceinline__ void soft_stage(SoftAcc& a, const uint4 (&v)[N], float sc,
+                                           float gm) {
   if (gm > a.m) {
     const float nms = __fmul_rn(gm, sc);
     a.s = __fmul_rn(a.s, ex2(__fsub_rn(a.ms, nms)));
@@ -447,22 +447,43 @@ __device__ __forceinline__ void soft_stage(SoftAcc& a, const uint4 (&v)[N], floa
   a.s = __fadd_rn(a.s, __fadd_rn(t2.x, t2.y));
 }
 
+// The same with the batch's max computed here.
+template <typename TIn, int N>
+__device__ __forceinline__ void soft_stage(SoftAcc& a, const uint4 (&v)[N], float sc) {
+  soft_stage<TIn>(a, v, sc, batch_max<TIn>(v));
+}
+
 // Argmax of a batch: one max; only when it beats the running best, a scan in
 // index order for its first occurrence.  `first` is the element index of
 // vector 0, vectors are `stride` elements apart.
 template <typename TIn, int N>
-__device__ __forceinline__ void arg_stage(ArgAcc& a, const uint4 (&v)[N], int first, int stride) {
+__device__ __forceinline__ void arg_stage(ArgAcc& a, const uint4 (&v)[N], int first, int stride,
+                                          float gm) {
   constexpr int EPV = ElemTraits<TIn>::kPerVec;
-  const float gm = batch_max<TIn>(v);
   if (!(gm > a.v)) return;
-  int found = INT32_MAX;
+  // The first vector whose max is gm (its elements come before the next
+  // vector's), then its first element equal to gm: the lowest index.
+  int t_hit = -1;
 #pragma unroll
-  for (int t = N - 1; t >= 0; --t)
+  for (int t = N - 1; t >= 0; --t) {
+    const uint4 one[1] = {v[t]};
+    if (batch_max<TIn>(one) == gm) t_hit = t;
+  }
+  uint4 w = v[0];
 #pragma unroll
-    for (int e = EPV - 1; e >= 0; --e)
-      if (vec_elem<TIn>(v[t], e) == gm) found = first + t * stride + e;
+  for (int t = 1; t < N; ++t)
+    if (t == t_hit) w = v[t];
+  int e_hit = 0;
+#pragma unroll
+  for (int e = EPV - 1; e >= 0; --e)
+    if (vec_elem<TIn>(w, e) == gm) e_hit = e;
   a.v = gm;
-  a.i = found;
+  a.i = t_hit >= 0 ? first + t_hit * stride + e_hit : INT32_MAX;
+}
+
+template <typename TIn, int N>
+__device__ __forceinline__ void arg_stage(ArgAcc& a, const uint4 (&v)[N], int first, int stride) {
+  arg_stage<TIn>(a, v, first, stride, batch_max<TIn>(v));
 }
 
 // Elements must be offered in increasing index order within one accumulator.

@@ -349,15 +349,20 @@ __device__ void opd_consumers(const OpdParams& p, OpdSmem& sm, int cid, int ncl,
         // rescale per row, then independent exponentials; vectors past the
         // stage's end are -inf.
         const int base = s0 + I.e0;
+        // Only a stage that ends a part is short: the others skip the padding.
+        if (nvec < kOpdVecPerThread * kOpdNC) {
 #pragma unroll
-        for (int u = 0; u < kOpdVecPerThread; ++u) {
-          if (ctid + u * kOpdNC >= nvec) {
-            vt[u] = neg_inf_vec<TIn>();
-            vd[u] = neg_inf_vec<TIn>();
+          for (int u = 0; u < kOpdVecPerThread; ++u) {
+            if (ctid + u * kOpdNC >= nvec) {
+              vt[u] = neg_inf_vec<TIn>();
+              vd[u] = neg_inf_vec<TIn>();
+            }
           }
         }
-        arg_stage<TIn>(ag, vt, base + ctid * EPV, kOpdNC * EPV);
-        soft_stage<TIn>(at, vt, kLog2e);
+        // One max of the target batch serves its argmax and its softmax.
+        const float gmt = batch_max<TIn>(vt);
+        arg_stage<TIn>(ag, vt, base + ctid * EPV, kOpdNC * EPV, gmt);
+        soft_stage<TIn>(at, vt, kLog2e, gmt);
         soft_stage<TIn>(ad, vd, kLog2e);
         if (ctid < rem) {
           soft_add1(at, xt, kLog2e);
