@@ -762,7 +762,7 @@ __device__ __forceinline__ long long spec_debug_index(long long i, long long n, 
 #ifdef SPEC_DEBUG
 #define SPEC_CHECKED(i, n, site) spec_debug_index((long long)(i), (long long)(n), (site))
 #else
-#define SPEC_CHECKED(i, n, site) (i)
+#define SPEC_CHECKED(i, n, site) ((void)(n), (i))
 #endif
 
 // ---------------------------------------------------------------------------
