@@ -59,7 +59,8 @@ struct WsHeader {
   unsigned long long final_bytes;
   int32_t sweep_exited;     // sweep CTAs that have finished
   int32_t final_ctas_done;  // final-pass CTAs that have finished
-  int32_t pad[44];
+  int32_t row_kinds;        // rows in the sweep's list: 1 greedy, 2 sampling (bits)
+  int32_t pad[43];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte block");
 
@@ -578,14 +579,34 @@ __device__ __forceinline__ FF ff_shfl_xor(FF a, int off) {
 
 // Sum over the aligned groups of 2^levels lanes, in a fixed butterfly order
 // (every lane of a group gets the same bits).
+// One butterfly level: both partners add (lower lane's value, upper lane's
+// value) in that order, so they compute the same bits.  The operands are
+// selected first, so that the warp runs one addition, not one per branch.
+__device__ __forceinline__ FF ff_level_add(FF x, int off) {
+  const FF y = ff_shfl_xor(x, off);
+  const bool upper = (threadIdx.x & off) != 0;
+  const FF a = {upper ? y.hi : x.hi, upper ? y.lo : x.lo};
+  const FF b = {upper ? x.hi : y.hi, upper ? x.lo : y.lo};
+  return ff_add(a, b);
+}
+
 __device__ __forceinline__ FF group_sum_ff(FF x, int levels) {
-  for (int l = 0; l < levels; ++l) {
-    const int off = 1 << l;
-    const FF y = ff_shfl_xor(x, off);
-    // Combine in lane order so that both partners compute the same value.
-    x = (threadIdx.x & off) ? ff_add(y, x) : ff_add(x, y);
-  }
+#pragma unroll
+  for (int l = 0; l < 5; ++l)
+    if (l < levels) x = ff_level_add(x, 1 << l);
   return x;
+}
+
+// Two independent sums over the same lanes, level by level (their chains
+// interleave).
+__device__ __forceinline__ void group_sum_ff2(FF& x, FF& z, int levels) {
+#pragma unroll
+  for (int l = 0; l < 5; ++l) {
+    if (l < levels) {
+      x = ff_level_add(x, 1 << l);
+      z = ff_level_add(z, 1 << l);
+    }
+  }
 }
 
 __device__ __forceinline__ float group_max(float x, int levels) {
@@ -909,8 +930,8 @@ __device__ __forceinline__ void pair_log2_normalisers(const Partial* parts, int 
     const float md = __shfl_sync(0xffffffffu, group_max(is_d ? mc : -FLT_MAX, lv), 0);
     const float msT = __fmul_rn(mt, sc), msD = __fmul_rn(md, sc);
     const float term = (is_t || is_d) ? chunk_term(mc, ac, sc, is_t ? msT : msD) : 0.0f;
-    FF St = group_sum_ff(FF{is_t ? term : 0.0f, 0.0f}, lv);
-    FF Sd = group_sum_ff(FF{is_d ? term : 0.0f, 0.0f}, lv);
+    FF St = {is_t ? term : 0.0f, 0.0f}, Sd = {is_d ? term : 0.0f, 0.0f};
+    group_sum_ff2(St, Sd, lv);
     St = FF{__shfl_sync(0xffffffffu, St.hi, 0), __shfl_sync(0xffffffffu, St.lo, 0)};
     Sd = FF{__shfl_sync(0xffffffffu, Sd.hi, 0), __shfl_sync(0xffffffffu, Sd.lo, 0)};
     const bool late = __any_sync(0xffffffffu, late1);
@@ -951,8 +972,7 @@ __device__ __forceinline__ void pair_log2_normalisers(const Partial* parts, int 
     if (e < nch) St = ff_add_f(St, chunk_term(m[j], a[j], sc, msT));
     else if (e < n2) Sd = ff_add_f(Sd, chunk_term(m[j], a[j], sc, msD));
   }
-  St = warp_sum_ff(St);
-  Sd = warp_sum_ff(Sd);
+  group_sum_ff2(St, Sd, 5);
   late = __any_sync(0xffffffffu, late);
   *timed_out = late;
   *ok_t = row_normaliser_from(msT, ff_to_float(St), ct) && !late;

@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   // (at most one request per thread).
   __shared__ __align__(16) uint32_t words[SPEC_MAX_B / 32];
   __shared__ int warp_tot[33];
+  __shared__ int row_kinds;
   const int tid = threadIdx.x;
   const bool small = p.B <= kPlanThreads;
   uint32_t* bad_mask = words;
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   }
   if (!small)
     for (int w = tid; w < ((p.B + 31) >> 5); w += kPlanThreads) bad_mask[w] = 0u;
+  if (tid == 0) row_kinds = 0;
 
   // Per-call state that does not depend on the inputs, with coalesced
   // stores: decision masks, chunk and final-pass counters to zero, every
@@ -186,8 +188,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       atomicMin(&h->first_bad, b);
       atomicCAS(&h->status, SPEC_OK, SPEC_ERR_BAD_INPUT);
     }
+    const bool listed = !bad && !(p.skip_t01 && (T == 0.0f || T == 1.0f));
+    if (listed) atomicOr(&row_kinds, T == 0.0f ? 1 : 2);
     if (small) {
-      const bool listed = !bad && !(p.skip_t01 && (T == 0.0f || T == 1.0f));
       req[b] = PlanReq{L, listed ? (T == 0.0f ? 1 : 2) : 0, T == 0.0f ? 0.0f : softmax_scale(T),
                        rb.x, rb.y};
     } else if (bad) {
@@ -246,6 +249,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     }
   }
   if (tid == 0) {
+    h->row_kinds = row_kinds;
     h->rows_planned = total;
     h->units_total = total * p.nch;
   }

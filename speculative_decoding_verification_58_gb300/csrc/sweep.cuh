@@ -108,12 +108,24 @@ __device__ __forceinline__ void sweep_abort(WsHeader* h, SweepSmem& sm) {
 // ---------------------------------------------------------------------------
 constexpr int kClaim = 4;
 
+// The descriptor of a CTA's first unit (unit blockIdx.x), loaded before the
+// unit count is known so that the two loads travel together: the grid has
+// at most one CTA per unit slot, so the index lies inside the descriptor
+// array; the caller uses the descriptor only if the unit exists.
+__device__ __forceinline__ int4 first_descriptor(const SweepParams& p, const int4* rowdesc) {
+  return __ldcg(&rowdesc[SPEC_CHECKED((int)blockIdx.x / p.nch, p.parts_total / p.nch,
+                                      kSiteSweepRowdesc)]);
+}
+
 template <typename TIn, bool kVerify>
 __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h) {
   using Tr = ElemTraits<TIn>;
   const int lane = threadIdx.x & 31;
   const int4* rowdesc = reinterpret_cast<const int4*>(p.ws + p.lay.rowdesc);
   const int32_t* first_reject = reinterpret_cast<const int32_t*>(p.ws + p.lay.first_reject);
+  // The first unit's descriptor goes out with the unit count (see
+  // first_descriptor).
+  const int4 rd_first = first_descriptor(p, rowdesc);
   const int units_total = __ldcg(&h->units_total);
   const int small_after = units_total - 4 * kClaim * (int)gridDim.x;
   volatile int* abort_flag = &sm.abort_flag;
@@ -162,7 +174,7 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
 
   int wantC = 1;
   int baseC = (int)blockIdx.x;
-  int4 rdC = describe(baseC, wantC);
+  int4 rdC = (lane == 0 && baseC < units_total) ? rd_first : make_int4(-1, 0, 0, 0);
   // No decision can precede a CTA's first unit by much; the check before
   // each stage still applies to it.
   int frC = INT32_MAX;
@@ -316,6 +328,7 @@ __device__ void sweep_producer_big(const SweepParams& p, SweepSmem& sm, WsHeader
   if ((threadIdx.x & 31) != 0) return;
   const int4* rowdesc = reinterpret_cast<const int4*>(p.ws + p.lay.rowdesc);
   const int32_t* first_reject = reinterpret_cast<const int32_t*>(p.ws + p.lay.first_reject);
+  const int4 rd_first = first_descriptor(p, rowdesc);
   const int units_total = __ldcg(&h->units_total);
   volatile int* abort_flag = &sm.abort_flag;
   const bool recheck = kVerify && p.early_exit;
@@ -342,7 +355,7 @@ __device__ void sweep_producer_big(const SweepParams& p, SweepSmem& sm, WsHeader
   // the first copy waits for no round trip; the counter hands out the units
   // after the grid's first ones.
   int nxt = (int)blockIdx.x;
-  int4 nrd = describe(nxt);
+  int4 nrd = nxt < units_total ? rd_first : make_int4(-1, 0, 0, 0);
   bool first_unit = true;
   while (nxt < units_total) {
     const int uu = nxt;
@@ -658,10 +671,11 @@ __device__ void sweep_bookkeeper(const SweepParams& p, SweepSmem& sm, WsHeader* 
   float pend_sc = 0.0f, pend_u = 0.0f;
   int2 pend_rb = make_int2(0, 0);
   if (kVerify) {
-    // Run both decision paths once, without effect, while the first units
-    // are still streaming in (see decide_position).
-    decide_position<TIn>(p, 0, false, 1.0f, 0, 0.5f, make_int2(0, 0), true);
-    decide_position<TIn>(p, 0, true, 0.0f, 0, 0.5f, make_int2(0, 0), true);
+    // Run the decision paths the round's rows need once, without effect,
+    // while the first units are still streaming in (see decide_position).
+    const int kinds = __ldcg(&h->row_kinds);
+    if (kinds & 2) decide_position<TIn>(p, 0, false, 1.0f, 0, 0.5f, make_int2(0, 0), true);
+    if (kinds & 1) decide_position<TIn>(p, 0, true, 0.0f, 0, 0.5f, make_int2(0, 0), true);
   }
   auto resolve_pending = [&]() {
     if (!kVerify || pend_bi < 0) return;
