@@ -761,12 +761,44 @@ class OurArm:
         same = bool(np.array_equal(h_out.numpy(), self.gpu_out) and
                     np.array_equal(h_n.numpy(), self.gpu_n))
         packed_s = timed(packed_step)
+
+        # The packed rows stay in pinned host memory and the kernels read them
+        # over the CPU-GPU link themselves: only the rows the round reads
+        # cross it (early exit spares the rest); the small per-request arrays
+        # are copied as before.
+        small = ("target_row_start", "draft_row_start", "draft_tokens", "lengths", "uniforms",
+                 "temperature")
+
+        def direct_step():
+            for key in small:
+                dp[key].copy_(hp[key], non_blocking=True)
+            sv.spec_verify_packed(target_rows=hp["target_rows"], draft_rows=hp["draft_rows"],
+                                  **{key: dp[key] for key in small}, workspace=self.ws,
+                                  out_tokens=self.out, num_accepted=self.nacc, stream=self.stream)
+            h_out.copy_(self.out, non_blocking=True)
+            h_n.copy_(self.nacc, non_blocking=True)
+            self.stream.synchronize()
+
+        direct_step()
+        same_direct = bool(np.array_equal(h_out.numpy(), self.gpu_out) and
+                           np.array_equal(h_n.numpy(), self.gpu_n))
+        rep = sv.spec_verify_report(self.ws, stream=self.stream)
+        read = int(rep.sweep_bytes) + int(rep.final_bytes)
+        h2d_direct = read + sum(hp[key].numel() * hp[key].element_size() for key in small)
+        direct_s = timed(direct_step)
         del dp
-        return ({"value": self.world / packed_s, "unit": "rounds/s",
-                 "h2d_bytes_per_step": h2d_packed, "d2h_bytes_per_step": d2h,
-                 "layout": "packed (rows 0..L_b of each request)", "same_outputs": same},
-                {"value": self.world / padded_s, "unit": "rounds/s", "h2d_bytes_per_step": h2d,
-                 "d2h_bytes_per_step": d2h, "layout": "padded [B, k+1, V] / [B, k, V]"})
+        copy_leg = {"value": self.world / packed_s, "unit": "rounds/s",
+                    "h2d_bytes_per_step": h2d_packed, "d2h_bytes_per_step": d2h,
+                    "layout": "packed (rows 0..L_b of each request) copied to the device",
+                    "same_outputs": same}
+        direct_leg = {"value": self.world / direct_s, "unit": "rounds/s",
+                      "h2d_bytes_per_step": h2d_direct, "d2h_bytes_per_step": d2h,
+                      "layout": "packed rows in pinned host memory, read by the kernels over "
+                                "the CPU-GPU link (only the rows the round reads)",
+                      "logit_bytes_read": read, "same_outputs": same_direct}
+        padded_leg = {"value": self.world / padded_s, "unit": "rounds/s", "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h, "layout": "padded [B, k+1, V] / [B, k, V]"}
+        return direct_leg, copy_leg, padded_leg
 
     def cpu_baseline(self, result, round_bytes):
         """The oracle on one host core for about ten seconds of full rounds, and the
@@ -833,7 +865,12 @@ class OurArm:
         opd = None if args.no_opd else self.opd_leg()
         opd_fused = None if args.no_opd else self.opd_fused_leg()
         d3d = None if args.no_d3d else self.d3d_leg()
-        e2e, e2e_padded = self.e2e_legs()
+        e2e_direct, e2e_copy, e2e_padded = self.e2e_legs()
+        # The end-to-end figure is the library's path for host-resident logits:
+        # the kernels read the pinned rows over the link (the copy-first
+        # path is reported beside it; a direct run whose outputs differed
+        # from the device run would not count).
+        e2e = e2e_direct if e2e_direct["same_outputs"] else e2e_copy
         clocks = sampler.stop()
         per_workload = (self.workload_legs(hbm_peak)
                         if self.world == 1 and not args.no_workloads else None)
@@ -863,6 +900,8 @@ class OurArm:
             "round_bytes": {"sweep": rep.sweep_bytes, "final": rep.final_bytes},
             "e2e": e2e,
             "e2e_padded": e2e_padded,
+            "e2e_direct": e2e_direct,
+            "e2e_copy": e2e_copy,
             "gpu_launches": 3 * args.steps,
             "clocks": clocks,
         }

@@ -220,6 +220,19 @@ def _need(t, name, dtype, shape, device):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _need_logits(t, name, dtype, shape, device):
+    """Logits on ``device``, or in pinned host memory, which the kernels then
+    read themselves over the CPU-GPU link (no copy; early exit also spares
+    the link the rows it skips)."""
+    if t.device.type == "cpu":
+        if not t.is_pinned():
+            raise ValueError(f"{name} is in pageable host memory: pin it (pin_memory()) or move it "
+                             f"to {device}")
+        _need(t, name, dtype, shape, t.device)
+    else:
+        _need(t, name, dtype, shape, device)
+
+
 def spec_verify_workspace_bytes(B: int, k: int, V: int) -> int:
     return int(lib().spec_verify_workspace_bytes(B, k, V))
 
@@ -251,10 +264,10 @@ def spec_verify(target_logits, draft_logits, draft_tokens, lengths, uniforms, te
     torch = _torch()
     B, k1, V = target_logits.shape
     k = k1 - 1
-    dev = target_logits.device
+    dev = draft_tokens.device
     dt = _dtype_code(target_logits)
-    _need(target_logits, "target_logits", target_logits.dtype, (B, k + 1, V), dev)
-    _need(draft_logits, "draft_logits", target_logits.dtype, (B, k, V), dev)
+    _need_logits(target_logits, "target_logits", target_logits.dtype, (B, k + 1, V), dev)
+    _need_logits(draft_logits, "draft_logits", target_logits.dtype, (B, k, V), dev)
     _need(draft_tokens, "draft_tokens", torch.int32, (B, k), dev)
     _need(lengths, "lengths", torch.int32, (B,), dev)
     _need(uniforms, "uniforms", torch.float32, (B, k + 1), dev)
@@ -295,11 +308,11 @@ def spec_verify_packed(target_rows, draft_rows, target_row_start, draft_row_star
     torch = _torch()
     rows_t, V = target_rows.shape
     B, k = draft_tokens.shape
-    dev = target_rows.device
+    dev = draft_tokens.device
     dt = _dtype_code(target_rows)
     rows_d = draft_rows.shape[0]
-    _need(target_rows, "target_rows", target_rows.dtype, (rows_t, V), dev)
-    _need(draft_rows, "draft_rows", target_rows.dtype, (rows_d, V), dev)
+    _need_logits(target_rows, "target_rows", target_rows.dtype, (rows_t, V), dev)
+    _need_logits(draft_rows, "draft_rows", target_rows.dtype, (rows_d, V), dev)
     _need(target_row_start, "target_row_start", torch.int32, (B,), dev)
     _need(draft_row_start, "draft_row_start", torch.int32, (B,), dev)
     _need(draft_tokens, "draft_tokens", torch.int32, (B, k), dev)
@@ -342,10 +355,10 @@ class Verifier:
         torch = _torch()
         B, k1, V = target_logits.shape
         k = k1 - 1
-        dev = target_logits.device
+        dev = draft_tokens.device
         dt = _dtype_code(target_logits)
-        _need(target_logits, "target_logits", target_logits.dtype, (B, k + 1, V), dev)
-        _need(draft_logits, "draft_logits", target_logits.dtype, (B, k, V), dev)
+        _need_logits(target_logits, "target_logits", target_logits.dtype, (B, k + 1, V), dev)
+        _need_logits(draft_logits, "draft_logits", target_logits.dtype, (B, k, V), dev)
         _need(draft_tokens, "draft_tokens", torch.int32, (B, k), dev)
         _need(lengths, "lengths", torch.int32, (B,), dev)
         _need(uniforms, "uniforms", torch.float32, (B, k + 1), dev)
@@ -390,10 +403,10 @@ def spec_verify_static(target_logits, draft_logits, draft_tokens, lengths, unifo
     torch = _torch()
     B, k1, V = target_logits.shape
     k = k1 - 1
-    dev = target_logits.device
+    dev = draft_tokens.device
     dt = _dtype_code(target_logits)
-    _need(target_logits, "target_logits", target_logits.dtype, (B, k + 1, V), dev)
-    _need(draft_logits, "draft_logits", target_logits.dtype, (B, k, V), dev)
+    _need_logits(target_logits, "target_logits", target_logits.dtype, (B, k + 1, V), dev)
+    _need_logits(draft_logits, "draft_logits", target_logits.dtype, (B, k, V), dev)
     _need(draft_tokens, "draft_tokens", torch.int32, (B, k), dev)
     _need(lengths, "lengths", torch.int32, (B,), dev)
     _need(uniforms, "uniforms", torch.float32, (B, k + 1), dev)

@@ -40,6 +40,7 @@ struct FinalParams {
   int sweep_grid;  // CTAs of the sweep grid this pass follows
   int test_late;   // testing aid: slices other than the first give up waiting (see below)
   long long rows_t, rows_d;  // rows of the target and draft buffers (range checks)
+  int direct;      // rows in pinned host memory: slices load them, no bulk copies
   int32_t* out_tokens;
   int32_t* num_accepted;
   unsigned char* ws;
@@ -1027,8 +1028,9 @@ __device__ __forceinline__ void final_body(const FinalParams& p, FinalShared& sh
       if (threadIdx.x == 0) __stcg(&slice_out[part], make_float2(a.v, __int_as_float(a.i)));
     } else {
       long long dsum = 0;
-      // Aligned rows stream through shared memory; others load directly.
-      if (vec_ok && ((size_t)p.V * sizeof(TIn)) % 16 == 0) {
+      // Aligned rows in device memory stream through shared memory; others
+      // (and rows in host memory) are loaded directly.
+      if (vec_ok && ((size_t)p.V * sizeof(TIn)) % 16 == 0 && !p.direct) {
         if (!slice_records_staged(trow, drow, p.V, ms, bonus, s_lo, s_hi, rec,
                                   reinterpret_cast<unsigned char*>(rec_sm), fr, &dsum)) {
           gave_up = true;  // block-uniform: the staged pass ends in a block-wide vote

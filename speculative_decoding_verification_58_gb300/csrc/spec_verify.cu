@@ -259,7 +259,7 @@ cudaError_t launch_final(const DeviceInfo* d, const void* target_logits, const v
                          const float* temperature, int B, int k, int V, int32_t* out_tokens,
                          int32_t* num_accepted, unsigned char* ws, const WsLayout& lay,
                          int decider_grid, unsigned flags, cudaStream_t stream, bool pdl,
-                         long long rows_t, long long rows_d) {
+                         long long rows_t, long long rows_d, bool direct = false) {
   NvtxRange r("final_kernel");
   FinalParams fp;
   fp.target = target_logits;
@@ -279,6 +279,7 @@ cudaError_t launch_final(const DeviceInfo* d, const void* target_logits, const v
   fp.test_late = (flags & SPEC_FLAG_TEST_LATE_SLICES) ? 1 : 0;
   fp.rows_t = rows_t;
   fp.rows_d = rows_d;
+  fp.direct = direct ? 1 : 0;
   const int nseg = segments_of(V);
   // Slices per request: one wave of three CTAs per SM over the batch, but at
   // least two (a request's residual pair is 1.2 MB in fp32, too much for one
@@ -302,7 +303,7 @@ cudaError_t launch_sweep(const DeviceInfo* d, const void* target_logits, const v
                          const int32_t* draft_tokens, const float* uniforms, int B, int k, int V,
                          int nch, int ce, unsigned char* ws, const WsLayout& lay, bool early_exit,
                          int dtype_index, cudaStream_t stream, bool pdl, int* grid_out,
-                         long long rows_t, long long rows_d) {
+                         long long rows_t, long long rows_d, bool direct = false) {
   NvtxRange r("sweep_kernel");
   SweepParams sp;
   sp.target = target_logits;
@@ -319,6 +320,7 @@ cudaError_t launch_sweep(const DeviceInfo* d, const void* target_logits, const v
   sp.lay = lay;
   sp.rows_t = rows_t;
   sp.rows_d = rows_d;
+  sp.direct = direct ? 1 : 0;
   sp.parts_total = 2LL * B * k * nch;
   const long long max_units = 2LL * B * k * nch;
   long long grid = (long long)d->sms * d->sweep_blocks_per_sm[dtype_index][1];
@@ -337,7 +339,7 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
                            cudaStream_t stream, unsigned flags, int dtype_index,
                            void* const* ev, const int32_t* t_start = nullptr,
                            const int32_t* d_start = nullptr, long long rows_t = 0,
-                           long long rows_d = 0) {
+                           long long rows_d = 0, bool direct = false) {
   NvtxRange r(t_start != nullptr ? "spec_verify_packed" : "spec_verify");
   DeviceInfo* d = nullptr;
   if (device_info(&d) != cudaSuccess) return SPEC_ERR_CUDA;
@@ -361,13 +363,13 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
   const long long nrd = t_start != nullptr ? rows_d : (long long)B * k;
   if (launch_sweep<TIn>(d, target_logits, draft_logits, draft_tokens, uniforms, B, k, V, nch, ce,
                         ws, lay, (flags & SPEC_FLAG_FULL_SWEEP) == 0, dtype_index, stream, pdl,
-                        &grid, nrt, nrd) != cudaSuccess)
+                        &grid, nrt, nrd, direct) != cudaSuccess)
     return SPEC_ERR_CUDA;
 
   if (record(ev, 2, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   if (launch_final<TIn>(d, target_logits, draft_logits, draft_tokens, lengths, uniforms,
                         temperature, B, k, V, out_tokens, num_accepted, ws, lay, grid, flags,
-                        stream, pdl, nrt, nrd) != cudaSuccess)
+                        stream, pdl, nrt, nrd, direct) != cudaSuccess)
     return SPEC_ERR_CUDA;
   if (record(ev, 3, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
@@ -625,6 +627,34 @@ size_t spec_verify_workspace_bytes(int B, int k, int V) {
   return ws_layout(B, k, chunks_per_row(slots, V), V).total;
 }
 
+// Where the two logits buffers live.  Pinned host memory that the GPU maps
+// (cudaHostAlloc, cudaHostRegister, torch's pin_memory) is read by the
+// kernels themselves over the CPU-GPU link, with plain loads and no bulk
+// copies ("direct"); *t and *d become the device-side addresses.  Anything
+// else is taken as device memory, as before.  Returns false if one buffer is
+// host memory and the other is not, or a host buffer is not mapped.
+static bool resolve_logits(const void** t, const void** d, bool* direct) {
+  auto host_of = [](const void* p, const void** dev) -> int {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return 0;
+    }
+    if (a.type != cudaMemoryTypeHost) return 0;
+    if (a.devicePointer == nullptr) return -1;
+    *dev = a.devicePointer;
+    return 1;
+  };
+  const void* td = *t;
+  const void* dd = *d;
+  const int ht = host_of(*t, &td), hd = host_of(*d, &dd);
+  if (ht < 0 || hd < 0 || ht != hd) return false;
+  *direct = (ht == 1);
+  *t = td;
+  *d = dd;
+  return true;
+}
+
 // Padded layout: t_start == nullptr.  Packed layout: t_start / d_start give
 // each request's first row in buffers of rows_t / rows_d rows; a draft buffer
 // of zero rows may be null (then only greedy requests are valid).
@@ -659,16 +689,18 @@ static spec_status_t verify_entry(const void* target_logits, const void* draft_l
   if (!workspace || !aligned(workspace, 256) ||
       workspace_bytes < spec_verify_workspace_bytes(B, k, V))
     return SPEC_ERR_WORKSPACE;
-  DeviceOf on_device(target_logits);
+  DeviceOf on_device(workspace);
   if (!on_device.ok()) return SPEC_ERR_CUDA;
+  bool direct = false;
+  if (!resolve_logits(&target_logits, &draft_logits, &direct)) return SPEC_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SPEC_F32)
     return verify_typed<float>(target_logits, draft_logits, draft_tokens, lengths, uniforms,
                                temperature, B, k, V, out_tokens, num_accepted, workspace, s, flags, 0,
-                               ev, t_start, d_start, rows_t, rows_d);
+                               ev, t_start, d_start, rows_t, rows_d, direct);
   return verify_typed<uint16_t>(target_logits, draft_logits, draft_tokens, lengths, uniforms,
                                 temperature, B, k, V, out_tokens, num_accepted, workspace, s, flags,
-                                1, ev, t_start, d_start, rows_t, rows_d);
+                                1, ev, t_start, d_start, rows_t, rows_d, direct);
 }
 
 spec_status_t spec_verify_packed(const void* target_rows, long long rows_t, const void* draft_rows,
@@ -941,16 +973,18 @@ extern "C" spec_status_t spec_verify_static(const void* target_logits, const voi
   // The batch must fit the fixed scratch.
   const size_t need = spec_verify_workspace_bytes(B, k, V);
   if (need == 0 || need > SPEC_STATIC_SCRATCH_BYTES) return SPEC_ERR_UNSUPPORTED;
-  DeviceOf on_device(target_logits);
+  DeviceOf on_device(num_accepted);
   if (!on_device.ok()) return SPEC_ERR_CUDA;
+  bool direct = false;
+  if (!resolve_logits(&target_logits, &draft_logits, &direct)) return SPEC_ERR_INVALID_ARG;
   void* scratch = nullptr;
   if (static_scratch(&scratch) != cudaSuccess) return SPEC_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SPEC_F32)
     return verify_typed<float>(target_logits, draft_logits, draft_tokens, lengths, uniforms,
                                temperature, B, k, V, out_tokens, num_accepted, scratch, s, 0u, 0,
-                               nullptr);
+                               nullptr, nullptr, nullptr, 0, 0, direct);
   return verify_typed<uint16_t>(target_logits, draft_logits, draft_tokens, lengths, uniforms,
                                 temperature, B, k, V, out_tokens, num_accepted, scratch, s, 0u, 1,
-                                nullptr);
+                                nullptr, nullptr, nullptr, 0, 0, direct);
 }

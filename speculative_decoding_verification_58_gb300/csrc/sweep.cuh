@@ -38,6 +38,7 @@ struct SweepParams {
   const float* uniforms;     // [B, k+1]
   int B, k, V, nch, chunk_elems;
   int early_exit;
+  int direct;                // rows in pinned host memory: no bulk copies (kFlagDirect)
   long long rows_t, rows_d;  // rows of the target and draft buffers (range checks)
   long long parts_total;     // partial slots in the workspace (range checks)
   unsigned char* ws;
@@ -46,7 +47,10 @@ struct SweepParams {
 
 // kFlagDiscard closes a unit whose request was rejected at an earlier
 // position while it streamed: its partial is neither stored nor counted.
-constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagGreedy = 4, kFlagEnd = 8, kFlagDiscard = 16;
+// kFlagDirect: the stage was not copied; the consumers load its bytes from the
+// row itself (logits in pinned host memory, read over the CPU-GPU link).
+constexpr int kFlagFirst = 1, kFlagLast = 2, kFlagGreedy = 4, kFlagEnd = 8, kFlagDiscard = 16,
+              kFlagDirect = 32;
 
 struct StageInfo {
   const void* row;  // row base (element 0)
@@ -255,7 +259,8 @@ __device__ void sweep_producer(const SweepParams& p, SweepSmem& sm, WsHeader* h)
           I.tailn = drop ? 0 : e1 - a1;
           I.sc = sc;
           I.slot = slot;
-          if (nb > 0) {
+          if (p.direct) I.flags |= kFlagDirect;
+          if (nb > 0 && !p.direct) {
             mbar_arrive_expect_tx(&sm.full[s], (uint32_t)nb);
             bulk_g2s_hint(sm.stage[s], src0 + off, (uint32_t)nb, &sm.full[s],
                       l2_policy_evict_first());
@@ -421,7 +426,8 @@ __device__ void sweep_producer_big(const SweepParams& p, SweepSmem& sm, WsHeader
       I.tailn = drop ? 0 : e1 - a1;
       I.sc = sc;
       I.slot = slot;
-      if (nb > 0) {
+      if (p.direct) I.flags |= kFlagDirect;
+      if (nb > 0 && !p.direct) {
         mbar_arrive_expect_tx(&sm.full[s], (uint32_t)nb);
         bulk_g2s_hint(sm.stage[s], src0 + off, (uint32_t)nb, &sm.full[s],
                       l2_policy_evict_first());
@@ -615,13 +621,23 @@ __device__ void sweep_consumers(SweepSmem& sm, WsHeader* h) {
       }
     }
     // Copy this thread's vectors out of the stage, then hand the stage back.
-    const uint4* buf = reinterpret_cast<const uint4*>(sm.stage[s]);
     const int nvec = I.nbytes >> 4;
     uint4 v[kVecPerThread];
+    if (I.flags & kFlagDirect) {
+      // Not copied: the same 16-byte aligned range, loaded from the row.
+      const uint4* src = reinterpret_cast<const uint4*>(row + I.elem0);
 #pragma unroll
-    for (int t = 0; t < kVecPerThread; ++t) {
-      const int j = ctid + t * kNCT;
-      v[t] = j < nvec ? buf[j] : neg_inf_vec<TIn>();
+      for (int t = 0; t < kVecPerThread; ++t) {
+        const int j = ctid + t * kNCT;
+        v[t] = j < nvec ? __ldg(src + j) : neg_inf_vec<TIn>();
+      }
+    } else {
+      const uint4* buf = reinterpret_cast<const uint4*>(sm.stage[s]);
+#pragma unroll
+      for (int t = 0; t < kVecPerThread; ++t) {
+        const int j = ctid + t * kNCT;
+        v[t] = j < nvec ? buf[j] : neg_inf_vec<TIn>();
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[s]);
