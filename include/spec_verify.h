@@ -35,13 +35,16 @@
  *     synchronises the stream except where stated.
  *   - The two logits buffers of the verification entry points (spec_verify,
  *     spec_verify_ex, spec_verify_timed, spec_verify_packed,
- *     spec_verify_static) may instead both be pinned host memory that the
- *     GPU maps (cudaHostAlloc, cudaHostRegister): the kernels then read the
- *     rows they need over the CPU-GPU link with plain loads, without a copy
- *     (early exit also spares the link the rows it skips); results are those
- *     of the same call on device-resident logits.  One buffer in host memory
- *     and the other not, or host memory the GPU does not map, is
- *     SPEC_ERR_INVALID_ARG.  Every other buffer is device memory.
+ *     spec_verify_static), and the logits of spec_row_stats, may instead be
+ *     pinned host memory that the GPU maps (cudaHostAlloc,
+ *     cudaHostRegister): the kernels then read the rows they need over the
+ *     CPU-GPU link with plain loads, without a copy (early exit also spares
+ *     the link the rows it skips); results are those of the same call on
+ *     device-resident logits.  One buffer in host memory and the other not,
+ *     or host memory the GPU does not map, is SPEC_ERR_INVALID_ARG.  The OPD
+ *     entry points (spec_opd_stats, spec_verify_opd) stream every row twice
+ *     and take device-resident logits only (host memory:
+ *     SPEC_ERR_INVALID_ARG).  Every other buffer is device memory.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Work is enqueued asynchronously on it.
  *   - Host-detectable argument errors return immediately and launch nothing.

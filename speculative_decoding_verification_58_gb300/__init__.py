@@ -446,9 +446,9 @@ def spec_row_stats(logits, temperature, *, stream=None):
     """
     torch = _torch()
     rows, V = logits.shape
-    dev = logits.device
+    dev = temperature.device
     dt = _dtype_code(logits)
-    _need(logits, "logits", logits.dtype, (rows, V), dev)
+    _need_logits(logits, "logits", logits.dtype, (rows, V), dev)
     _need(temperature, "temperature", torch.float32, (rows,), dev)
     n = int(lib().spec_row_stats_workspace_bytes(rows, V))
     if n == 0:
@@ -501,10 +501,11 @@ def spec_opd_stats(target_logits, draft_logits, lengths, *, delta: float = 0.01,
     torch = _torch()
     B, k1, V = target_logits.shape
     k = k1 - 1
-    dev = target_logits.device
+    dev = lengths.device
     dt = _dtype_code(target_logits)
-    _need(target_logits, "target_logits", target_logits.dtype, (B, k + 1, V), dev)
-    _need(draft_logits, "draft_logits", target_logits.dtype, (B, k, V), dev)
+    # Host-resident logits reach the library, which refuses them.
+    _need_logits(target_logits, "target_logits", target_logits.dtype, (B, k + 1, V), dev)
+    _need_logits(draft_logits, "draft_logits", target_logits.dtype, (B, k, V), dev)
     _need(lengths, "lengths", torch.int32, (B,), dev)
     if out is None:
         f = dict(dtype=torch.float32, device=dev)

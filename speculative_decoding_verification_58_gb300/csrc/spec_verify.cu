@@ -378,7 +378,7 @@ spec_status_t verify_typed(const void* target_logits, const void* draft_logits,
 template <typename TIn>
 spec_status_t row_stats_typed(const void* logits, int rows, int V, const float* temperature,
                               float* row_max, float* row_lse, int32_t* row_arg, void* workspace,
-                              cudaStream_t stream, int dtype_index) {
+                              cudaStream_t stream, int dtype_index, bool direct = false) {
   DeviceInfo* d = nullptr;
   if (device_info(&d) != cudaSuccess) return SPEC_ERR_CUDA;
   const int C = chunks_per_row(rows, V);
@@ -402,6 +402,7 @@ spec_status_t row_stats_typed(const void* logits, int rows, int V, const float* 
   sp.lay = lay;
   sp.rows_t = rows;
   sp.rows_d = rows;
+  sp.direct = direct ? 1 : 0;
   sp.parts_total = (long long)rows * nch;
   long long grid = (long long)d->sms * d->sweep_blocks_per_sm[dtype_index][0];
   if (grid > (long long)rows * nch) grid = (long long)rows * nch;
@@ -801,6 +802,13 @@ spec_status_t spec_opd_stats(const void* target_logits, const void* draft_logits
     return SPEC_ERR_INVALID_ARG;
   const bool vec_ok = aligned(target_logits, 16) && aligned(draft_logits, 16) &&
                       ((size_t)V * esize) % 16 == 0;
+  // The statistics stream every row twice through bulk copies: device memory only.
+  {
+    bool direct = false;
+    const void* t = target_logits;
+    const void* d = draft_logits;
+    if (!resolve_logits(&t, &d, &direct) || direct) return SPEC_ERR_INVALID_ARG;
+  }
   DeviceOf on_device(target_logits);
   if (!on_device.ok()) return SPEC_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -837,6 +845,13 @@ spec_status_t spec_verify_opd(const void* target_logits, const void* draft_logit
     return SPEC_ERR_WORKSPACE;
   const bool vec_ok = aligned(target_logits, 16) && aligned(draft_logits, 16) &&
                       ((size_t)V * esize) % 16 == 0;
+  // The statistics stream every row twice through bulk copies: device memory only.
+  {
+    bool direct = false;
+    const void* t = target_logits;
+    const void* d = draft_logits;
+    if (!resolve_logits(&t, &d, &direct) || direct) return SPEC_ERR_INVALID_ARG;
+  }
   DeviceOf on_device(target_logits);
   if (!on_device.ok()) return SPEC_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -902,14 +917,17 @@ spec_status_t spec_row_stats(const void* logits, spec_dtype_t dtype, int rows, i
   if (!workspace || !aligned(workspace, 256) ||
       workspace_bytes < spec_row_stats_workspace_bytes(rows, V))
     return SPEC_ERR_WORKSPACE;
-  DeviceOf on_device(logits);
+  DeviceOf on_device(workspace);
   if (!on_device.ok()) return SPEC_ERR_CUDA;
+  bool direct = false;
+  const void* unused = logits;
+  if (!resolve_logits(&logits, &unused, &direct)) return SPEC_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == SPEC_F32)
     return row_stats_typed<float>(logits, rows, V, temperature, row_max, row_lse, row_arg, workspace,
-                                  s, 0);
+                                  s, 0, direct);
   return row_stats_typed<uint16_t>(logits, rows, V, temperature, row_max, row_lse, row_arg,
-                                   workspace, s, 1);
+                                   workspace, s, 1, direct);
 }
 
 }  // extern "C"

@@ -85,3 +85,20 @@ def test_mixed_or_pageable_placements_are_refused():
     pageable = dict(d, target_logits=d["target_logits"].cpu(), draft_logits=d["draft_logits"].cpu())
     with pytest.raises(ValueError):
         sv.spec_verify(**pageable)
+
+
+def test_row_stats_read_host_logits_and_opd_refuses_them():
+    inp = synth.make_inputs("zipf_mixed_temp", 8, 4, 4096, "bf16", seed=5)
+    d = sv.to_device(inp)
+    rows = d["target_logits"].reshape(-1, inp.V)
+    temp = torch.from_numpy(np.tile(np.array([0.0, 0.7, 1.0, 1.3], np.float32),
+                                    rows.shape[0] // 4 + 1)[:rows.shape[0]]).cuda()
+    mx_d, lse_d, arg_d = sv.spec_row_stats(rows, temp)
+    mx_h, lse_h, arg_h = sv.spec_row_stats(_pinned(rows), temp)
+    torch.cuda.synchronize()
+    greedy = temp == 0
+    assert torch.equal(mx_h, mx_d) and torch.equal(arg_h, arg_d)
+    assert torch.equal(lse_h[~greedy], lse_d[~greedy])  # NaN on greedy rows
+    with pytest.raises(sv.SpecVerifyError) as e:
+        sv.spec_opd_stats(_pinned(d["target_logits"]), _pinned(d["draft_logits"]), d["lengths"])
+    assert e.value.code == sv.SPEC_ERR_INVALID_ARG
