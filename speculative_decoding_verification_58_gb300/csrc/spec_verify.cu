@@ -296,6 +296,9 @@ cudaError_t launch_final(const DeviceInfo* d, const void* target_logits, const v
                 fp);
 }
 
+// Sweep CTAs for rows in host memory: the SM count divided by this.
+constexpr int kDirectSweepDivisor = 4;
+
 // Launch the verification sweep (persistent, a multiple of the SM count);
 // *grid_out: its CTAs.
 template <typename TIn>
@@ -323,7 +326,12 @@ cudaError_t launch_sweep(const DeviceInfo* d, const void* target_logits, const v
   sp.direct = direct ? 1 : 0;
   sp.parts_total = 2LL * B * k * nch;
   const long long max_units = 2LL * B * k * nch;
-  long long grid = (long long)d->sms * d->sweep_blocks_per_sm[dtype_index][1];
+  // Rows in host memory arrive at the link's rate, which a fraction of the
+  // SMs saturates with their loads: fewer CTAs keep fewer units in flight,
+  // so the claim front runs less far past the decisions and fewer rows
+  // behind a rejection cross the link.
+  long long grid = direct ? (long long)d->sms / kDirectSweepDivisor
+                          : (long long)d->sms * d->sweep_blocks_per_sm[dtype_index][1];
   if (grid > max_units) grid = max_units;
   if (grid < 1) grid = 1;
   *grid_out = (int)grid;
