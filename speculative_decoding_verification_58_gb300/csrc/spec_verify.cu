@@ -332,6 +332,17 @@ cudaError_t launch_sweep(const DeviceInfo* d, const void* target_logits, const v
   // behind a rejection cross the link.
   long long grid = direct ? (long long)d->sms / kDirectSweepDivisor
                           : (long long)d->sms * d->sweep_blocks_per_sm[dtype_index][1];
+  // A work list much longer than one wave of CTAs (mid-size batches: 32
+  // requests are 16 positions of 128 units for 456 CTAs) is claimed nearly
+  // whole at once, far ahead of the decisions; at most two positions' units
+  // in flight (but every SM busy) keep the claim front near the decisions,
+  // so fewer rows behind a rejection are read (32 requests: 112 MB a round
+  // instead of 149, 49.4 µs instead of 51.4).  Small batches keep every unit
+  // in flight: their rounds are latency chains.
+  if (!direct && max_units > 2 * grid) {
+    const long long per_position = 2LL * B * nch;
+    grid = std::min(grid, std::max((long long)d->sms, 2 * per_position));
+  }
   if (grid > max_units) grid = max_units;
   if (grid < 1) grid = 1;
   *grid_out = (int)grid;
