@@ -798,6 +798,32 @@ class OurArm:
                       "logit_bytes_read": read, "same_outputs": same_direct}
         padded_leg = {"value": self.world / padded_s, "unit": "rounds/s", "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h, "layout": "padded [B, k+1, V] / [B, k, V]"}
+
+        # The padded buffers left in pinned host memory, read in place.
+        psmall = ("draft_tokens", "lengths", "uniforms", "temperature")
+
+        def padded_direct_step():
+            for key in psmall:
+                d[key].copy_(host[key], non_blocking=True)
+            sv.spec_verify(host["target_logits"], host["draft_logits"],
+                           **{key: d[key] for key in psmall}, workspace=self.ws,
+                           out_tokens=self.out, num_accepted=self.nacc, stream=self.stream)
+            h_out.copy_(self.out, non_blocking=True)
+            h_n.copy_(self.nacc, non_blocking=True)
+            self.stream.synchronize()
+
+        padded_direct_step()
+        same_pd = bool(np.array_equal(h_out.numpy(), self.gpu_out) and
+                       np.array_equal(h_n.numpy(), self.gpu_n))
+        rep = sv.spec_verify_report(self.ws, stream=self.stream)
+        read_pd = int(rep.sweep_bytes) + int(rep.final_bytes)
+        pd_s = timed(padded_direct_step)
+        padded_leg["direct"] = {
+            "value": self.world / pd_s, "unit": "rounds/s",
+            "h2d_bytes_per_step": read_pd + sum(host[key].numel() * host[key].element_size()
+                                                for key in psmall),
+            "d2h_bytes_per_step": d2h, "logit_bytes_read": read_pd, "same_outputs": same_pd,
+            "layout": "padded buffers in pinned host memory, read in place over the link"}
         return direct_leg, copy_leg, padded_leg
 
     def cpu_baseline(self, result, round_bytes):
