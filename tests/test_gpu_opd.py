@@ -197,6 +197,22 @@ def test_opd_special_cases():
     assert np.all(g["x_star"][5] == -1) and np.isnan(g["loss"][5])
 
 
+@pytest.mark.parametrize("shift", [12.0, -9.0])
+def test_opd_shifted_draft_logits(shift):
+    """Logits are defined up to a constant per row: a draft row shifted by a
+    large constant has the same q.  Every term q (dz - c) then holds the shift
+    twice, in dz = z_d - z_t and in c = lse_d - lse_t, so this checks that the
+    divergence, small here, is not lost to the large parts that cancel."""
+    rng = np.random.default_rng(int(abs(shift)) + 30)
+    B, k, V = 4, 4, 151936
+    t = (rng.standard_normal((B, k + 1, V)) * 1.5).astype(np.float32)
+    d = (t[:, :k] + rng.standard_normal((B, k, V)).astype(np.float32) * np.float32(0.05)
+         + np.float32(shift)).astype(np.float32)
+    inp = synth.SpecInputs(t, d, np.zeros((B, k), np.int32), np.array([4, 3, 2, 1], np.int32),
+                           np.zeros((B, k + 1), np.float32), np.ones(B, np.float32), "f32")
+    check(inp, f"draft shifted by {shift}")
+
+
 def test_opd_host_checks():
     d = sv.to_device(synth.make_inputs("gauss", 2, 3, 64, "f32", seed=1))
     for kw in (dict(delta=0.0), dict(delta=float("inf")), dict(alpha=1.5), dict(alpha=-0.1)):
