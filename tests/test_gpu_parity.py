@@ -164,6 +164,47 @@ def test_p_equals_q_always_accepts(dtype):
     check(inp, "p == q")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("T", [1e-3, 0.05, 0.2, 8.0, 100.0])
+def test_extreme_temperatures_match_oracle(dtype, T):
+    """Every request at one temperature far from 1: at T = 1e-3 both rows are
+    nearly one-hot (scaled logits in the thousands of bits), at T = 100 both
+    are nearly uniform and the residual max(0, p - q) is small.  Each draft
+    token is drawn from q at the request's own temperature (Gumbel-max on
+    the stored draft logits), as a drafter sampling at T would; one position
+    per request carries the uniform 0.999 so that rejections, and with them
+    the residual draw, happen at every temperature.  (A token the drafter
+    gives almost no probability can leave a residual below what single or
+    double precision resolves; such draws are decided by rounding on both
+    sides and are not what this test compares.)"""
+    B, k, V = 48, 6, 20000
+    inp = synth.make_inputs("zipf_mixed_noise", B, k, V, dtype, seed=int(T * 1000) % 9973 + 7)
+    inp.temperature[:] = np.float32(T)
+    rng = np.random.default_rng(12)
+    zd = (inp.draft.astype(np.uint32) << 16).view(np.float32) if dtype == "bf16" else inp.draft
+    g = rng.gumbel(size=zd.shape)
+    inp.tokens[:] = np.argmax(zd.astype(np.float64) / np.float64(np.float32(T)) + g,
+                              axis=2).astype(np.int32)
+    forced = rng.integers(0, k, size=B)
+    inp.uniforms[np.arange(B), forced] = np.float32(0.999)
+    info, rep, o = check(inp, f"T={T} {dtype}")
+    rejected = o.num_accepted < inp.lengths
+    assert np.sum(rejected) >= 10, "too few rejections to exercise the residual"
+    assert rep.residual_zero == 0, rep
+
+
+def test_logits_far_from_zero_match_oracle():
+    """Softmax is shift-invariant, and the kernels subtract row maxima in
+    scaled form: target rows shifted by +3000 and draft rows by -2000 (fp32,
+    so that the shifted values are what both sides read) must still give the
+    oracle's outputs, at mixed temperatures and with greedy requests."""
+    inp = synth.make_inputs("zipf_mixed_temp", 40, 8, 30000, "f32", seed=314)
+    inp.target[:] = (inp.target + np.float32(3000.0)).astype(np.float32)
+    inp.draft[:] = (inp.draft - np.float32(2000.0)).astype(np.float32)
+    info, rep, o = check(inp, "shifted logits")
+    assert np.sum(o.num_accepted < inp.lengths) >= 5
+
+
 def test_single_token_vocabulary():
     inp = _inputs(4, 3, 1)
     inp.tokens[:] = 0
