@@ -281,6 +281,52 @@ def test_residual_mass_is_total_variation():
         assert abs(r.final_mass[b] - tv) < 1e-12
 
 
+@pytest.mark.parametrize("T", [0.05, 0.2, 8.0, 100.0])
+def test_residual_draw_matches_extended_precision(T):
+    """The residual draw (AdaFlash Section 2.1: a token from
+    normalize(max(0, p - q)) by inverse CDF with u_L) recomputed in 50-digit
+    arithmetic from the same float32 logits and temperature: nearly one-hot
+    rows at T = 0.05, nearly uniform ones at T = 100.  Position 0 is
+    rejected by construction (the token with the smallest p/q, u = 0.999999);
+    a draw whose u_L * TV lies within 1e-9 of a CDF edge is skipped."""
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 50
+    rng = np.random.default_rng(int(T * 100) + 3)
+    B, k, V = 30, 2, 200
+    tl = (rng.standard_normal((B, k + 1, V)) * 2).astype(np.float32)
+    dl = (tl[:, :k] + rng.standard_normal((B, k, V)) * 0.5).astype(np.float32)
+    Tf = np.float32(T)
+    tok = np.zeros((B, k), np.int32)
+    for b in range(B):
+        p, q = softmax(tl[b, 0], Tf), softmax(dl[b, 0], Tf)
+        tok[b, 0] = int(np.argmax(q / p))
+    u = np.full((B, k + 1), 0.999999, np.float32)
+    u[:, k] = rng.random(B).astype(np.float32)
+    r = oracle.verify(tl, dl, tok, np.full(B, k, np.int32), u, np.full(B, Tf, np.float32))
+    assert np.all(r.num_accepted == 0)
+    checked = 0
+    for b in range(B):
+        Tm = mp.mpf(float(Tf))
+        et = [mp.exp(mp.mpf(float(z)) / Tm) for z in tl[b, 0]]
+        ed = [mp.exp(mp.mpf(float(z)) / Tm) for z in dl[b, 0]]
+        st, sd = mp.fsum(et), mp.fsum(ed)
+        res = [max(mp.mpf(0), a / st - c / sd) for a, c in zip(et, ed)]
+        tv = mp.fsum(res)
+        target = mp.mpf(float(u[b, k])) * tv
+        acc, want, edge = mp.mpf(0), None, None
+        for y, w in enumerate(res):
+            if acc + w > target:
+                want, edge = y, min(target - acc, acc + w - target)
+                break
+            acc += w
+        if want is None or edge < mp.mpf("1e-9") * tv:
+            continue
+        assert r.out_tokens[b, 0] == want, (T, b)
+        assert abs(r.final_mass[b] - float(tv)) <= 1e-12 * max(1.0, float(tv)) + 1e-300
+        checked += 1
+    assert checked >= B - 2
+
+
 def test_disjoint_supports_reject_and_resample_target():
     rng = np.random.default_rng(9)
     B, k, V = 200, 2, 16
