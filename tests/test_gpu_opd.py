@@ -213,6 +213,23 @@ def test_opd_shifted_draft_logits(shift):
     check(inp, f"draft shifted by {shift}")
 
 
+def test_opd_sharply_peaked_rows():
+    """Logits scaled so that p and q are nearly one-hot: where the two
+    argmaxes differ the reverse KL and the hard-label term reach tens of nats
+    and a few entries carry them; a row pair that differs only by a shift
+    has no divergence."""
+    rng = np.random.default_rng(77)
+    B, k, V = 6, 4, 30000
+    t = (rng.standard_normal((B, k + 1, V)) * 40).astype(np.float32)
+    d = (t[:, :k] + rng.standard_normal((B, k, V)).astype(np.float32) * np.float32(8)).astype(
+        np.float32)
+    d[0] = t[0, :k] + np.float32(0.5)  # same argmaxes, shifted rows: divergence 0
+    inp = synth.SpecInputs(t, d, np.zeros((B, k), np.int32), np.full(B, k, np.int32),
+                           np.zeros((B, k + 1), np.float32), np.ones(B, np.float32), "f32")
+    g, o = check(inp, "peaked rows")
+    assert np.max(o.rkl) > 10 and np.max(o.hard) > 10
+
+
 def test_opd_host_checks():
     d = sv.to_device(synth.make_inputs("gauss", 2, 3, 64, "f32", seed=1))
     for kw in (dict(delta=0.0), dict(delta=float("inf")), dict(alpha=1.5), dict(alpha=-0.1)):

@@ -193,15 +193,22 @@ def test_extreme_temperatures_match_oracle(dtype, T):
     assert rep.residual_zero == 0, rep
 
 
-def test_logits_far_from_zero_match_oracle():
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_logits_far_from_zero_match_oracle(dtype):
     """Softmax is shift-invariant, and the kernels subtract row maxima in
-    scaled form: target rows shifted by +3000 and draft rows by -2000 (fp32,
-    so that the shifted values are what both sides read) must still give the
-    oracle's outputs, at mixed temperatures and with greedy requests."""
+    scaled form: target rows shifted by +3000 and draft rows by -2000 must
+    still give the oracle's outputs, at mixed temperatures and with greedy
+    requests.  The shifted values are stored in the call's dtype (in bf16
+    they lie 16 apart, so the rows become sharply peaked), and both sides
+    read exactly those values."""
     inp = synth.make_inputs("zipf_mixed_temp", 40, 8, 30000, "f32", seed=314)
-    inp.target[:] = (inp.target + np.float32(3000.0)).astype(np.float32)
-    inp.draft[:] = (inp.draft - np.float32(2000.0)).astype(np.float32)
-    info, rep, o = check(inp, "shifted logits")
+    t = (inp.target + np.float32(3000.0)).astype(np.float32)
+    d = (inp.draft - np.float32(2000.0)).astype(np.float32)
+    if dtype == "bf16":
+        inp.target, inp.draft, inp.dtype = synth.bf16_bits(t), synth.bf16_bits(d), "bf16"
+    else:
+        inp.target, inp.draft = t, d
+    info, rep, o = check(inp, f"shifted logits {dtype}")
     assert np.sum(o.num_accepted < inp.lengths) >= 5
 
 
